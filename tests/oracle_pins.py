@@ -1,0 +1,286 @@
+"""Pins for the fp64 oracle: checks against facts that do not come from the
+oracle itself.  Each pin takes ``scan(u, delta, A, B, C, D, z, delta_bias,
+softplus) -> (y, h_last)`` and returns the largest error it saw, so the same
+pins run against the committed oracle (tests/test_oracle_pins.py) and against
+deliberately broken copies of it (tests/test_oracle_mutants.py).
+
+What each pin rests on:
+  bruteforce      the unrolled closed form of the linear recurrence,
+                  y_t = sum_{s<=t} sum_n C_t[n] exp(A[n] * sum_{r=s+1..t} dt_r)
+                        dt_s B_s[n] u_s + D u_t, evaluated in 40-digit mpmath
+                  with softplus and SiLU from their textbook definitions
+                  ("State Space Models (SSM)" summary page, section 3.2, and
+                  the recurrence/readout of section 1.2).
+  lti_direct /    time-invariant delta, B, C: y = u * K with
+  lti_fft         K_k = sum_n C[n] exp(k dt A[n]) dt B[n] (the convolution
+                  kernel K = (C B, C A B, C A^2 B, ...) of the itwiki page's
+                  "순환 형태와 합성곱 형태" section, with the diagonal-A
+                  Vandermonde form of the youngju.dev S4Layer listing),
+                  convolved directly and through a zero-padded FFT.
+  associativity   splitting the sequence anywhere and composing the two
+                  halves' (decay, state) pairs gives the full result (the
+                  associative-scan property of the Obsidian "Mamba" note, 5.1).
+  special cases   N = 1, L = 1 scalar recurrence; A = 0 (prefix sum); C = 0
+                  (y = D u gate); delta = 0 on a suffix keeps the state
+                  (itwiki "Mamba의 선택 메커니즘": small Delta keeps the state);
+                  z = 0 gives y = 0; A < 0, delta > 0 keeps h bounded.
+  golden          tests/golden/hand_worked.json, worked by hand.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import mpmath
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "hand_worked.json")
+
+
+def _rel_err(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if got.shape != ref.shape:
+        return float("inf")
+    if got.size == 0:
+        return 0.0
+    return float(np.max(np.abs(got - ref) / (1.0 + np.abs(ref))))
+
+
+def random_problem(rng, batch, L, dim, N, softplus=True, bias=True, gate=True, skip=True,
+                   a_neg=True):
+    u = rng.standard_normal((batch, L, dim))
+    if softplus:
+        delta = rng.standard_normal((batch, L, dim)) - 1.0
+    else:
+        delta = np.exp(rng.uniform(np.log(1e-2), np.log(5e-1), size=(batch, L, dim)))
+    A = -np.exp(rng.uniform(-1.0, 1.5, size=(dim, N))) if a_neg else rng.standard_normal((dim, N))
+    B = rng.standard_normal((batch, L, N))
+    C = rng.standard_normal((batch, L, N))
+    D = rng.standard_normal(dim) if skip else None
+    z = rng.standard_normal((batch, L, dim)) if gate else None
+    db = 0.5 * rng.standard_normal(dim) if bias else None
+    return dict(u=u, delta=delta, A=A, B=B, C=C, D=D, z=z, delta_bias=db, softplus=softplus)
+
+
+def _call(scan, p):
+    return scan(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
+                p["delta_bias"], p["softplus"])
+
+
+# ---------------------------------------------------------------- brute force
+def bruteforce(p, dps=40):
+    """Unrolled closed form in high precision (see module docstring)."""
+    mpmath.mp.dps = dps
+    u, delta, A, B, C = p["u"], p["delta"], p["A"], p["B"], p["C"]
+    D, z, db, sp = p["D"], p["z"], p["delta_bias"], p["softplus"]
+    batch, L, dim = u.shape
+    N = A.shape[1]
+    y = np.zeros((batch, L, dim))
+    h = np.zeros((batch, dim, N))
+    mpf = mpmath.mpf
+    for b in range(batch):
+        for d in range(dim):
+            dts = []
+            for t in range(L):
+                x = mpf(float(delta[b, t, d])) + (mpf(float(db[d])) if db is not None else 0)
+                if sp:
+                    x = mpmath.log(1 + mpmath.exp(x))       # softplus, textbook form
+                dts.append(x)
+            for t in range(L):
+                acc = mpf(0)
+                for s in range(t + 1):
+                    tail = sum(dts[s + 1:t + 1], mpf(0))     # sum of dt over (s, t]
+                    for n in range(N):
+                        a = mpf(float(A[d, n]))
+                        acc += (mpf(float(C[b, t, n])) * mpmath.exp(a * tail) * dts[s]
+                                * mpf(float(B[b, s, n])) * mpf(float(u[b, s, d])))
+                if D is not None:
+                    acc += mpf(float(D[d])) * mpf(float(u[b, t, d]))
+                if z is not None:
+                    zz = mpf(float(z[b, t, d]))
+                    acc *= zz / (1 + mpmath.exp(-zz))
+                y[b, t, d] = float(acc)
+            for n in range(N):
+                a = mpf(float(A[d, n]))
+                hn = mpf(0)
+                for s in range(L):
+                    tail = sum(dts[s + 1:L], mpf(0))
+                    hn += (mpmath.exp(a * tail) * dts[s] * mpf(float(B[b, s, n]))
+                           * mpf(float(u[b, s, d])))
+                h[b, d, n] = float(hn)
+    return y, h
+
+
+def pin_bruteforce(scan, seed=0):
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for kw in (dict(),
+               dict(softplus=False, bias=False, gate=False, skip=False),
+               dict(softplus=True, bias=False, gate=True, skip=False),
+               dict(softplus=False, bias=True, gate=False, skip=True, a_neg=False)):
+        p = random_problem(rng, batch=2, L=6, dim=3, N=5, **kw)
+        y, h = _call(scan, p)
+        yr, hr = bruteforce(p)
+        worst = max(worst, _rel_err(y, yr), _rel_err(h, hr))
+    return worst
+
+
+# ---------------------------------------------------------------- time-invariant
+def _lti_problem(rng, batch=2, L=384, dim=5, N=16, skip=False):
+    dt = np.exp(rng.uniform(np.log(1e-3), np.log(1e-1), size=dim))
+    A = -np.broadcast_to(np.arange(1, N + 1, dtype=np.float64), (dim, N)).copy()
+    A[1] *= 0.37                      # one channel with a non-integer spectrum
+    bvec = rng.standard_normal(N)
+    cvec = rng.standard_normal(N)
+    u = rng.standard_normal((batch, L, dim))
+    p = dict(u=u, delta=np.broadcast_to(dt, (batch, L, dim)).copy(), A=A,
+             B=np.broadcast_to(bvec, (batch, L, N)).copy(),
+             C=np.broadcast_to(cvec, (batch, L, N)).copy(),
+             D=(np.linspace(0.5, 1.5, dim) if skip else None), z=None, delta_bias=None,
+             softplus=False)
+    return p, dt, bvec, cvec
+
+
+def lti_kernel(dt, A, bvec, cvec, L):
+    """K[d, k] = sum_n C[n] exp(k dt_d A[d,n]) dt_d B[n]  (Vandermonde form)."""
+    k = np.arange(L, dtype=np.float64)
+    # (dim, N, L) powers exp(k * dt * A)
+    pw = np.exp(dt[:, None, None] * A[:, :, None] * k[None, None, :])
+    return np.einsum("n,dnl->dl", cvec * bvec, pw) * dt[:, None]
+
+
+def pin_lti_direct(scan, seed=1, skip=False):
+    rng = np.random.default_rng(seed)
+    p, dt, bvec, cvec = _lti_problem(rng, skip=skip)
+    y, _ = _call(scan, p)
+    batch, L, dim = p["u"].shape
+    K = lti_kernel(dt, p["A"], bvec, cvec, L)
+    yr = np.zeros_like(y)
+    for b in range(batch):
+        for d in range(dim):
+            yr[b, :, d] = np.convolve(p["u"][b, :, d], K[d])[:L]
+    if p["D"] is not None:
+        yr += p["D"][None, None, :] * p["u"]
+    return _rel_err(y, yr)
+
+
+def pin_lti_fft(scan, seed=2):
+    rng = np.random.default_rng(seed)
+    p, dt, bvec, cvec = _lti_problem(rng, L=1000)
+    y, _ = _call(scan, p)
+    batch, L, dim = p["u"].shape
+    K = lti_kernel(dt, p["A"], bvec, cvec, L)
+    kf = np.fft.rfft(K, n=2 * L, axis=-1)                          # (dim, L+1)
+    uf = np.fft.rfft(np.transpose(p["u"], (0, 2, 1)), n=2 * L, axis=-1)
+    yr = np.fft.irfft(uf * kf[None], n=2 * L, axis=-1)[..., :L]
+    yr = np.transpose(yr, (0, 2, 1))
+    return _rel_err(y, yr)
+
+
+# ---------------------------------------------------------------- associativity
+def pin_associativity(scan, seed=3):
+    """Run [0, s) and [s, L) separately from zero state; compose with the
+    decay exp(A * sum of dt over [s, t]) of the prefix state."""
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for split in (1, 7, 16):
+        p = random_problem(rng, batch=2, L=23, dim=4, N=6, gate=False, skip=False)
+        y, h = _call(scan, p)
+        pre = {k: (v[:, :split] if isinstance(v, np.ndarray) and v.ndim == 3 else v)
+               for k, v in p.items()}
+        suf = {k: (v[:, split:] if isinstance(v, np.ndarray) and v.ndim == 3 else v)
+               for k, v in p.items()}
+        yp, hp = _call(scan, pre)
+        ys, hs = _call(scan, suf)
+        dt = p["delta"] + (p["delta_bias"][None, None, :] if p["delta_bias"] is not None else 0)
+        dt = np.logaddexp(0.0, dt) if p["softplus"] else dt          # (batch, L, dim)
+        cum = np.cumsum(dt[:, split:], axis=1)                        # (batch, Ls, dim)
+        decay = np.exp(cum[..., None] * p["A"][None, None])           # (batch, Ls, dim, N)
+        carry = np.einsum("btn,btdn,bdn->btd", p["C"][:, split:], decay, hp)
+        worst = max(worst, _rel_err(y[:, :split], yp), _rel_err(y[:, split:], ys + carry),
+                    _rel_err(h, hs + decay[:, -1] * hp))
+    return worst
+
+
+# ---------------------------------------------------------------- special cases
+def pin_special_cases(scan, seed=4):
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    # N = 1, L = 1: y = C dt B u + D u, h = dt B u
+    p = random_problem(rng, 3, 1, 2, 1, softplus=False, bias=False, gate=False)
+    y, h = _call(scan, p)
+    dt = p["delta"][:, 0, :]
+    hr = dt * p["B"][:, 0, :] * p["u"][:, 0, :]
+    worst = max(worst, _rel_err(h[:, :, 0], hr),
+                _rel_err(y[:, 0, :], p["C"][:, 0, :] * hr + p["D"] * p["u"][:, 0, :]))
+    # A = 0: the state is the running sum of dt B u
+    p = random_problem(rng, 2, 9, 3, 4, softplus=True, gate=False, skip=False)
+    p["A"] = np.zeros_like(p["A"])
+    y, h = _call(scan, p)
+    dt = np.logaddexp(0.0, p["delta"] + p["delta_bias"])
+    hs = np.cumsum(dt[..., None] * p["B"][:, :, None, :] * p["u"][..., None], axis=1)
+    worst = max(worst, _rel_err(h, hs[:, -1]),
+                _rel_err(y, np.einsum("btn,btdn->btd", p["C"], hs)))
+    # C = 0: y = D u silu(z)
+    p = random_problem(rng, 2, 5, 3, 4)
+    p["C"] = np.zeros_like(p["C"])
+    y, _ = _call(scan, p)
+    zz = p["z"]
+    worst = max(worst, _rel_err(y, p["D"] * p["u"] * zz / (1 + np.exp(-zz))))
+    # z = 0: the gate closes
+    p = random_problem(rng, 2, 5, 3, 4)
+    p["z"] = np.zeros_like(p["z"])
+    y, _ = _call(scan, p)
+    worst = max(worst, float(np.max(np.abs(y))))
+    # delta = 0 on a suffix keeps the state (no softplus), and a softplus input
+    # driven to -1e4 (softplus -> 0) does the same
+    for sp in (False, True):
+        p = random_problem(rng, 2, 12, 3, 4, softplus=sp, bias=False, gate=False)
+        _, h_pre = _call(scan, {**p, "u": p["u"][:, :8], "delta": p["delta"][:, :8],
+                                "B": p["B"][:, :8], "C": p["C"][:, :8]})
+        p["delta"][:, 8:] = -1e4 if sp else 0.0
+        _, h = _call(scan, p)
+        worst = max(worst, _rel_err(h, h_pre))
+    # A < 0, delta > 0: |h[n]| <= max|dt B u| / (1 - max exp(dt A))
+    p = random_problem(rng, 2, 200, 3, 4, softplus=False, bias=False, gate=False)
+    _, h = _call(scan, p)
+    dt = p["delta"]
+    dbu = np.abs(dt[..., None] * p["B"][:, :, None, :] * p["u"][..., None])   # (b,t,d,n)
+    da = np.exp(dt[..., None] * p["A"][None, None])
+    bound = dbu.max(axis=1) / (1.0 - da.max(axis=1))
+    excess = np.max(np.abs(h) - bound)
+    worst = max(worst, 0.0 if excess <= 0 else float(excess) + 1.0)
+    return worst
+
+
+# ---------------------------------------------------------------- golden
+def _ev(x):
+    if isinstance(x, str):
+        return eval(x, {"__builtins__": {}}, {"ln2": math.log(2.0), "ln3": math.log(3.0)})
+    if isinstance(x, list):
+        return [_ev(v) for v in x]
+    return x
+
+
+def pin_golden(scan):
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    worst = 0.0
+    for c in cases:
+        arr = lambda k: None if c[k] is None else np.array(_ev(c[k]), dtype=np.float64)
+        y, h = scan(arr("u"), arr("delta"), arr("A"), arr("B"), arr("C"), arr("D"), arr("z"),
+                    arr("delta_bias"), c["softplus"])
+        worst = max(worst, _rel_err(y, arr("y")), _rel_err(h, arr("h_last")))
+    return worst
+
+
+ALL_PINS = {
+    "bruteforce": (pin_bruteforce, 1e-12),
+    "lti_direct": (pin_lti_direct, 1e-9),
+    "lti_fft": (pin_lti_fft, 1e-9),
+    "associativity": (pin_associativity, 1e-12),
+    "special_cases": (pin_special_cases, 1e-12),
+    "golden": (pin_golden, 1e-14),
+}

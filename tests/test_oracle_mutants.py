@@ -1,0 +1,70 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch every one (the committed oracle is never modified)."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+from tests.oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "ssm_oracle.c")
+
+MUTANTS = {
+    "dA_sign": ("exp(dt * A[d * N + n])", "exp(-dt * A[d * N + n])"),
+    "dBu_drops_dt": ("dt * B[i_bln + n] * x", "B[i_bln + n] * x"),
+    "readout_uses_B": ("acc += C[i_bln + n] * h[n]", "acc += B[i_bln + n] * h[n]"),
+    "A_transposed": ("A[d * N + n]", "A[n * dim + d]"),
+    "skip_dropped": ("acc += D[d] * x;", "acc += 0.0 * x;"),
+    "skip_on_dt": ("acc += D[d] * x;", "acc += D[d] * dt;"),
+    "bias_dropped": ("dt += delta_bias[d];", "dt += 0.0;"),
+    "bias_after_softplus": ("""                if (delta_bias)
+                    dt += delta_bias[d];
+                if (softplus_flag)
+                    dt = softplus(dt);""", """                if (softplus_flag)
+                    dt = softplus(dt);
+                if (delta_bias)
+                    dt += delta_bias[d];"""),
+    "gate_sigmoid_only": ("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
+    "softplus_wrong": ("return log1p(exp(x));", "return exp(x);"),
+    "readout_before_update": ("""                    h[n] = dA * h[n] + dBu;
+                    acc += C[i_bln + n] * h[n];""", """                    acc += C[i_bln + n] * h[n];
+                    h[n] = dA * h[n] + dBu;"""),
+    "state_not_reset": ("""            for (int64_t n = 0; n < N; ++n)
+                h[n] = 0.0;
+""", ""),
+    "B_index_uses_t_minus_1": ("B[i_bln + n]", "B[(i_bln >= N ? i_bln - N : i_bln) + n]"),
+}
+
+
+@pytest.fixture(scope="module")
+def tmpdir_mod(tmp_path_factory):
+    return tmp_path_factory.mktemp("mutants")
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmpdir_mod):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert old in src, f"mutation anchor for {name} not found"
+    msrc = src.replace(old, new)
+    cfile = os.path.join(tmpdir_mod, f"{name}.c")
+    sofile = os.path.join(tmpdir_mod, f"lib{name}.so")
+    with open(cfile, "w") as f:
+        f.write(msrc)
+    oracle.build(force=True, src=cfile, out=sofile)
+    lib = oracle.load(sofile)
+
+    def scan(*a):
+        return oracle.selective_scan_fwd(*a, lib=lib)
+
+    failures = []
+    for pname, (fn, tol) in ALL_PINS.items():
+        try:
+            err = fn(scan)
+        except Exception:           # a crash or a shape error also counts as caught
+            err = float("inf")
+        if not (err <= tol):
+            failures.append(pname)
+    assert failures, f"mutant {name} passed every pin"

@@ -1,0 +1,50 @@
+"""The fp64 oracle against what the pages and the mathematics fix (see
+tests/oracle_pins.py for what each pin rests on).  CPU only."""
+import numpy as np
+import pytest
+
+import oracle
+from tests.oracle_pins import ALL_PINS
+
+
+@pytest.mark.parametrize("name", sorted(ALL_PINS))
+def test_oracle_pin(name):
+    fn, tol = ALL_PINS[name]
+    err = fn(oracle.selective_scan_fwd)
+    assert err <= tol, f"{name}: error {err:.3e} > {tol:.1e}"
+
+
+def test_oracle_lti_with_skip():
+    from tests.oracle_pins import pin_lti_direct
+    assert pin_lti_direct(oracle.selective_scan_fwd, seed=5, skip=True) <= 1e-9
+
+
+def test_oracle_threaded_split_is_identical():
+    rng = np.random.default_rng(9)
+    from tests.oracle_pins import random_problem
+    p = random_problem(rng, 2, 17, 11, 4)
+    args = (p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"], p["delta_bias"],
+            p["softplus"])
+    y1, h1 = oracle.selective_scan_fwd(*args)
+    y4, h4 = oracle.selective_scan_fwd_threads(*args, threads=4)
+    assert np.array_equal(y1, y4) and np.array_equal(h1, h4)
+
+
+def test_oracle_empty_and_degenerate_sizes():
+    A = -np.ones((3, 2))
+    for L in (0, 1):
+        u = np.ones((2, L, 3)); B = np.ones((2, L, 2))
+        y, h = oracle.selective_scan_fwd(u, u, A, B, B)
+        assert y.shape == (2, L, 3) and h.shape == (2, 3, 2)
+        if L == 0:
+            assert not np.any(h)
+    # zero batch / zero channels
+    y, h = oracle.selective_scan_fwd(np.ones((0, 4, 3)), np.ones((0, 4, 3)), A,
+                                     np.ones((0, 4, 2)), np.ones((0, 4, 2)))
+    assert y.shape == (0, 4, 3)
+
+
+def test_oracle_rejects_bad_arguments():
+    lib = oracle.load()
+    assert lib.ssm_oracle_fwd(None, None, None, None, None, None, None, None, 0,
+                              None, None, 1, 1, 1, 1) == -1
