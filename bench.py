@@ -1,0 +1,465 @@
+#!/usr/bin/env python
+"""Selective-scan forward throughput on one (or N) B300 GPUs.
+
+One step = one call of the fused selective-scan forward (discretise, scan,
+readout, gate) over one batch of seeded synthetic input of the workload: by
+default the Mamba-130M-layer shape (batch 8, L 2048, dim 1536, N 16, bf16
+inputs and output, fp32 state, softplus + bias, SiLU gate).  Prints ONE JSON
+line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--all]
+
+Under torchrun (N > 1) every rank runs its own full-size replica of the
+workload on its GPU (weak scaling; the path shards over batch rows with no
+exchange), the timed region is bracketed by a barrier and a device
+synchronise, and the slowest rank's time is used.
+
+Token = one (batch row, step) pair: tokens per step = batch * L, the tokens/s
+convention of the pages' benchmark_inference harness (youngju.dev page).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import ssm_workloads as W  # noqa: E402
+
+METRIC = "selective-scan fwd tokens/s and HBM GB/s as % of B300 peak (D=1536,N=16)"
+HBM_FALLBACK_GBS = 6400.0
+KERNEL_SRC = os.path.join(ROOT, "selective_state_space_150_b300", "csrc", "ssmscan.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ----------------------------------------------------------------- accounting
+def algorithmic_bytes(wl: W.Workload) -> int:
+    """Bytes one call must move at least: every input element read once, every
+    output element written once; the (batch, L, dim, N) state never moves."""
+    es = 2 if wl.dtype == "bf16" else 4
+    bld = wl.batch * wl.L * wl.dim
+    n = bld * es * (2 + (1 if wl.gate else 0))          # u, delta, z
+    n += bld * es                                      # y
+    n += 2 * wl.batch * wl.L * wl.N * es               # B, C
+    n += 4 * wl.batch * wl.dim * wl.N                  # h_last
+    n += 4 * wl.dim * wl.N                             # A
+    n += 4 * wl.dim * ((1 if wl.skip else 0) + (1 if wl.delta_bias else 0))
+    return n
+
+
+def algorithmic_ops(wl: W.Workload):
+    """(MUFU ops, FP32 lane ops) one call needs: per (b, t, d, n) one exp and
+    four FP32 ops (dt*A, (dt*u)*B, the state FMA, the readout FMA); per
+    (b, t, d) an exp + log for softplus, an exp + reciprocal for the SiLU gate,
+    and the bias add, dt*u, D*u and gate multiply."""
+    bld = wl.batch * wl.L * wl.dim
+    mufu = bld * wl.N + bld * ((2 if wl.softplus else 0) + (2 if wl.gate else 0))
+    fp32 = 4 * bld * wl.N + bld * (1 + (1 if wl.delta_bias else 0) + (1 if wl.skip else 0)
+                                   + (1 if wl.gate else 0))
+    return mufu, fp32
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json, bf16 copy)"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback (6.4 TB/s recipe figure)"
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, only if it was
+    taken on the current kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_sha") == kernel_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """Polls NVML every 10 ms: SM clock, max SM clock, clock-event reasons."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+    def __init__(self, index: int):
+        self.samples, self.reasons, self.ok = [], set(), False
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.max_mhz = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                bits = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for b, name in self.REASONS.items():
+                    if bits & b:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(0.01)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self.ok:
+            self.t.join()
+
+    def summary(self):
+        return {"sm_mhz": (statistics.median(self.samples) if self.samples else None),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
+                "samples": len(self.samples), "source": "NVML, 10 ms polling"}
+
+
+# ----------------------------------------------------------------- distributed
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- cpu side
+def oracle_rate(wl: W.Workload, inp, budget_s: float, threads: int, seed: int = 2):
+    """Time the fp64 oracle on a bounded sample of the workload: all batch rows
+    and all steps of a seeded subset of channels, sized to about budget_s of
+    thread-time.  Returns (tokens/s scaled to the full channel count, sample
+    description, wall seconds)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    # calibrate on a tiny piece
+    probe_d = np.arange(min(4, wl.dim))
+    sub = W.gather(inp, np.arange(1), probe_d)
+    t0 = time.perf_counter()
+    oracle.selective_scan_fwd(sub["u"], sub["delta"], sub["A"], sub["B"], sub["C"], sub["D"],
+                              sub["z"], sub["delta_bias"], sub["softplus"])
+    per_btd = (time.perf_counter() - t0) / (wl.L * len(probe_d))
+    n_dim = int(budget_s / max(per_btd * wl.batch * wl.L, 1e-12))
+    n_dim = max(threads, min(wl.dim, n_dim))
+    ds = np.sort(rng.choice(wl.dim, size=n_dim, replace=False))
+    sub = W.gather(inp, np.arange(wl.batch), ds)
+    t0 = time.perf_counter()
+    oracle.selective_scan_fwd_threads(sub["u"], sub["delta"], sub["A"], sub["B"], sub["C"],
+                                      sub["D"], sub["z"], sub["delta_bias"], sub["softplus"],
+                                      threads=threads)
+    wall = time.perf_counter() - t0
+    tokens_equiv = wl.batch * wl.L * n_dim / wl.dim
+    desc = (f"all {wl.batch} batch rows x {wl.L} steps x {n_dim} of {wl.dim} channels "
+            f"(N={wl.N}), fp64 C loop on {threads} host threads; tokens scaled by "
+            f"{n_dim}/{wl.dim}")
+    return tokens_equiv / wall, desc, wall
+
+
+def config_of(wl: W.Workload, l2_note: str):
+    return {"workload": wl.name, "batch": wl.batch, "L": wl.L, "dim": wl.dim, "N": wl.N,
+            "io_dtype": wl.dtype, "state_dtype": "f32", "softplus": wl.softplus,
+            "delta_bias": wl.delta_bias, "gate": wl.gate, "skip": wl.skip,
+            "tokens_per_step": wl.tokens, "l2": l2_note}
+
+
+# ----------------------------------------------------------------- reference arm
+def run_reference(args, wl):
+    world, rank, _ = (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0)
+    if rank != 0:
+        return None
+    threads = os.cpu_count() or 1
+    inp = W.make_inputs(wl, seed=0)
+    rates = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        r, desc, _ = oracle_rate(wl, inp, budget_s=args.ref_step_seconds * threads,
+                                 threads=threads, seed=100 + i)
+        if i >= args.warmup:
+            rates.append(r)
+    value = float(np.mean(rates))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * wl.tokens / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl, "n/a (host)"),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": desc + "; each step a fresh channel sample"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args, wl, world, rank, local):
+    import torch
+    import selective_state_space_150_b300 as ssm
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    inp = W.make_inputs(wl, seed=rank)
+    bf = wl.dtype == "bf16"
+    tdt = torch.bfloat16 if bf else torch.float32
+
+    def host(a, pin=True):
+        if a is None:
+            return None
+        t = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
+             else torch.from_numpy(a))
+        return t.pin_memory() if pin else t
+
+    hin = {k: host(inp[k]) for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}
+
+    def device_set():
+        return {k: (None if v is None else v.to(dev)) for k, v in hin.items()}
+
+    # Two resident copies of the inputs (and outputs), alternated step by step,
+    # so that each step streams a working set larger than the 126 MB L2.
+    sets = [device_set(), device_set()]
+    outs = [(torch.empty((wl.batch, wl.L, wl.dim), dtype=tdt, device=dev),
+             torch.empty((wl.batch, wl.dim, wl.N), dtype=torch.float32, device=dev))
+            for _ in range(2)]
+    fn = ssm.ssm_scan_fwd_bf16 if bf else ssm.ssm_scan_fwd
+    P = lambda t: 0 if t is None else t.data_ptr()  # noqa: E731
+
+    def launch(i):
+        s, (y, h) = sets[i & 1], outs[i & 1]
+        st = fn(P(s["u"]), P(s["delta"]), P(s["A"]), P(s["B"]), P(s["C"]), P(s["D"]), P(s["z"]),
+                P(s["delta_bias"]), int(wl.softplus), P(y), P(h), wl.batch, wl.L, wl.dim, wl.N,
+                sptr)
+        if st != 0:
+            raise RuntimeError(ssm.ssm_status_string(st))
+
+    working_set = 2 * (algorithmic_bytes(wl))
+    l2_note = (f"inputs and outputs rotate over 2 resident copies "
+               f"({working_set / 1e6:.0f} MB > 126 MB L2); no flush")
+
+    for i in range(args.warmup):
+        launch(i)
+    torch.cuda.synchronize(dev)
+
+    # pipe peaks for the compute roofline (measured on this GPU, this run)
+    peaks = None
+    try:
+        import ctypes
+        lib = ctypes.CDLL(os.path.join(ROOT, "selective_state_space_150_b300", "libpipepeaks.so"))
+        out = (ctypes.c_double * 4)()
+        if lib.ssm_pipe_peaks(out, ctypes.c_void_p(sptr)) == 0:
+            peaks = {"ex2_per_s": out[0], "fma_lane_ops_per_s": out[1],
+                     "fma2_lane_ops_per_s": out[2], "sms": int(out[3])}
+    except Exception as e:  # measurement support missing: report without it
+        peaks = {"error": str(e)}
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(local)
+    with sampler:
+        # keep the GPU busy for a short untimed window so the clock samples
+        # include the steady state, then the timed region
+        t_end = time.perf_counter() + args.clock_window
+        i = 0
+        while time.perf_counter() < t_end:
+            launch(i)
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for k in range(K):
+            starts[k].record(stream)
+            launch(k)
+            ends[k].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    total_ms = starts[0].elapsed_time(ends[-1])
+    per_launch_ms = [starts[k].elapsed_time(ends[k]) for k in range(K)]
+    total_ms = max_over_ranks(total_ms, world, dev)
+    kern_ms = statistics.mean(per_launch_ms)
+
+    value = world * wl.tokens * K / (total_ms * 1e-3)
+    bytes_launch = algorithmic_bytes(wl)
+    hbm_gbs, hbm_src = measured_peaks()
+    achieved_gbs = bytes_launch / (kern_ms * 1e-3) / 1e9
+    mufu, fp32 = algorithmic_ops(wl)
+    t_hbm = bytes_launch / (hbm_gbs * 1e9)
+    roof = None
+    if peaks and "ex2_per_s" in peaks:
+        t_mufu = mufu / peaks["ex2_per_s"]
+        t_fp32 = fp32 / peaks["fma_lane_ops_per_s"]
+        t_alu = max(t_mufu, t_fp32)
+        if t_alu > t_hbm:
+            pipe = "mufu_ex2" if t_mufu >= t_fp32 else "fp32_fma"
+            ops = mufu if pipe == "mufu_ex2" else fp32
+            peak = peaks["ex2_per_s"] if pipe == "mufu_ex2" else peaks["fma_lane_ops_per_s"]
+            roof = {"bound": "alu", "pipe": pipe, "achieved": ops / (kern_ms * 1e-3) / 1e9,
+                    "peak": peak / 1e9, "unit": "Gop/s",
+                    "frac": (ops / (kern_ms * 1e-3)) / peak,
+                    "peak_source": "measured on this GPU by libpipepeaks (8 chains/thread, "
+                                   "64 warps/SM), same run"}
+    if roof is None:
+        roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved_gbs / hbm_gbs, "peak_source": hbm_src}
+    roof["traffic"] = recorded_traffic(wl.name)
+    roof["algorithmic_bytes_per_launch"] = bytes_launch
+    roof["mufu_ops_per_launch"] = mufu
+    roof["fp32_ops_per_launch"] = fp32
+    roof["kernel_ms"] = kern_ms
+
+    # ---- end to end through the C ABI: pinned host inputs -> device -> kernel
+    #      -> y and h_last back to pinned host memory, every step
+    hy = torch.empty((wl.batch, wl.L, wl.dim), dtype=tdt).pin_memory()
+    hh = torch.empty((wl.batch, wl.dim, wl.N), dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in hin.values() if v is not None)
+    d2h = hy.numel() * hy.element_size() + hh.numel() * hh.element_size()
+    Ke = max(3, min(K, args.e2e_steps))
+
+    def e2e_step():
+        s, (y, h) = sets[0], outs[0]
+        for k, v in hin.items():
+            if v is not None:
+                s[k].copy_(v, non_blocking=True)
+        launch(0)
+        hy.copy_(y, non_blocking=True)
+        hh.copy_(h, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = world * wl.tokens * Ke / (e2e_ms * 1e-3)
+    st = ssm.ssm_scan_last_device_status(sptr)
+    if st != 0:
+        raise RuntimeError("device status: " + ssm.ssm_status_string(st))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": total_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded; see ssm_workloads.py)",
+        "config": config_of(wl, l2_note),
+        "hbm": {"achieved_gbs": achieved_gbs, "peak_gbs": hbm_gbs, "frac": achieved_gbs / hbm_gbs,
+                "peak_source": hbm_src, "roofline_ms": t_hbm * 1e3},
+        "roofline": roof,
+        "pipe_peaks": peaks,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": Ke,
+                "path": "pinned host -> cudaMemcpyAsync -> ssm_scan_fwd_bf16 (C ABI) -> "
+                        "pinned host, one stream"},
+        "gpu_launches": K,
+        "clocks": sampler.summary(),
+        "plan": ssm.ssm_scan_plan(wl.batch, wl.L, wl.dim, wl.N, 1 if bf else 0),
+        "impl": "ours",
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        r, desc, _ = oracle_rate(wl, inp, budget_s=args.cpu_seconds, threads=threads)
+        line["cpu_baseline"] = {"value": r, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle", "sample": desc}
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mamba130m_bf16", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--all", action="store_true", help="one line per workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="thread-seconds of oracle work in the cpu_baseline sample")
+    ap.add_argument("--ref-step-seconds", type=float, default=1.5,
+                    help="wall seconds of oracle work per reference step")
+    ap.add_argument("--clock-window", type=float, default=0.5)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    names = sorted(W.WORKLOADS) if args.all else [args.workload]
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        for n in names:
+            line = run_reference(args, W.WORKLOADS[n])
+            print(json.dumps(line), flush=True)
+        return 0
+
+    world, rank, local = dist_init()
+    for n in names:
+        line = run_ours(args, W.WORKLOADS[n], world, rank, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,163 @@
+/*
+ * ssmscan.h -- C ABI of libssmscan, the selective-scan forward pass of the
+ * Mamba S6 selective state-space layer on one NVIDIA B300 (sm_103a).
+ *
+ * What the library computes
+ * -------------------------
+ * For every batch row b, channel d and state n, starting from h = 0:
+ *
+ *   dt        = delta[b,t,d] + delta_bias[d]           (bias optional)
+ *   dt        = softplus(dt) = log(1 + exp(dt))        (if softplus_flag)
+ *   h[b,d,n]  = exp(dt * A[d,n]) * h[b,d,n] + dt * B[b,t,n] * u[b,t,d]
+ *   y[b,t,d]  = sum_n C[b,t,n] * h[b,d,n] + D[d] * u[b,t,d]   (D optional)
+ *   y[b,t,d] *= z[b,t,d] / (1 + exp(-z[b,t,d]))          (SiLU gate, optional)
+ *   h_last[b,d,n] = h after the last step t = L-1          (optional output)
+ *
+ * The scan and its shapes follow the "State Space Models (SSM)" summary page,
+ * section 3.2 "Selective Scan Algorithm" (u, delta (B,L,D); A (D,N);
+ * B, C (B,L,N); zero initial state; deltaA = exp(delta A),
+ * deltaB_u = delta B u).  The softplus of (delta + bias), the D skip on the
+ * scan input and the SiLU(z) gate after the skip follow the SelectiveSSM /
+ * MambaBlock listings of that page (sections 5.1-5.2) and of the youngju.dev
+ * page "Mamba와 State Space Model 논문 심층 분석".  B is discretised in the
+ * simplified form dt * B that every listing on the pages uses.  The state
+ * h_last is the only thing a generation step needs to continue a sequence
+ * (Obsidian "Mamba" note, section 4.2).  The expanded (B,L,D,N) state is
+ * never written to memory: it lives in registers (itwiki "상태 공간 모델",
+ * section "Mamba의 선택 메커니즘"; Obsidian note section 5.1).
+ *
+ * Layout and ownership
+ * --------------------
+ * All tensors are dense, row-major, last index fastest, no strides:
+ *   u, delta, z, y : (batch, L, dim)      B, C   : (batch, L, N)
+ *   A              : (dim, N)  fp32       D, delta_bias : (dim,)  fp32
+ *   h_last         : (batch, dim, N)  fp32
+ * "dim" is the channel count the pages call D (renamed so it does not clash
+ * with the skip vector D).  Every pointer is a DEVICE pointer owned by the
+ * caller; the library never allocates, frees or keeps a pointer past the
+ * call.  Work is enqueued on `stream` and the call returns without
+ * synchronising.  y must not overlap any input.  Optional pointers may be
+ * NULL: D (no skip), z (no gate), delta_bias (bias 0), h_last (not written).
+ * A required pointer may be NULL only when its tensor has no elements (for
+ * example u, delta and y when L = 0, which still writes h_last = 0).
+ *
+ * Precision: the state h and all arithmetic are fp32.  In the bf16 entry
+ * point u, delta, B, C, z and y are bf16 (passed as their 16-bit patterns in
+ * uint16_t) while A, D, delta_bias and h_last stay fp32; y is rounded to
+ * nearest-even.  Results match an fp64 evaluation to |err| <= 1e-4 (1+|ref|)
+ * for fp32 inputs and <= 2e-2 (1+|ref|) for bf16 inputs.
+ *
+ * Errors
+ * ------
+ * Host-side argument checks return a nonzero ssm_status and launch nothing.
+ * Errors that can only be seen on the device (a bounded wait inside a kernel
+ * that ran out) are recorded in a device status word and reported by
+ * ssm_scan_last_device_status().  No kernel of this library traps.
+ */
+#ifndef SSMSCAN_H
+#define SSMSCAN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+/* The CUDA runtime's stream handle (same definition as the CUDA headers). */
+typedef struct CUstream_st *cudaStream_t;
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_NULL = 1,            /* a required pointer is NULL                 */
+    SSM_ERR_SIZE = 2,            /* a size is negative, N < 1, or a product    */
+                                 /* overflows the index range                  */
+    SSM_ERR_ALIGN = 3,           /* a pointer is not aligned to its element    */
+    SSM_ERR_UNSUPPORTED_N = 4,   /* N > SSM_MAX_N                              */
+    SSM_ERR_LAUNCH = 5,          /* the CUDA runtime refused the launch        */
+    SSM_ERR_TIMEOUT = 6,         /* a bounded device-side wait ran out         */
+    SSM_ERR_ALIAS = 7,           /* y overlaps an input                        */
+    SSM_ERR_ARG = 8              /* an invalid debug key or value              */
+} ssm_status;
+
+/* Largest state size N the kernels are built for. */
+#define SSM_MAX_N 128
+
+/*
+ * fp32 entry point: every tensor is fp32.
+ * Returns SSM_OK once the work is enqueued on `stream`.
+ */
+SSM_API int ssm_scan_fwd(const float *u, const float *delta, const float *A,
+                 const float *B, const float *C, const float *D,
+                 const float *z, const float *delta_bias, int softplus_flag,
+                 float *y, float *h_last,
+                 int64_t batch, int64_t L, int64_t dim, int64_t N,
+                 cudaStream_t stream);
+
+/*
+ * bf16 entry point: u, delta, B, C, z, y are bf16 bit patterns; A, D,
+ * delta_bias and h_last are fp32.  Same argument order and meaning as
+ * ssm_scan_fwd.
+ */
+SSM_API int ssm_scan_fwd_bf16(const uint16_t *u, const uint16_t *delta, const float *A,
+                      const uint16_t *B, const uint16_t *C, const float *D,
+                      const uint16_t *z, const float *delta_bias, int softplus_flag,
+                      uint16_t *y, float *h_last,
+                      int64_t batch, int64_t L, int64_t dim, int64_t N,
+                      cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns SSM_OK, SSM_ERR_TIMEOUT if a kernel gave up a
+ * bounded wait since the last call (its outputs are then incomplete), or
+ * SSM_ERR_LAUNCH if the CUDA runtime reports an error on the stream.
+ */
+SSM_API int ssm_scan_last_device_status(cudaStream_t stream);
+
+/* Short English text for a status code (static storage, never NULL). */
+SSM_API const char *ssm_status_string(int status);
+
+/*
+ * Launch plan the library would use for a problem, without launching.
+ * dtype: 0 = fp32, 1 = bf16.  On SSM_OK, plan[0..7] receives:
+ *   [0] lanes per channel S     [1] states per lane      [2] timesteps per chunk
+ *   [3] channels per block      [4] threads per block    [5] blocks in the grid
+ *   [6] dynamic shared bytes    [7] 1 if tiles move by TMA, 0 if by plain loads
+ */
+SSM_API int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype,
+                  int64_t plan[8]);
+
+/*
+ * Process-wide knobs for tests and tuning sweeps (not for production use;
+ * not thread-safe against concurrent launches).  Keys:
+ *   SSM_KNOB_WAIT_NS        give-up time of every device-side wait, in ns
+ *                           (default 2e9; must be >= 1000)
+ *   SSM_KNOB_FORCE_TIMEOUT  1: every block first waits on a barrier that
+ *                           nothing completes, so the wait runs out, the
+ *                           block drains its copies and returns, and
+ *                           ssm_scan_last_device_status reports
+ *                           SSM_ERR_TIMEOUT.  0 (default): off.
+ *   SSM_KNOB_LANES          force S (1, 2, 4 or 8); 0 = automatic
+ *   SSM_KNOB_CHUNK          force timesteps per chunk (32 or 64); 0 = automatic
+ *   SSM_KNOB_PLAIN_LOADS    1: move tiles with plain loads even when TMA applies
+ * Returns SSM_OK or SSM_ERR_ARG.
+ */
+enum {
+    SSM_KNOB_WAIT_NS = 1,
+    SSM_KNOB_FORCE_TIMEOUT = 2,
+    SSM_KNOB_LANES = 3,
+    SSM_KNOB_CHUNK = 4,
+    SSM_KNOB_PLAIN_LOADS = 5
+};
+SSM_API int ssm_set_knob(int key, int64_t value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSMSCAN_H */

@@ -1,0 +1,15 @@
+"""libssmscan: the selective-scan forward pass of the Mamba S6 layer on B300.
+
+The computation lives in the CUDA library ``libssmscan.so`` (C ABI declared in
+``include/ssmscan.h``); ``ssmscan`` is its thin Python binding.
+"""
+from .ssmscan import (  # noqa: F401
+    SSMError,
+    selective_scan_fwd,
+    ssm_scan_fwd,
+    ssm_scan_fwd_bf16,
+    ssm_scan_last_device_status,
+    ssm_scan_plan,
+    ssm_set_knob,
+    ssm_status_string,
+)

@@ -1,0 +1,148 @@
+"""Python binding of libssmscan (the selective-scan forward on sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libssmscan.so.  The functions named like the C ABI take raw device
+pointers (ints) and sizes; ``selective_scan_fwd`` is a convenience wrapper that
+takes torch CUDA tensors, allocates the outputs with torch when they are not
+given, and raises on a nonzero status.  There is no CPU fallback: importing this
+module fails if the shared library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssmscan.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libssmscan.so not found at {LIB_PATH}; build it with "
+        "`python -m selective_state_space_150_b300.build` (nvcc, sm_103a)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+SSM_OK = 0
+SSM_ERR_NULL = 1
+SSM_ERR_SIZE = 2
+SSM_ERR_ALIGN = 3
+SSM_ERR_UNSUPPORTED_N = 4
+SSM_ERR_LAUNCH = 5
+SSM_ERR_TIMEOUT = 6
+SSM_ERR_ALIAS = 7
+SSM_ERR_ARG = 8
+SSM_MAX_N = 128
+
+SSM_KNOB_WAIT_NS = 1
+SSM_KNOB_FORCE_TIMEOUT = 2
+SSM_KNOB_LANES = 3
+SSM_KNOB_CHUNK = 4
+SSM_KNOB_PLAIN_LOADS = 5
+
+EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_last_device_status",
+            "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_FWD_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp,
+             _i64, _i64, _i64, _i64, _vp]
+for _name in ("ssm_scan_fwd", "ssm_scan_fwd_bf16"):
+    getattr(_lib, _name).argtypes = _FWD_ARGS
+    getattr(_lib, _name).restype = ctypes.c_int
+_lib.ssm_scan_last_device_status.argtypes = [_vp]
+_lib.ssm_scan_last_device_status.restype = ctypes.c_int
+_lib.ssm_status_string.argtypes = [ctypes.c_int]
+_lib.ssm_status_string.restype = ctypes.c_char_p
+_lib.ssm_scan_plan.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int, ctypes.POINTER(_i64)]
+_lib.ssm_scan_plan.restype = ctypes.c_int
+_lib.ssm_set_knob.argtypes = [ctypes.c_int, _i64]
+_lib.ssm_set_knob.restype = ctypes.c_int
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({ssm_status_string(status)})")
+
+
+# ------------------------------------------------------------ C ABI, verbatim
+def ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, h_last,
+                 batch, L, dim, N, stream) -> int:
+    """fp32 entry point; pointer arguments are ints (0 for NULL)."""
+    return _lib.ssm_scan_fwd(u or None, delta or None, A or None, B or None, C or None,
+                             D or None, z or None, delta_bias or None, int(softplus_flag),
+                             y or None, h_last or None, batch, L, dim, N, stream or None)
+
+
+def ssm_scan_fwd_bf16(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, h_last,
+                      batch, L, dim, N, stream) -> int:
+    """bf16 entry point; pointer arguments are ints (0 for NULL)."""
+    return _lib.ssm_scan_fwd_bf16(u or None, delta or None, A or None, B or None, C or None,
+                                  D or None, z or None, delta_bias or None, int(softplus_flag),
+                                  y or None, h_last or None, batch, L, dim, N, stream or None)
+
+
+def ssm_scan_last_device_status(stream=0) -> int:
+    return _lib.ssm_scan_last_device_status(stream or None)
+
+
+def ssm_status_string(status: int) -> str:
+    return _lib.ssm_status_string(int(status)).decode()
+
+
+def ssm_scan_plan(batch, L, dim, N, dtype: int):
+    """Launch plan as a dict (see include/ssmscan.h); raises on a bad argument."""
+    out = (_i64 * 8)()
+    st = _lib.ssm_scan_plan(batch, L, dim, N, int(dtype), out)
+    if st != SSM_OK:
+        raise SSMError(st, "ssm_scan_plan")
+    keys = ("lanes", "states_per_lane", "chunk", "channels_per_block", "threads",
+            "blocks", "smem_bytes", "tma")
+    return dict(zip(keys, [int(v) for v in out]))
+
+
+def ssm_set_knob(key: int, value: int) -> int:
+    return _lib.ssm_set_knob(int(key), int(value))
+
+
+# ------------------------------------------------------------ torch convenience
+def _ptr(t):
+    return 0 if t is None else t.data_ptr()
+
+
+def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
+                       y=None, h_last=None, stream=None, want_h_last=True):
+    """Run the kernel on torch CUDA tensors.
+
+    u, delta, z: (batch, L, dim); B, C: (batch, L, N); A: (dim, N) fp32;
+    D, delta_bias: (dim,) fp32.  u/delta/B/C/z are all fp32 (fp32 entry point)
+    or all bf16 (bf16 entry point).  Returns (y, h_last).  Work is enqueued on
+    ``stream`` (default: torch's current stream) without synchronising.
+    """
+    import torch
+
+    bf16 = u.dtype == torch.bfloat16
+    if not bf16 and u.dtype != torch.float32:
+        raise TypeError(f"u must be float32 or bfloat16, got {u.dtype}")
+    io = (u, delta, B, C) + ((z,) if z is not None else ())
+    for t in io:
+        if t.dtype != u.dtype or not t.is_cuda or not t.is_contiguous():
+            raise TypeError("u, delta, B, C, z must share u's dtype and be contiguous CUDA tensors")
+    for t in (A, D, delta_bias):
+        if t is not None and (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()):
+            raise TypeError("A, D, delta_bias must be contiguous float32 CUDA tensors")
+    batch, L, dim = u.shape
+    N = A.shape[1]
+    if y is None:
+        y = torch.empty_like(u)
+    if h_last is None and want_h_last:
+        h_last = torch.empty((batch, dim, N), dtype=torch.float32, device=u.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(u.device).cuda_stream
+    fn = ssm_scan_fwd_bf16 if bf16 else ssm_scan_fwd
+    st = fn(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+            _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(h_last),
+            batch, L, dim, N, int(stream))
+    if st != SSM_OK:
+        raise SSMError(st, fn.__name__)
+    return y, h_last

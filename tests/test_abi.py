@@ -1,0 +1,118 @@
+"""C ABI of libssmscan on the host: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU.  No call
+here reaches a kernel launch, so these run without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import selective_state_space_150_b300 as ssm
+from selective_state_space_150_b300 import ssmscan
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssmscan.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^SSM_API\s+(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_symbols() == sorted(ssmscan.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(ssmscan.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    for st in range(0, 9):
+        s = ssm.ssm_status_string(st)
+        assert s and s != "unknown status"
+    assert ssm.ssm_status_string(99) == "unknown status"
+
+
+# fake device addresses: validation must reject before dereferencing or launching
+P = 0x10000000
+Q = 0x20000000
+
+
+def fwd(fn, **kw):
+    args = dict(u=P, delta=P + 0x100000, A=P + 0x200000, B=P + 0x300000, C=P + 0x400000,
+                D=0, z=0, delta_bias=0, softplus_flag=0, y=Q, h_last=0,
+                batch=2, L=8, dim=16, N=4, stream=0)
+    args.update(kw)
+    return fn(**args)
+
+
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16])
+def test_null_pointers(fn):
+    for k in ("u", "delta", "A", "B", "C", "y"):
+        assert fwd(fn, **{k: 0}) == ssmscan.SSM_ERR_NULL, k
+
+
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16])
+def test_bad_sizes(fn):
+    assert fwd(fn, batch=-1) == ssmscan.SSM_ERR_SIZE
+    assert fwd(fn, L=-3) == ssmscan.SSM_ERR_SIZE
+    assert fwd(fn, dim=-1) == ssmscan.SSM_ERR_SIZE
+    assert fwd(fn, N=0) == ssmscan.SSM_ERR_SIZE
+    assert fwd(fn, N=ssmscan.SSM_MAX_N + 1) == ssmscan.SSM_ERR_UNSUPPORTED_N
+    assert fwd(fn, batch=1 << 40, L=1 << 20, dim=1 << 10) == ssmscan.SSM_ERR_SIZE
+
+
+def test_misaligned_pointers():
+    assert fwd(ssm.ssm_scan_fwd, u=P + 2) == ssmscan.SSM_ERR_ALIGN
+    assert fwd(ssm.ssm_scan_fwd_bf16, u=P + 1) == ssmscan.SSM_ERR_ALIGN
+    assert fwd(ssm.ssm_scan_fwd_bf16, A=P + 0x200002) == ssmscan.SSM_ERR_ALIGN
+    assert fwd(ssm.ssm_scan_fwd_bf16, h_last=Q + 0x100002) == ssmscan.SSM_ERR_ALIGN
+
+
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16])
+def test_outputs_must_not_alias_inputs(fn):
+    assert fwd(fn, y=P + 0x100000) == ssmscan.SSM_ERR_ALIAS            # y == delta
+    assert fwd(fn, y=P + 0x10) == ssmscan.SSM_ERR_ALIAS                # y inside u
+    assert fwd(fn, h_last=P + 0x300000) == ssmscan.SSM_ERR_ALIAS       # h_last == B
+    assert fwd(fn, h_last=Q + 0x8) == ssmscan.SSM_ERR_ALIAS            # h_last inside y
+
+
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16])
+def test_empty_problems_launch_nothing(fn):
+    assert fwd(fn, batch=0) == ssmscan.SSM_OK
+    assert fwd(fn, dim=0) == ssmscan.SSM_OK
+
+
+def test_knobs_validate():
+    K = ssmscan
+    assert ssm.ssm_set_knob(K.SSM_KNOB_WAIT_NS, 10) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(K.SSM_KNOB_LANES, 3) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(K.SSM_KNOB_CHUNK, 48) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(99, 0) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(K.SSM_KNOB_LANES, 0) == K.SSM_OK
+    assert ssm.ssm_set_knob(K.SSM_KNOB_WAIT_NS, 2_000_000_000) == K.SSM_OK
+
+
+@pytest.mark.parametrize("shape", [(8, 2048, 1536, 16), (4, 8192, 5120, 16), (1, 131072, 5120, 16),
+                                   (1, 256, 64, 16), (2, 4096, 256, 64), (3, 5, 7, 1),
+                                   (1, 1, 1, 128), (2, 9, 33, 3)])
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_plans_cover_the_state(shape, dtype):
+    pl = ssm.ssm_scan_plan(*shape, dtype)
+    batch, L, dim, N = shape
+    S, npt = pl["lanes"], pl["states_per_lane"]
+    assert S in (1, 2, 4, 8) and npt in (1, 2, 4, 8, 16)
+    assert S * npt >= N and (S == 1 or (S // 2) * npt < N)        # no all-padding lane
+    assert pl["threads"] == 128 and pl["channels_per_block"] * S == 128
+    assert pl["blocks"] == batch * -(-dim // pl["channels_per_block"])
+    assert 0 < pl["smem_bytes"] <= 227 * 1024
+
+
+def test_plan_rejects_bad_arguments():
+    with pytest.raises(ssm.SSMError):
+        ssm.ssm_scan_plan(1, 1, 1, 0, 1)
+    with pytest.raises(ssm.SSMError):
+        ssm.ssm_scan_plan(1, 1, 1, 16, 7)
