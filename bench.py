@@ -105,9 +105,17 @@ class ClockSampler:
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
                0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
 
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.sw_power_cap,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown")
+
     def __init__(self, index: int):
-        self.samples, self.reasons, self.ok = [], set(), False
+        self.index = index
+        self.samples, self.reasons, self.ok, self.err = [], set(), False, None
+        self.max_mhz = None
+        self.source = "NVML, 10 ms polling"
         self._stop = threading.Event()
+        self.proc = None
         try:
             import pynvml
             pynvml.nvmlInit()
@@ -115,8 +123,9 @@ class ClockSampler:
             self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
             self.ok = True
-        except Exception:
-            self.max_mhz = None
+        except Exception as e:  # fall back to polling nvidia-smi
+            self.err = f"NVML unavailable ({type(e).__name__}: {e}); used nvidia-smi"
+            self.source = "nvidia-smi -lms 50"
 
     def _run(self):
         while not self._stop.is_set():
@@ -134,17 +143,45 @@ class ClockSampler:
         if self.ok:
             self.t = threading.Thread(target=self._run, daemon=True)
             self.t.start()
+        else:
+            import subprocess
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.SMI_FIELDS,
+                     "--format=csv,noheader,nounits", "-lms", "50"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception as e:
+                self.err = f"no clock source: {e}"
         return self
 
     def __exit__(self, *a):
         self._stop.set()
         if self.ok:
             self.t.join()
+        elif self.proc is not None:
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            names = ("sw_power_cap", "hw_slowdown", "sw_thermal_slowdown", "hw_thermal_slowdown")
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, v in zip(names, f[2:6]):
+                    if v.lower() == "active":
+                        self.reasons.add(name)
 
     def summary(self):
-        return {"sm_mhz": (statistics.median(self.samples) if self.samples else None),
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
-                "samples": len(self.samples), "source": "NVML, 10 ms polling"}
+        d = {"sm_mhz": (statistics.median(self.samples) if self.samples else None),
+             "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
+             "samples": len(self.samples), "source": self.source}
+        if self.err:
+            d["note"] = self.err
+        return d
 
 
 # ----------------------------------------------------------------- distributed

@@ -10,21 +10,24 @@
 // itwiki page ("Mamba의 선택 메커니즘") and the Obsidian "Mamba" note (5.1)
 // describe; the way it is mapped onto B300 here is our own.
 //
-// Work decomposition (one thread block = 128 threads):
-//   * a block owns one batch row b and DT = 128/S consecutive channels, and
-//     walks the sequence in chunks of TC timesteps;
-//   * each channel's N states are split over S adjacent lanes, NPT states per
-//     lane (N <= S*NPT); the state stays in registers for the whole sequence;
-//   * per chunk, TMA (cp.async.bulk.tensor, 3-D maps over (dim, L, batch)) brings
-//     the u / delta / z tiles [TC x DT] and the B / C tiles [TC x N] into a
-//     two-stage shared-memory ring tracked by mbarriers, one chunk ahead;
-//   * PREP: every (t, d) of the chunk computes dt = softplus(delta + bias) and
-//     dt*u once; B and C are widened to fp32;
-//   * SCAN: each lane advances its NPT states over the chunk and leaves its
-//     partial <C_t, h_t> in shared memory;
-//   * POST: every (t, d) sums the S partials, adds D*u, applies the SiLU gate,
-//     rounds to the output type into a tile that one thread stores with a TMA
-//     bulk tensor store (double-buffered).
+// Work decomposition (one thread block = 4 warps):
+//   * a block owns one batch row b and a tile of DT consecutive channels and
+//     walks the sequence in chunks of TC = 32 timesteps;
+//   * a warp owns 32/S channel groups; the S lanes of a group share KC channels
+//     and split their N states, NPT per lane (N <= S * NPT), so a lane keeps
+//     KC x NPT states in registers for the whole sequence;
+//   * per chunk, TMA (cp.async.bulk.tensor, 3-D maps over (dim, L, batch), with
+//     the 32/64/128-byte swizzle that matches the tile's row width) brings the
+//     u / delta / z tiles and the B / C rows into a two-stage ring tracked by
+//     mbarriers, one chunk ahead; the block widens B and C to fp32 once;
+//   * then each warp runs its own pipeline over groups of S steps: every lane
+//     computes dt = softplus(delta + bias), dt*u, the gate silu(z) and the skip
+//     D*u*silu(z) for ONE (step, channel) item of the group and shares dt, dt*u
+//     with the group through a small shared buffer; all lanes advance their
+//     states over the S steps; a transposed shuffle reduction of the partial
+//     readouts <C, h> leaves each lane the full readout of exactly the item it
+//     prepared, so skip and gate apply in registers and y goes to a swizzled
+//     output tile that one thread stores with a TMA bulk tensor store.
 // Shapes TMA cannot describe (rows not a multiple of 16 bytes, misaligned
 // pointers, L = 0) take the same kernel with plain loads and stores.
 //
@@ -43,6 +46,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "ssmscan.h"
 
@@ -156,22 +160,59 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // ------------------------------------------------------------------ element types
 template <typename T> struct Elt;
 template <> struct Elt<float> {
-    using S = float;
     __device__ static float to_f(float v) { return v; }
     __device__ static float from_f(float v) { return v; }
     static constexpr CUtensorMapDataType tmap_type = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 };
 template <> struct Elt<__nv_bfloat16> {
-    using S = __nv_bfloat16;
     __device__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
     __device__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
     static constexpr CUtensorMapDataType tmap_type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 };
 
-// softplus(x) = log(1 + e^x) = max(x, 0) + log1p(e^-|x|), and SiLU(z) = z/(1+e^-z).
-// fp32 inputs use the accurate library functions; bf16 inputs use the MUFU
-// approximations (ex2/lg2/rcp), with log1p of a small argument taken from its
-// series so that small softplus values keep their relative accuracy.
+// KC consecutive elements (KC = 1 or 2) widened to fp32, and stored back.
+template <typename T, int KC>
+__device__ __forceinline__ void ld_k(const unsigned char* p, float (&v)[KC]) {
+    if constexpr (KC == 1) {
+        v[0] = Elt<T>::to_f(*reinterpret_cast<const T*>(p));
+    } else if constexpr (sizeof(T) == 4) {
+        const float2 q = *reinterpret_cast<const float2*>(p);
+        v[0] = q.x;
+        v[1] = q.y;
+    } else {
+        const float2 q = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+        v[0] = q.x;
+        v[1] = q.y;
+    }
+}
+template <typename T, int KC>
+__device__ __forceinline__ void st_k(unsigned char* p, const float (&v)[KC]) {
+    if constexpr (KC == 1) {
+        *reinterpret_cast<T*>(p) = Elt<T>::from_f(v[0]);
+    } else if constexpr (sizeof(T) == 4) {
+        *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+    } else {
+        *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v[0], v[1]);
+    }
+}
+
+// Four consecutive elements widened to fp32 (B / C rows).
+template <typename T> __device__ __forceinline__ float4 ld_quad(const T* p);
+template <> __device__ __forceinline__ float4 ld_quad<float>(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+}
+template <> __device__ __forceinline__ float4 ld_quad<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    // bf16 -> fp32 is exact: the 16 bits become the top half of the fp32 word.
+    return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                       __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+}
+
+// softplus(x) = log(1 + e^x) and SiLU(z) = z / (1 + e^-z).
+// fp32 inputs use the accurate library functions.  bf16 inputs use the MUFU
+// approximations: softplus = lg2(1 + 2^(x log2 e)) ln 2 (x for x > 15, where the
+// two differ by < 4e-7), whose error is ~1e-7 absolute -- the accuracy the state
+// update needs, since a step's contribution to h scales with its dt.
 template <typename T> struct Act;
 template <> struct Act<float> {
     __device__ static float softplus(float x) {
@@ -181,15 +222,8 @@ template <> struct Act<float> {
 };
 template <> struct Act<__nv_bfloat16> {
     __device__ static float softplus(float x) {
-        const float e = ex2_approx(-fabsf(x) * kLog2e);  // in (0, 1]
-        float l;
-        if (e < 0.03125f) {
-            // log1p(e) = e - e^2/2 + e^3/3 - e^4/4 + ...; the next term is < 2e-7 e.
-            l = e * fmaf(e, fmaf(e, fmaf(e, -0.25f, 0.33333334f), -0.5f), 1.f);
-        } else {
-            l = lg2_approx(1.f + e) * kLn2;
-        }
-        return fmaxf(x, 0.f) + l;
+        const float l = lg2_approx(1.f + ex2_approx(x * kLog2e)) * kLn2;
+        return x > 15.f ? x : l;
     }
     __device__ static float silu(float z) {
         // 1 + e^-z overflows to +inf for very negative z; rcp(inf) = 0 -> silu = -0.
@@ -197,7 +231,62 @@ template <> struct Act<__nv_bfloat16> {
     }
 };
 
-__host__ __device__ constexpr size_t round128(size_t x) { return (x + 127) & ~size_t(127); }
+// Load NPT consecutive floats from shared memory with the widest vector ops.
+template <int NPT>
+__device__ __forceinline__ void ld_states(const float* p, float (&v)[NPT]) {
+    if constexpr (NPT % 4 == 0) {
+#pragma unroll
+        for (int j = 0; j < NPT; j += 4) {
+            const float4 q = *reinterpret_cast<const float4*>(p + j);
+            v[j] = q.x; v[j + 1] = q.y; v[j + 2] = q.z; v[j + 3] = q.w;
+        }
+    } else if constexpr (NPT == 2) {
+        const float2 q = *reinterpret_cast<const float2*>(p);
+        v[0] = q.x; v[1] = q.y;
+    } else {
+        v[0] = p[0];
+    }
+}
+
+// [TC][WB-byte] tiles (u, delta, z and y) live in shared memory as WB/RS column
+// blocks of [TC][RS bytes], RS = min(WB, 128), each with the TMA swizzle of span
+// RS: address bits [4, 4 + log2(RS/16)) are XORed with bits [7, ...).  Rows that
+// a warp touches together then fall in different banks.
+template <int WB>
+struct Tile {
+    static constexpr int RS = WB < 128 ? WB : 128;
+    static constexpr int NB = WB / RS;
+    static constexpr uint32_t SWZ_MASK = uint32_t(RS / 16 - 1);
+    // Byte offset of byte b of row t in a tile of TC rows.
+    __device__ static __forceinline__ uint32_t off(int t, int b, int TC) {
+        const uint32_t o = uint32_t((b / RS) * TC * RS + t * RS + (b % RS));
+        return o ^ (((o >> 7) & SWZ_MASK) << 4);
+    }
+};
+
+// Transposed reduction of each lane's partial readouts over the S lanes that
+// share a channel group: on entry v[k][q] is this lane's partial for channel k
+// at step q of the group; on exit v[k][0] holds the full sum for step q = sl.
+// Each round halves the steps a lane keeps and exchanges the other half with
+// its partner, so S - 1 shuffles per channel replace S log2(S) of a butterfly.
+template <int S, int KC>
+__device__ __forceinline__ void reduce_transposed(float (&v)[KC][S], int sl) {
+#pragma unroll
+    for (int m = S / 2; m >= 1; m >>= 1) {
+        const bool up = (sl & m) != 0;
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+#pragma unroll
+            for (int i = 0; i < m; ++i) {
+                const float send = up ? v[k][i] : v[k][i + m];
+                const float keep = up ? v[k][i + m] : v[k][i];
+                v[k][i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            }
+        }
+    }
+}
+
+__host__ __device__ constexpr size_t round1k(size_t x) { return (x + 1023) & ~size_t(1023); }
 
 struct KParams {
     const void* u;
@@ -219,29 +308,49 @@ struct KParams {
     int force_timeout;
 };
 
-// Shared-memory layout of one block, in bytes from a 128-byte aligned base.
-template <typename T, int NPT, int S, int TC>
+constexpr int kWarps = kThreads / 32;
+
+// Compile-time geometry of one block.
+//   A block has kWarps warps.  A warp has 32/S channel groups of S lanes; a lane
+//   holds KC channels x NPT states, so a group covers KC channels x S*NPT states.
+template <typename T, int NPT, int S, int KC, int TC>
+struct Geo {
+    static constexpr int ES = int(sizeof(T));
+    static constexpr int CGW = 32 / S;        // channel groups per warp
+    static constexpr int CW = CGW * KC;       // channels per warp
+    static constexpr int DT = kWarps * CW;    // channels per block
+    static constexpr int NP = NPT * S;        // states per group (>= N)
+    static constexpr int WB = DT * ES;        // tile row bytes
+    using TileT = Tile<WB>;
+    static constexpr size_t TILE = round1k(size_t(TC) * WB);
+    static constexpr size_t DD_WARP = size_t(S) * KC * CGW * 16;  // one group's (dt,dt,dtu,dtu)
+    static_assert(TC % S == 0, "chunk must hold whole groups");
+    static_assert(WB % 16 == 0 && (WB <= 128 || WB % 128 == 0), "tile rows");
+};
+
+// Shared-memory layout of one block (bytes from a 1024-byte aligned base).
+//   raw ring  kStages x { u, delta, z : tile ; B, C : [TC][N] T }
+//   s_B, s_C  [TC][NP] fp32            B, C widened (rows past L are zero)
+//   s_dd      2 x kWarps x [S][KC][CGW] float4   (dt, dt, dt*u, dt*u) per group
+//   s_y       2 x tile                  output tiles for the TMA store
+template <typename T, int NPT, int S, int KC, int TC>
 struct Layout {
-    static constexpr int DT = kThreads / S;
-    static constexpr int NP = NPT * S;
-    static constexpr size_t es = sizeof(T);
-    size_t tile_udz, tile_bc, stage, off_raw, off_bf, off_cf, off_dd, off_part, off_y, off_bar, total;
+    using G = Geo<T, NPT, S, KC, TC>;
+    size_t tile_bc, stage, off_raw, off_bf, off_cf, off_dd, off_y, off_bar, total;
     __host__ __device__ explicit Layout(int64_t N) {
-        tile_udz = round128(size_t(TC) * DT * es);
-        tile_bc = round128(size_t(TC) * size_t(N) * es);
-        stage = 3 * tile_udz + 2 * tile_bc;
+        tile_bc = round1k(size_t(TC) * size_t(N) * G::ES);
+        stage = 3 * G::TILE + 2 * tile_bc;
         off_raw = 0;
         off_bf = off_raw + kStages * stage;
-        off_cf = off_bf + round128(size_t(TC) * NP * 4);
-        off_dd = off_cf + round128(size_t(TC) * NP * 4);
-        off_part = off_dd + round128(size_t(TC) * DT * 8);
-        off_y = off_part + round128(size_t(TC) * kThreads * 4);
-        off_bar = off_y + 2 * tile_udz;
-        total = off_bar + 128;
+        off_cf = off_bf + round1k(size_t(TC) * G::NP * 4);
+        off_dd = off_cf + round1k(size_t(TC) * G::NP * 4);
+        off_y = off_dd + round1k(2 * kWarps * G::DD_WARP);
+        off_bar = off_y + 2 * G::TILE;
+        total = off_bar + 64;
     }
 };
 
-template <typename T, int NPT, int S, int TC>
+template <typename T, int NPT, int S, int KC, int TC>
 __global__ void __launch_bounds__(kThreads)
     ssm_scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u,
                         const __grid_constant__ CUtensorMap tm_dt,
@@ -250,52 +359,45 @@ __global__ void __launch_bounds__(kThreads)
                         const __grid_constant__ CUtensorMap tm_C,
                         const __grid_constant__ CUtensorMap tm_y, const KParams p) {
     using E = Elt<T>;
-    using Lay = Layout<T, NPT, S, TC>;
-    constexpr int DT = Lay::DT;
-    constexpr int NP = Lay::NP;
-    static_assert(kThreads % S == 0 && TC % S == 0, "bad tiling");
+    using G = Geo<T, NPT, S, KC, TC>;
+    using TT = typename G::TileT;
+    constexpr int DT = G::DT, NP = G::NP, CGW = G::CGW, CW = G::CW, ES = G::ES;
+    constexpr int RS = TT::RS, NB = TT::NB;
+    constexpr int NG = TC / S;  // groups per chunk
 
     extern __shared__ unsigned char smem_raw[];
     __shared__ int s_abort;
-    // Align the dynamic shared-memory base to 128 bytes (TMA destinations).
-    unsigned char* base =
-        smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-    const Lay lay(p.N);
+    unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const Layout<T, NPT, S, KC, TC> lay(p.N);
 
     const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int q = lane / S, sl = lane % S;         // channel group in warp, lane in group
     const int64_t N = p.N, L = p.L, dim = p.dim;
     const int64_t b = blockIdx.x / p.nblk_d;
     const int64_t d0 = (blockIdx.x % p.nblk_d) * DT;
+    const int cl0 = warp * CW + q * KC;            // first channel of this lane in the tile
 
-    // Stage s of the raw ring holds the u, delta, z tiles [TC][DT] then the
-    // B, C tiles [TC][N], each at a 128-byte aligned offset.
-    auto raw_u = [&](int s) { return reinterpret_cast<T*>(base + lay.off_raw + s * lay.stage); };
-    auto raw_dt = [&](int s) {
-        return reinterpret_cast<T*>(base + lay.off_raw + s * lay.stage + lay.tile_udz);
-    };
-    auto raw_z = [&](int s) {
-        return reinterpret_cast<T*>(base + lay.off_raw + s * lay.stage + 2 * lay.tile_udz);
-    };
-    auto raw_B = [&](int s) {
-        return reinterpret_cast<T*>(base + lay.off_raw + s * lay.stage + 3 * lay.tile_udz);
-    };
-    auto raw_C = [&](int s) {
-        return reinterpret_cast<T*>(base + lay.off_raw + s * lay.stage + 3 * lay.tile_udz +
-                                    lay.tile_bc);
-    };
-    float* s_B = reinterpret_cast<float*>(base + lay.off_bf);       // [TC][NP]
-    float* s_C = reinterpret_cast<float*>(base + lay.off_cf);       // [TC][NP]
-    float2* s_dd = reinterpret_cast<float2*>(base + lay.off_dd);    // [TC][DT] (dt, dt*u)
-    float* s_part = reinterpret_cast<float*>(base + lay.off_part);  // [TC][DT][S]
-    T* const s_y0 = reinterpret_cast<T*>(base + lay.off_y);  // two [TC][DT] output tiles
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + lay.off_bar);  // [kStages] + debug
-    const uint32_t bar0 = smem_u32(bars);
+    unsigned char* const raw0 = base + lay.off_raw;
+    const uint32_t stage_b = uint32_t(lay.stage), tbc = uint32_t(lay.tile_bc);
+    constexpr uint32_t TILE = uint32_t(G::TILE);
+    auto raw_u = [=](int s) { return raw0 + s * stage_b; };
+    auto raw_dt = [=](int s) { return raw0 + s * stage_b + TILE; };
+    auto raw_z = [=](int s) { return raw0 + s * stage_b + 2 * TILE; };
+    auto raw_B = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + 3 * TILE); };
+    auto raw_C = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + 3 * TILE + tbc); };
+    float* const s_B = reinterpret_cast<float*>(base + lay.off_bf);
+    float* const s_C = reinterpret_cast<float*>(base + lay.off_cf);
+    float4* const s_dd = reinterpret_cast<float4*>(base + lay.off_dd);
+    unsigned char* const s_y0 = base + lay.off_y;
+    const uint32_t bar0 = smem_u32(base + lay.off_bar);
     const uint32_t bar_never = bar0 + 8 * kStages;  // a barrier nothing ever completes
 
     const bool has_z = p.z != nullptr;
     const int64_t nchunks = (L + TC - 1) / TC;
-    const uint32_t tx_bytes = uint32_t((has_z ? 3 : 2) * TC * DT * sizeof(T)) +
-                              (p.tma_bc ? uint32_t(2 * TC * N * sizeof(T)) : 0u);
+    const uint32_t tx_bytes = uint32_t((has_z ? 3 : 2) * TC * G::WB) +
+                              (p.tma_bc ? uint32_t(2 * TC * N * ES) : 0u);
+    const bool bc_vec = p.tma_bc && N == NP && (N % 4) == 0;
 
     if (tid == 0) {
         s_abort = 0;
@@ -304,40 +406,40 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
 
-    // Issue the TMA loads of chunk cc into stage ss (thread 0 only).
-    auto issue_loads = [&](int64_t cc, int ss) {
+    auto issue_loads = [&](int64_t cc, int ss) {  // thread 0 only
         const uint32_t bar = bar0 + 8 * ss;
         const int t0 = int(cc * TC);
         mbar_arrive_expect_tx(bar, tx_bytes);
-        tma_load_3d(smem_u32(raw_u(ss)), &tm_u, int(d0), t0, int(b), bar);
-        tma_load_3d(smem_u32(raw_dt(ss)), &tm_dt, int(d0), t0, int(b), bar);
-        if (has_z) tma_load_3d(smem_u32(raw_z(ss)), &tm_z, int(d0), t0, int(b), bar);
+#pragma unroll
+        for (int cb = 0; cb < NB; ++cb) {
+            const int x = int(d0) + cb * (RS / ES);
+            const uint32_t o = uint32_t(cb * TC * RS);
+            tma_load_3d(smem_u32(raw_u(ss) + o), &tm_u, x, t0, int(b), bar);
+            tma_load_3d(smem_u32(raw_dt(ss) + o), &tm_dt, x, t0, int(b), bar);
+            if (has_z) tma_load_3d(smem_u32(raw_z(ss) + o), &tm_z, x, t0, int(b), bar);
+        }
         if (p.tma_bc) {
             tma_load_3d(smem_u32(raw_B(ss)), &tm_B, 0, t0, int(b), bar);
             tma_load_3d(smem_u32(raw_C(ss)), &tm_C, 0, t0, int(b), bar);
         }
     };
 
-    // ---- SCAN role: channel ch of the tile, lane sl of its S lanes.
-    const int ch = tid / S;
-    const int sl = tid % S;
-    const int64_t d_scan = d0 + ch;
-    const bool scan_valid = d_scan < dim;
-    float a2[NPT], h[NPT];
+    // ---- this lane's channels: parameters, state
+    float a2[KC][NPT], h[KC][NPT];
+    float bias[KC], dsk[KC];
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) {
-        const int64_t n = int64_t(sl) * NPT + j;
-        a2[j] = (scan_valid && n < N) ? p.A[d_scan * N + n] * kLog2e : 0.f;
-        h[j] = 0.f;
+    for (int k = 0; k < KC; ++k) {
+        const int64_t d = d0 + cl0 + k;
+        const bool ok = d < dim;
+        bias[k] = (p.bias != nullptr && ok) ? p.bias[d] : 0.f;
+        dsk[k] = (p.D != nullptr && ok) ? p.D[d] : 0.f;
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+            const int64_t n = int64_t(sl) * NPT + j;
+            a2[k][j] = (ok && n < N) ? p.A[d * N + n] * kLog2e : 0.f;
+            h[k][j] = 0.f;
+        }
     }
-
-    // ---- PREP / POST role: channel dd of the tile, timesteps tq, tq+S, ...
-    const int dd = tid % DT;
-    const int tq = tid / DT;
-    const int64_t d_pp = d0 + dd;
-    const bool pp_valid = d_pp < dim;
-    const float bias = (p.bias != nullptr && pp_valid) ? p.bias[d_pp] : 0.f;
-    const float Dsk = (p.D != nullptr && pp_valid) ? p.D[d_pp] : 0.f;
 
     const T* gu = static_cast<const T*>(p.u);
     const T* gdt = static_cast<const T*>(p.delta);
@@ -363,42 +465,48 @@ __global__ void __launch_bounds__(kThreads)
                 *reinterpret_cast<volatile int*>(&s_abort) = 1;
             }
         } else {
-            // Plain loads of the chunk's u / delta / z tiles (zero outside the tensor).
+            // Plain loads of the chunk's u / delta / z tiles, same swizzled layout,
+            // zero outside the tensor.
             for (int i = tid; i < TC * DT; i += kThreads) {
                 const int t = i / DT, k = i % DT;
                 const int64_t gt = t0 + t, gd = d0 + k;
                 const bool in = gt < L && gd < dim;
                 const int64_t off = (b * L + gt) * dim + gd;
-                raw_u(st)[i] = in ? gu[off] : E::from_f(0.f);
-                raw_dt(st)[i] = in ? gdt[off] : E::from_f(0.f);
-                if (has_z) raw_z(st)[i] = in ? gz[off] : E::from_f(0.f);
+                const uint32_t o = TT::off(t, k * ES, TC);
+                *reinterpret_cast<T*>(raw_u(st) + o) = in ? gu[off] : E::from_f(0.f);
+                *reinterpret_cast<T*>(raw_dt(st) + o) = in ? gdt[off] : E::from_f(0.f);
+                if (has_z) *reinterpret_cast<T*>(raw_z(st) + o) = in ? gz[off] : E::from_f(0.f);
             }
         }
 
-        // ---------------- PREP: widen B, C; dt = softplus(delta + bias); dt*u
-        for (int i = tid; i < TC * NP; i += kThreads) {
-            const int t = i / NP, n = i % NP;
-            float bv = 0.f, cv = 0.f;
-            if (n < N && t < tv) {
-                if (p.tma_bc) {
-                    bv = E::to_f(raw_B(st)[t * N + n]);
-                    cv = E::to_f(raw_C(st)[t * N + n]);
-                } else {
-                    const int64_t off = (b * L + t0 + t) * N + n;
-                    bv = E::to_f(gB[off]);
-                    cv = E::to_f(gC[off]);
-                }
+        // B, C widened to fp32 (rows past L are zero: TMA fills them, or we do).
+        if (bc_vec) {
+            const int items = TC * NP / 4;
+            for (int i = tid; i < 2 * items; i += kThreads) {
+                const bool isC = i >= items;
+                const int j = (isC ? i - items : i) * 4;
+                const float4 qv = ld_quad<T>((isC ? raw_C(st) : raw_B(st)) + j);
+                *reinterpret_cast<float4*>((isC ? s_C : s_B) + j) = qv;
             }
-            s_B[i] = bv;
-            s_C[i] = cv;
+        } else {
+            for (int i = tid; i < TC * NP; i += kThreads) {
+                const int t = i / NP, n = i % NP;
+                float bv = 0.f, cv = 0.f;
+                if (n < N && t < tv) {
+                    if (p.tma_bc) {
+                        bv = E::to_f(raw_B(st)[t * N + n]);
+                        cv = E::to_f(raw_C(st)[t * N + n]);
+                    } else {
+                        const int64_t off = (b * L + t0 + t) * N + n;
+                        bv = E::to_f(gB[off]);
+                        cv = E::to_f(gC[off]);
+                    }
+                }
+                s_B[i] = bv;
+                s_C[i] = cv;
+            }
         }
-        if (!p.tma_udz) __syncthreads();  // plain-loaded tiles visible to PREP
-        for (int t = tq; t < tv; t += S) {
-            const float x = E::to_f(raw_dt(st)[t * DT + dd]) + bias;
-            const float dt = p.softplus ? Act<T>::softplus(x) : x;
-            const float uu = E::to_f(raw_u(st)[t * DT + dd]);
-            s_dd[t * DT + dd] = make_float2(dt, dt * uu);
-        }
+        if (p.tma_udz && tid == 0) bulk_wait_read_le1();  // this chunk's output tile is free
         __syncthreads();
         if (*reinterpret_cast<volatile int*>(&s_abort)) {
             // Give up: wait (bounded) for this block's own loads in flight, then
@@ -416,45 +524,114 @@ __global__ void __launch_bounds__(kThreads)
             return;
         }
 
-        // ---------------- SCAN: NPT states per lane over the chunk
-        {
-            const float* Bp = s_B + sl * NPT;
-            const float* Cp = s_C + sl * NPT;
-            for (int t = 0; t < tv; ++t) {
-                const float2 v = s_dd[t * DT + ch];
-                float part = 0.f;
-#pragma unroll
-                for (int j = 0; j < NPT; ++j) {
-                    const float e = ex2_approx(v.x * a2[j]);
-                    h[j] = fmaf(e, h[j], v.y * Bp[t * NP + j]);
-                    part = fmaf(Cp[t * NP + j], h[j], part);
-                }
-                s_part[(t * DT + ch) * S + sl] = part;
-            }
-        }
-        if (p.tma_udz && tid == 0) bulk_wait_read_le1();  // s_y[c & 1] free again
-        __syncthreads();
+        // ---------------- per-warp pipeline over the chunk's groups of S steps.
+        // PREP(g): this lane computes step g*S + sl of its KC channels -- dt,
+        //   dt*u for the group's scan (shared through s_dd), and the gate g and
+        //   skip D*u*g, which it keeps for POST(g).
+        // SCAN(g): every lane advances its KC x NPT states over the S steps.
+        // reduce + POST(g): the transposed reduction leaves the full readout of
+        //   step g*S + sl in this lane, which applies skip and gate and writes y.
+        // PREP(g+1) is issued before SCAN(g) (double-buffered s_dd).
+        unsigned char* yt = s_y0 + (c & 1) * TILE;
+        const unsigned char* ru = raw_u(st);
+        const unsigned char* rdt = raw_dt(st);
+        const unsigned char* rz = raw_z(st);
+        float gate[2][KC], skip[2][KC];
 
-        // ---------------- POST: y = (sum of partials + D u) * silu(z)
-        T* yt = s_y0 + (c & 1) * (lay.tile_udz / sizeof(T));
-        for (int t = tq; t < tv; t += S) {
-            float acc = 0.f;
+        auto prep = [&](int g, int buf) {  // buf is a constant at every call site
+            const int t = g * S + sl;
+            const uint32_t o = TT::off(t, cl0 * ES, TC);
+            float xr[KC], uu[KC], zz[KC];
+            ld_k<T, KC>(rdt + o, xr);
+            ld_k<T, KC>(ru + o, uu);
+            if (has_z) ld_k<T, KC>(rz + o, zz);
+            const bool live = t < tv;
+            float4* dd = s_dd + (buf * kWarps + warp) * (S * KC * CGW);
 #pragma unroll
-            for (int s = 0; s < S; ++s) acc += s_part[(t * DT + dd) * S + s];
-            const float uu = E::to_f(raw_u(st)[t * DT + dd]);
-            acc = fmaf(Dsk, uu, acc);
-            if (has_z) acc *= Act<T>::silu(E::to_f(raw_z(st)[t * DT + dd]));
-            if (p.tma_udz) {
-                yt[t * DT + dd] = E::from_f(acc);
-            } else if (pp_valid) {
-                gy[(b * L + t0 + t) * dim + d_pp] = E::from_f(acc);
+            for (int k = 0; k < KC; ++k) {
+                float x = xr[k] + bias[k];
+                if (p.softplus) x = Act<T>::softplus(x);
+                const float xu = x * uu[k];
+                const float gg = has_z ? Act<T>::silu(zz[k]) : 1.f;
+                gate[buf][k] = gg;
+                skip[buf][k] = dsk[k] * uu[k] * gg;
+                dd[(sl * KC + k) * CGW + q] =
+                    live ? make_float4(x, x, xu, xu) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+        };
+
+        // One group: issue PREP of the next group, then SCAN, reduce and POST of
+        // this one.  BUF is compile-time so gate/skip stay in registers.
+        auto group = [&](int g, auto buf_tag) {
+            constexpr int buf = decltype(buf_tag)::value;
+            if (g + 1 < NG) prep(g + 1, buf ^ 1);
+            const float4* dd = s_dd + (buf * kWarps + warp) * (S * KC * CGW);
+            float pv[KC][S];
+#pragma unroll
+            for (int qq = 0; qq < S; ++qq) {
+                const int t = g * S + qq;
+                float bb[NPT], cc[NPT];
+                ld_states<NPT>(s_B + t * NP + sl * NPT, bb);
+                ld_states<NPT>(s_C + t * NP + sl * NPT, cc);
+#pragma unroll
+                for (int k = 0; k < KC; ++k) {
+                    const float4 v = dd[(qq * KC + k) * CGW + q];
+                    if constexpr (NPT == 1) {
+                        const float e = ex2_approx(v.x * a2[k][0]);
+                        h[k][0] = fmaf(e, h[k][0], v.z * bb[0]);
+                        pv[k][qq] = cc[0] * h[k][0];
+                    } else {
+                        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int j = 0; j < NPT; j += 2) {
+                            const float2 x = __fmul2_rn(make_float2(v.x, v.y),
+                                                        make_float2(a2[k][j], a2[k][j + 1]));
+                            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                            const float2 w = __fmul2_rn(make_float2(v.z, v.w),
+                                                        make_float2(bb[j], bb[j + 1]));
+                            const float2 hh = __ffma2_rn(e, make_float2(h[k][j], h[k][j + 1]), w);
+                            h[k][j] = hh.x;
+                            h[k][j + 1] = hh.y;
+                            acc = __ffma2_rn(make_float2(cc[j], cc[j + 1]), hh, acc);
+                        }
+                        pv[k][qq] = acc.x + acc.y;
+                    }
+                }
+            }
+            if constexpr (S > 1) reduce_transposed<S, KC>(pv, sl);
+            // POST: step g*S + sl of this lane's channels.
+            const int t = g * S + sl;
+            float yv[KC];
+#pragma unroll
+            for (int k = 0; k < KC; ++k) yv[k] = fmaf(pv[k][0], gate[buf][k], skip[buf][k]);
+            if (p.tma_udz) {
+                st_k<T, KC>(yt + TT::off(t, cl0 * ES, TC), yv);
+            } else if (t < tv) {
+#pragma unroll
+                for (int k = 0; k < KC; ++k)
+                    if (d0 + cl0 + k < dim)
+                        gy[(b * L + t0 + t) * dim + d0 + cl0 + k] = E::from_f(yv[k]);
+            }
+            __syncwarp();
+        };
+
+        prep(0, 0);
+        __syncwarp();
+        static_assert(NG % 2 == 0, "groups per chunk must be even");
+#pragma unroll 1
+        for (int g = 0; g < NG; g += 2) {
+            group(g, std::integral_constant<int, 0>{});
+            group(g + 1, std::integral_constant<int, 1>{});
         }
+
         if (p.tma_udz) {
             fence_proxy_async_smem();
             __syncthreads();
             if (tid == 0) {
-                tma_store_3d(&tm_y, int(d0), int(t0), int(b), smem_u32(yt));
+#pragma unroll
+                for (int cb = 0; cb < NB; ++cb)
+                    tma_store_3d(&tm_y, int(d0) + cb * (RS / ES), int(t0), int(b),
+                                 smem_u32(yt + cb * TC * RS));
                 bulk_commit();
             }
         } else {
@@ -463,11 +640,16 @@ __global__ void __launch_bounds__(kThreads)
     }
     if (p.tma_udz && tid == 0) bulk_wait_all();
 
-    if (p.h_last != nullptr && scan_valid) {
+    if (p.h_last != nullptr) {
 #pragma unroll
-        for (int j = 0; j < NPT; ++j) {
-            const int64_t n = int64_t(sl) * NPT + j;
-            if (n < N) p.h_last[(b * dim + d_scan) * N + n] = h[j];
+        for (int k = 0; k < KC; ++k) {
+            const int64_t d = d0 + cl0 + k;
+            if (d >= dim) continue;
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) {
+                const int64_t n = int64_t(sl) * NPT + j;
+                if (n < N) p.h_last[(b * dim + d) * N + n] = h[k][j];
+            }
         }
     }
 }
@@ -476,7 +658,7 @@ __global__ void __launch_bounds__(kThreads)
 std::atomic<int64_t> g_wait_ns{2000000000LL};
 std::atomic<int> g_force_timeout{0};
 std::atomic<int> g_force_lanes{0};
-std::atomic<int> g_force_chunk{0};
+std::atomic<int> g_force_kc{0};
 std::atomic<int> g_plain_loads{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -484,18 +666,18 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static std::once_flag once;
     std::call_once(once, [] {
         void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
+        cudaDriverEntryPointQueryResult qr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
+                                             cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
     });
     return fn;
 }
 
-// 3-D map over a (outer, mid, inner) = (batch, L, inner) row-major tensor.
+// 3-D map over a (batch, L, inner) row-major tensor; box = box_inner x box_t x 1.
 bool encode3d(CUtensorMap* tm, CUtensorMapDataType ty, size_t es, const void* ptr, int64_t inner,
-              int64_t L, int64_t batch, int box_inner, int box_t) {
+              int64_t L, int64_t batch, int box_inner, int box_t, CUtensorMapSwizzle swz) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t gdim[3] = {cuuint64_t(inner), cuuint64_t(L), cuuint64_t(batch)};
@@ -503,15 +685,18 @@ bool encode3d(CUtensorMap* tm, CUtensorMapDataType ty, size_t es, const void* pt
     cuuint32_t box[3] = {cuuint32_t(box_inner), cuuint32_t(box_t), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(tm, ty, 3, const_cast<void*>(ptr), gdim, gstride, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
+constexpr int kTC = 32;  // timesteps per chunk
+
 struct Plan {
-    int S = 1, NPT = 1, TC = 32, DT = kThreads;
+    int S = 1, NPT = 1, KC = 1, TC = kTC, DT = kThreads;
     int64_t grid = 0;
     size_t smem = 0;
+    int row_span = 16;
     bool tma_udz = false, tma_bc = false;
 };
 
@@ -521,46 +706,90 @@ int supported_npt(int64_t need) {
     return 0;
 }
 
-// Relative cost model used to pick the lanes per channel S:
-// per-thread work per timestep = NPT inner updates + per-timestep overheads +
-// this thread's share of the per-(t, d) PREP/POST work; the machine runs
-// ceil(warps / warp slots) rounds of it, and a round with fewer than two warps
-// per scheduler hides latency poorly.
-double plan_cost(int64_t channels, int S, int npt) {
+// Relative cost model for the lane split (S lanes per channel group, KC
+// channels x NPT states per lane).  Per lane and time step: the state updates
+// (~3.3 issue slots per state with packed f32x2 math, plus per-step loads),
+// this lane's share of the per-(t, d) work, and the transposed reduction.  The
+// machine runs ceil(warps / schedulers) rounds; a round with fewer than two
+// warps per scheduler hides latency poorly.
+double plan_cost(int64_t channels, int S, int npt, int kc) {
     const double slots = 148.0 * 4.0;
-    const double warps = std::ceil(double(channels) * S / 32.0);
+    const double warps = std::ceil(double(channels) * S / (32.0 * kc));
     const double rounds = std::ceil(warps / slots);
     const double per_sched = warps / slots;
     const double eff = per_sched >= 2.0 ? 1.0 : (0.55 + 0.225 * per_sched);
-    const double per_thread = npt * 3.3 + 3.0 + 30.0 / S;
-    return rounds * per_thread / eff;
+    const double lg = S == 8 ? 3 : S == 4 ? 2 : S == 2 ? 1 : 0;
+    const double per_lane = kc * (npt * 3.3 + 1.5) + 2.0 * std::ceil(npt / 4.0) +
+                            kc * 24.0 / S + kc * 2.0 * lg;
+    return rounds * per_lane / eff;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, size_t es, const void* u,
-               const void* dt, const void* z, const void* y, const void* Bp, const void* Cp) {
+template <typename T, int NPT, int S, int KC>
+size_t smem_bytes(int64_t N) {
+    return Layout<T, NPT, S, KC, kTC>(N).total + 1024;
+}
+
+#define SSM_FOR_EACH_VARIANT(X)                                                          \
+    X(1, 1, 1) X(2, 1, 1) X(4, 1, 1) X(8, 1, 1) X(16, 1, 1)                              \
+    X(1, 2, 1) X(2, 2, 1) X(4, 2, 1) X(8, 2, 1) X(16, 2, 1)                              \
+    X(1, 4, 1) X(2, 4, 1) X(4, 4, 1) X(8, 4, 1) X(16, 4, 1)                              \
+    X(1, 8, 1) X(2, 8, 1) X(4, 8, 1) X(8, 8, 1) X(16, 8, 1)                              \
+    X(2, 2, 2) X(4, 2, 2) X(8, 2, 2) X(2, 4, 2) X(4, 4, 2) X(8, 4, 2) X(2, 8, 2) X(4, 8, 2)
+
+bool variant_exists(int npt, int S, int kc) {
+#define SSM_EXISTS(NPT_, S_, KC_) \
+    if (npt == NPT_ && S == S_ && kc == KC_) return true;
+    SSM_FOR_EACH_VARIANT(SSM_EXISTS)
+#undef SSM_EXISTS
+    return false;
+}
+
+template <typename T>
+size_t variant_smem(int npt, int S, int kc, int64_t N) {
+#define SSM_SMEM(NPT_, S_, KC_) \
+    if (npt == NPT_ && S == S_ && kc == KC_) return smem_bytes<T, NPT_, S_, KC_>(N);
+    SSM_FOR_EACH_VARIANT(SSM_SMEM)
+#undef SSM_SMEM
+    return 0;
+}
+
+template <typename T>
+Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, const void* dt,
+               const void* z, const void* y, const void* Bp, const void* Cp) {
+    const size_t es = sizeof(T);
     Plan pl;
     const int64_t channels = batch * dim;
-    int best_S = 0;
     double best = 1e300;
-    const int forced = g_force_lanes.load();
-    for (int S : {1, 2, 4, 8}) {
-        const int npt = supported_npt((N + S - 1) / S);
-        if (npt == 0) continue;
-        if (S > 1 && N <= int64_t(S / 2) * npt) continue;  // a whole lane would be padding
-        if (forced != 0 && S != forced) continue;
-        const double cst = plan_cost(channels, S, npt);
-        if (cst < best) {
-            best = cst;
-            best_S = S;
+    const int forced_s = g_force_lanes.load(), forced_kc = g_force_kc.load();
+    for (int kc : {1, 2}) {
+        for (int S : {1, 2, 4, 8}) {
+            const int npt = supported_npt((N + S - 1) / S);
+            if (npt == 0 || !variant_exists(npt, S, kc)) continue;
+            if (S > 1 && N <= int64_t(S / 2) * npt) continue;  // a whole lane would be padding
+            if (forced_s != 0 && S != forced_s) continue;
+            if (forced_kc != 0 && kc != forced_kc) continue;
+            if (variant_smem<T>(npt, S, kc, N) > kMaxSmem) continue;
+            const double cst = plan_cost(channels, S, npt, kc);
+            if (cst < best) {
+                best = cst;
+                pl.S = S;
+                pl.NPT = npt;
+                pl.KC = kc;
+            }
         }
     }
-    if (best_S == 0) best_S = 8;  // N too large for smaller S (N <= 128 checked by caller)
-    pl.S = best_S;
-    pl.NPT = supported_npt((N + pl.S - 1) / pl.S);
-    pl.TC = g_force_chunk.load() == 64 ? 64 : 32;
-    pl.DT = kThreads / pl.S;
+    if (best == 1e300) {  // forced choice not available: fall back to automatic
+        pl.S = N > 64 ? 8 : N > 32 ? 4 : N > 16 ? 2 : 1;
+        pl.NPT = supported_npt((N + pl.S - 1) / pl.S);
+        pl.KC = 1;
+    }
+    pl.TC = kTC;
+    pl.DT = kWarps * (32 / pl.S) * pl.KC;
+    pl.smem = variant_smem<T>(pl.NPT, pl.S, pl.KC, N);
+    const int wb = pl.DT * int(es);
+    pl.row_span = wb < 128 ? wb : 128;
     const int64_t nblk = (dim + pl.DT - 1) / pl.DT;
     pl.grid = nblk * batch;
     const bool plain = g_plain_loads.load() != 0;
@@ -573,16 +802,10 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, size_t es, cons
     return pl;
 }
 
-template <typename T, int NPT, int S>
-size_t smem_bytes(int64_t N, int TC) {
-    if (TC == 64) return Layout<T, NPT, S, 64>(N).total + 128;
-    return Layout<T, NPT, S, 32>(N).total + 128;
-}
-
-template <typename T, int NPT, int S, int TC>
+template <typename T, int NPT, int S, int KC>
 int launch_one(const Plan& pl, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
-    auto kern = ssm_scan_fwd_kernel<T, NPT, S, TC>;
-    const size_t smem = Layout<T, NPT, S, TC>(kp.N).total + 128;
+    auto kern = ssm_scan_fwd_kernel<T, NPT, S, KC, kTC>;
+    const size_t smem = smem_bytes<T, NPT, S, KC>(kp.N);
     // The opt-in shared-memory limit is a per-device function attribute.
     static std::atomic<size_t> configured[64];
     int dev = 0;
@@ -599,34 +822,20 @@ int launch_one(const Plan& pl, const CUtensorMap* tms, const KParams& kp, cudaSt
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
-template <typename T, int NPT, int S>
-int launch_tc(const Plan& pl, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
-    if (pl.TC == 64) return launch_one<T, NPT, S, 64>(pl, tms, kp, stream);
-    return launch_one<T, NPT, S, 32>(pl, tms, kp, stream);
-}
-
 template <typename T>
 int dispatch(const Plan& pl, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
-#define SSM_CASE(NPT_, S_) \
-    if (pl.NPT == NPT_ && pl.S == S_) return launch_tc<T, NPT_, S_>(pl, tms, kp, stream);
-    SSM_CASE(1, 1) SSM_CASE(2, 1) SSM_CASE(4, 1) SSM_CASE(8, 1) SSM_CASE(16, 1)
-    SSM_CASE(1, 2) SSM_CASE(2, 2) SSM_CASE(4, 2) SSM_CASE(8, 2) SSM_CASE(16, 2)
-    SSM_CASE(1, 4) SSM_CASE(2, 4) SSM_CASE(4, 4) SSM_CASE(8, 4) SSM_CASE(16, 4)
-    SSM_CASE(1, 8) SSM_CASE(2, 8) SSM_CASE(4, 8) SSM_CASE(8, 8) SSM_CASE(16, 8)
+#define SSM_CASE(NPT_, S_, KC_) \
+    if (pl.NPT == NPT_ && pl.S == S_ && pl.KC == KC_) return launch_one<T, NPT_, S_, KC_>(pl, tms, kp, stream);
+    SSM_FOR_EACH_VARIANT(SSM_CASE)
 #undef SSM_CASE
     return SSM_ERR_UNSUPPORTED_N;
 }
 
-template <typename T>
-size_t plan_smem(const Plan& pl, int64_t N) {
-#define SSM_CASE(NPT_, S_) \
-    if (pl.NPT == NPT_ && pl.S == S_) return smem_bytes<T, NPT_, S_>(N, pl.TC);
-    SSM_CASE(1, 1) SSM_CASE(2, 1) SSM_CASE(4, 1) SSM_CASE(8, 1) SSM_CASE(16, 1)
-    SSM_CASE(1, 2) SSM_CASE(2, 2) SSM_CASE(4, 2) SSM_CASE(8, 2) SSM_CASE(16, 2)
-    SSM_CASE(1, 4) SSM_CASE(2, 4) SSM_CASE(4, 4) SSM_CASE(8, 4) SSM_CASE(16, 4)
-    SSM_CASE(1, 8) SSM_CASE(2, 8) SSM_CASE(4, 8) SSM_CASE(8, 8) SSM_CASE(16, 8)
-#undef SSM_CASE
-    return 0;
+CUtensorMapSwizzle swizzle_for(int row_span) {
+    return row_span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                           : (row_span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : (row_span == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                               : CU_TENSOR_MAP_SWIZZLE_NONE));
 }
 
 bool mul_ok(int64_t a, int64_t b, int64_t* out) {
@@ -673,8 +882,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     if (overlaps(y, by, h_last, bh)) return SSM_ERR_ALIAS;
     if (batch == 0 || dim == 0) return SSM_OK;  // nothing to compute
 
-    Plan pl = make_plan(batch, L, dim, N, es, u, delta, z, y, B, C);
-    if (plan_smem<typename Elt<T>::S>(pl, N) > kMaxSmem) pl.TC = 32;  // chunk 64 does not fit
+    const Plan pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C);
     if (pl.grid > int64_t(0x7fffffff)) return SSM_ERR_SIZE;
 
     CUtensorMap tms[6];
@@ -682,13 +890,17 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     bool tma_udz = pl.tma_udz, tma_bc = pl.tma_bc;
     if (tma_udz) {
         const auto ty = Elt<T>::tmap_type;
-        tma_udz = encode3d(&tms[0], ty, es, u, dim, L, batch, pl.DT, pl.TC) &&
-                  encode3d(&tms[1], ty, es, delta, dim, L, batch, pl.DT, pl.TC) &&
-                  encode3d(&tms[2], ty, es, z ? z : u, dim, L, batch, pl.DT, pl.TC) &&
-                  encode3d(&tms[5], ty, es, y, dim, L, batch, pl.DT, pl.TC);
+        const int box = pl.row_span / int(es);
+        const auto swz = swizzle_for(pl.row_span);
+        tma_udz = encode3d(&tms[0], ty, es, u, dim, L, batch, box, pl.TC, swz) &&
+                  encode3d(&tms[1], ty, es, delta, dim, L, batch, box, pl.TC, swz) &&
+                  encode3d(&tms[2], ty, es, z ? z : u, dim, L, batch, box, pl.TC, swz) &&
+                  encode3d(&tms[5], ty, es, y, dim, L, batch, box, pl.TC, swz);
         if (tma_udz && tma_bc)
-            tma_bc = encode3d(&tms[3], ty, es, B, N, L, batch, int(N), pl.TC) &&
-                     encode3d(&tms[4], ty, es, C, N, L, batch, int(N), pl.TC);
+            tma_bc = encode3d(&tms[3], ty, es, B, N, L, batch, int(N), pl.TC,
+                              CU_TENSOR_MAP_SWIZZLE_NONE) &&
+                     encode3d(&tms[4], ty, es, C, N, L, batch, int(N), pl.TC,
+                              CU_TENSOR_MAP_SWIZZLE_NONE);
         if (!tma_udz) tma_bc = false;
     }
 
@@ -713,7 +925,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     kp.tma_udz = tma_udz ? 1 : 0;
     kp.tma_bc = tma_bc ? 1 : 0;
     kp.force_timeout = (tma_udz && g_force_timeout.load()) ? 1 : 0;
-    return dispatch<typename Elt<T>::S>(pl, tms, kp, stream);
+    return dispatch<T>(pl, tms, kp, stream);
 }
 
 }  // namespace
@@ -775,20 +987,18 @@ int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype, i
     if (batch < 0 || L < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED_N;
     if (dtype != 0 && dtype != 1) return SSM_ERR_ARG;
-    const size_t es = dtype == 1 ? 2 : 4;
     // Plan for 256-byte aligned buffers (what cudaMalloc returns).
     const void* al = reinterpret_cast<const void*>(uintptr_t(256));
-    Plan pl = make_plan(batch, L, dim, N, es, al, al, al, al, al, al);
-    const size_t sm = dtype == 1 ? plan_smem<__nv_bfloat16>(pl, N) : plan_smem<float>(pl, N);
-    if (sm > kMaxSmem) pl.TC = 32;
+    const Plan pl = dtype == 1 ? make_plan<__nv_bfloat16>(batch, L, dim, N, al, al, al, al, al, al)
+                               : make_plan<float>(batch, L, dim, N, al, al, al, al, al, al);
     plan[0] = pl.S;
     plan[1] = pl.NPT;
     plan[2] = pl.TC;
     plan[3] = pl.DT;
     plan[4] = kThreads;
     plan[5] = pl.grid;
-    plan[6] = int64_t(dtype == 1 ? plan_smem<__nv_bfloat16>(pl, N) : plan_smem<float>(pl, N));
-    plan[7] = pl.tma_udz ? 1 : 0;
+    plan[6] = int64_t(pl.smem);
+    plan[7] = pl.KC;
     return SSM_OK;
 }
 
@@ -806,9 +1016,9 @@ int ssm_set_knob(int key, int64_t value) {
             if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return SSM_ERR_ARG;
             g_force_lanes.store(int(value));
             return SSM_OK;
-        case SSM_KNOB_CHUNK:
-            if (value != 0 && value != 32 && value != 64) return SSM_ERR_ARG;
-            g_force_chunk.store(int(value));
+        case SSM_KNOB_CHANNELS_PER_LANE:
+            if (value != 0 && value != 1 && value != 2) return SSM_ERR_ARG;
+            g_force_kc.store(int(value));
             return SSM_OK;
         case SSM_KNOB_PLAIN_LOADS:
             if (value != 0 && value != 1) return SSM_ERR_ARG;

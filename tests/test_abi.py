@@ -90,7 +90,7 @@ def test_knobs_validate():
     K = ssmscan
     assert ssm.ssm_set_knob(K.SSM_KNOB_WAIT_NS, 10) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(K.SSM_KNOB_LANES, 3) == K.SSM_ERR_ARG
-    assert ssm.ssm_set_knob(K.SSM_KNOB_CHUNK, 48) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(K.SSM_KNOB_CHANNELS_PER_LANE, 3) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(99, 0) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(K.SSM_KNOB_LANES, 0) == K.SSM_OK
     assert ssm.ssm_set_knob(K.SSM_KNOB_WAIT_NS, 2_000_000_000) == K.SSM_OK
@@ -103,10 +103,10 @@ def test_knobs_validate():
 def test_plans_cover_the_state(shape, dtype):
     pl = ssm.ssm_scan_plan(*shape, dtype)
     batch, L, dim, N = shape
-    S, npt = pl["lanes"], pl["states_per_lane"]
-    assert S in (1, 2, 4, 8) and npt in (1, 2, 4, 8, 16)
+    S, npt, kc = pl["lanes"], pl["states_per_lane"], pl["channels_per_lane"]
+    assert S in (1, 2, 4, 8) and npt in (1, 2, 4, 8, 16) and kc in (1, 2)
     assert S * npt >= N and (S == 1 or (S // 2) * npt < N)        # no all-padding lane
-    assert pl["threads"] == 128 and pl["channels_per_block"] * S == 128
+    assert pl["threads"] == 128 and pl["channels_per_block"] * S == 128 * kc
     assert pl["blocks"] == batch * -(-dim // pl["channels_per_block"])
     assert 0 < pl["smem_bytes"] <= 227 * 1024
 
