@@ -253,7 +253,7 @@ def config_of(wl: W.Workload, l2_note: str):
 
 # ----------------------------------------------------------------- reference arm
 def run_reference(args, wl):
-    world, rank, _ = (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0)
+    world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
     threads = os.cpu_count() or 1
