@@ -323,7 +323,7 @@ struct Geo {
     static constexpr int WB = DT * ES;        // tile row bytes
     using TileT = Tile<WB>;
     static constexpr size_t TILE = round1k(size_t(TC) * WB);
-    static constexpr size_t DD_WARP = size_t(S) * KC * CGW * 16;  // one group's (dt,dt,dtu,dtu)
+    static constexpr size_t DD_WARP = size_t(TC) * KC * CGW * 16;  // a chunk's (dt,dt,dtu,dtu)
     static_assert(TC % S == 0, "chunk must hold whole groups");
     static_assert(WB % 16 == 0 && (WB <= 128 || WB % 128 == 0), "tile rows");
 };
@@ -331,7 +331,7 @@ struct Geo {
 // Shared-memory layout of one block (bytes from a 1024-byte aligned base).
 //   raw ring  kStages x { u, delta, z : tile ; B, C : [TC][N] T }
 //   s_B, s_C  [TC][NP] fp32            B, C widened (rows past L are zero)
-//   s_dd      2 x kWarps x [S][KC][CGW] float4   (dt, dt, dt*u, dt*u) per group
+//   s_dd      kWarps x [TC][KC][CGW] float4   (dt, dt, dt*u, dt*u) per step
 //   s_y       2 x tile                  output tiles for the TMA store
 template <typename T, int NPT, int S, int KC, int TC>
 struct Layout {
@@ -344,7 +344,7 @@ struct Layout {
         off_bf = off_raw + kStages * stage;
         off_cf = off_bf + round1k(size_t(TC) * G::NP * 4);
         off_dd = off_cf + round1k(size_t(TC) * G::NP * 4);
-        off_y = off_dd + round1k(2 * kWarps * G::DD_WARP);
+        off_y = off_dd + round1k(kWarps * G::DD_WARP);
         off_bar = off_y + 2 * G::TILE;
         total = off_bar + 64;
     }
@@ -524,21 +524,25 @@ __global__ void __launch_bounds__(kThreads)
             return;
         }
 
-        // ---------------- per-warp pipeline over the chunk's groups of S steps.
-        // PREP(g): this lane computes step g*S + sl of its KC channels -- dt,
-        //   dt*u for the group's scan (shared through s_dd), and the gate g and
-        //   skip D*u*g, which it keeps for POST(g).
-        // SCAN(g): every lane advances its KC x NPT states over the S steps.
-        // reduce + POST(g): the transposed reduction leaves the full readout of
-        //   step g*S + sl in this lane, which applies skip and gate and writes y.
-        // PREP(g+1) is issued before SCAN(g) (double-buffered s_dd).
+        // ---------------- per-warp pipeline over the chunk, in four batched phases
+        // (batching keeps the long softplus / SiLU and shuffle latency chains of
+        // different groups independent, so they overlap):
+        // PREP: for each group g of S steps this lane computes step g*S + sl of
+        //   its KC channels -- dt and dt*u for the scan (shared with the group
+        //   through s_dd), the gate g and the skip D*u*g (kept in registers).
+        // SCAN: every lane advances its KC x NPT states over all TC steps and
+        //   keeps its partial readouts.
+        // REDUCE: per group, a transposed shuffle reduction leaves this lane the
+        //   full readout of exactly the item it prepared.
+        // POST: skip and gate in registers, y into the output tile.
         unsigned char* yt = s_y0 + (c & 1) * TILE;
         const unsigned char* ru = raw_u(st);
         const unsigned char* rdt = raw_dt(st);
         const unsigned char* rz = raw_z(st);
-        float gate[2][KC], skip[2][KC];
-
-        auto prep = [&](int g, int buf) {  // buf is a constant at every call site
+        float4* const ddw = s_dd + warp * (TC * KC * CGW);
+        float gate[NG][KC], skip[NG][KC];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
             const int t = g * S + sl;
             const uint32_t o = TT::off(t, cl0 * ES, TC);
             float xr[KC], uu[KC], zz[KC];
@@ -546,64 +550,61 @@ __global__ void __launch_bounds__(kThreads)
             ld_k<T, KC>(ru + o, uu);
             if (has_z) ld_k<T, KC>(rz + o, zz);
             const bool live = t < tv;
-            float4* dd = s_dd + (buf * kWarps + warp) * (S * KC * CGW);
 #pragma unroll
             for (int k = 0; k < KC; ++k) {
                 float x = xr[k] + bias[k];
                 if (p.softplus) x = Act<T>::softplus(x);
                 const float xu = x * uu[k];
                 const float gg = has_z ? Act<T>::silu(zz[k]) : 1.f;
-                gate[buf][k] = gg;
-                skip[buf][k] = dsk[k] * uu[k] * gg;
-                dd[(sl * KC + k) * CGW + q] =
+                gate[g][k] = gg;
+                skip[g][k] = dsk[k] * uu[k] * gg;
+                ddw[(t * KC + k) * CGW + q] =
                     live ? make_float4(x, x, xu, xu) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-        };
-
-        // One group: issue PREP of the next group, then SCAN, reduce and POST of
-        // this one.  BUF is compile-time so gate/skip stay in registers.
-        auto group = [&](int g, auto buf_tag) {
-            constexpr int buf = decltype(buf_tag)::value;
-            if (g + 1 < NG) prep(g + 1, buf ^ 1);
-            const float4* dd = s_dd + (buf * kWarps + warp) * (S * KC * CGW);
-            float pv[KC][S];
+        }
+        __syncwarp();
+        float pv[NG][KC][S];
 #pragma unroll
-            for (int qq = 0; qq < S; ++qq) {
-                const int t = g * S + qq;
-                float bb[NPT], cc[NPT];
-                ld_states<NPT>(s_B + t * NP + sl * NPT, bb);
-                ld_states<NPT>(s_C + t * NP + sl * NPT, cc);
+        for (int t = 0; t < TC; ++t) {
+            const int g = t / S, qq = t % S;
+            float bb[NPT], cc[NPT];
+            ld_states<NPT>(s_B + t * NP + sl * NPT, bb);
+            ld_states<NPT>(s_C + t * NP + sl * NPT, cc);
 #pragma unroll
-                for (int k = 0; k < KC; ++k) {
-                    const float4 v = dd[(qq * KC + k) * CGW + q];
-                    if constexpr (NPT == 1) {
-                        const float e = ex2_approx(v.x * a2[k][0]);
-                        h[k][0] = fmaf(e, h[k][0], v.z * bb[0]);
-                        pv[k][qq] = cc[0] * h[k][0];
-                    } else {
-                        float2 acc = make_float2(0.f, 0.f);
+            for (int k = 0; k < KC; ++k) {
+                const float4 v = ddw[(t * KC + k) * CGW + q];
+                if constexpr (NPT == 1) {
+                    const float e = ex2_approx(v.x * a2[k][0]);
+                    h[k][0] = fmaf(e, h[k][0], v.z * bb[0]);
+                    pv[g][k][qq] = cc[0] * h[k][0];
+                } else {
+                    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-                        for (int j = 0; j < NPT; j += 2) {
-                            const float2 x = __fmul2_rn(make_float2(v.x, v.y),
-                                                        make_float2(a2[k][j], a2[k][j + 1]));
-                            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                            const float2 w = __fmul2_rn(make_float2(v.z, v.w),
-                                                        make_float2(bb[j], bb[j + 1]));
-                            const float2 hh = __ffma2_rn(e, make_float2(h[k][j], h[k][j + 1]), w);
-                            h[k][j] = hh.x;
-                            h[k][j + 1] = hh.y;
-                            acc = __ffma2_rn(make_float2(cc[j], cc[j + 1]), hh, acc);
-                        }
-                        pv[k][qq] = acc.x + acc.y;
+                    for (int j = 0; j < NPT; j += 2) {
+                        const float2 x = __fmul2_rn(make_float2(v.x, v.y),
+                                                    make_float2(a2[k][j], a2[k][j + 1]));
+                        const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        const float2 w = __fmul2_rn(make_float2(v.z, v.w),
+                                                    make_float2(bb[j], bb[j + 1]));
+                        const float2 hh = __ffma2_rn(e, make_float2(h[k][j], h[k][j + 1]), w);
+                        h[k][j] = hh.x;
+                        h[k][j + 1] = hh.y;
+                        acc = __ffma2_rn(make_float2(cc[j], cc[j + 1]), hh, acc);
                     }
+                    pv[g][k][qq] = acc.x + acc.y;
                 }
             }
-            if constexpr (S > 1) reduce_transposed<S, KC>(pv, sl);
-            // POST: step g*S + sl of this lane's channels.
+        }
+        if constexpr (S > 1) {
+#pragma unroll
+            for (int g = 0; g < NG; ++g) reduce_transposed<S, KC>(pv[g], sl);
+        }
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
             const int t = g * S + sl;
             float yv[KC];
 #pragma unroll
-            for (int k = 0; k < KC; ++k) yv[k] = fmaf(pv[k][0], gate[buf][k], skip[buf][k]);
+            for (int k = 0; k < KC; ++k) yv[k] = fmaf(pv[g][k][0], gate[g][k], skip[g][k]);
             if (p.tma_udz) {
                 st_k<T, KC>(yt + TT::off(t, cl0 * ES, TC), yv);
             } else if (t < tv) {
@@ -612,17 +613,8 @@ __global__ void __launch_bounds__(kThreads)
                     if (d0 + cl0 + k < dim)
                         gy[(b * L + t0 + t) * dim + d0 + cl0 + k] = E::from_f(yv[k]);
             }
-            __syncwarp();
-        };
-
-        prep(0, 0);
-        __syncwarp();
-        static_assert(NG % 2 == 0, "groups per chunk must be even");
-#pragma unroll 1
-        for (int g = 0; g < NG; g += 2) {
-            group(g, std::integral_constant<int, 0>{});
-            group(g + 1, std::integral_constant<int, 1>{});
         }
+        __syncwarp();
 
         if (p.tma_udz) {
             fence_proxy_async_smem();
