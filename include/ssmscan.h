@@ -125,12 +125,12 @@ SSM_API const char *ssm_status_string(int status);
 /*
  * Launch plan the library would use for a problem, without launching.
  * dtype: 0 = fp32, 1 = bf16.  On SSM_OK, plan[0..7] receives:
- *   [0] lanes per channel group S      [1] states per lane NPT
+ *   [0] state groups WS                [1] states per lane NPT
  *   [2] timesteps per chunk            [3] channels per block
  *   [4] threads per block              [5] blocks in the grid
- *   [6] dynamic shared bytes           [7] channels per lane KC
- * A channel group is S lanes sharing KC channels; each lane holds KC x NPT
- * states (N <= S * NPT).
+ *   [6] dynamic shared bytes           [7] 1 if tiles move by TMA, else 0
+ * Each channel's N states are split over WS warps (state groups), NPT states
+ * per lane (N <= WS * NPT); a lane is a channel.
  */
 SSM_API int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype,
                   int64_t plan[8]);
@@ -145,8 +145,9 @@ SSM_API int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int 
  *                           block drains its copies and returns, and
  *                           ssm_scan_last_device_status reports
  *                           SSM_ERR_TIMEOUT.  0 (default): off.
- *   SSM_KNOB_LANES          force S (1, 2, 4 or 8); 0 = automatic
- *   SSM_KNOB_CHANNELS_PER_LANE  force KC (1 or 2); 0 = automatic
+ *   SSM_KNOB_STATE_GROUPS   force WS (1, 2, 4 or 8); 0 = automatic
+ *   SSM_KNOB_STAGES         force the TMA ring depth (2, 3 or 4); 0 = automatic
+ *   SSM_KNOB_CHUNK          force timesteps per chunk (16 or 32); 0 = automatic
  *   SSM_KNOB_PLAIN_LOADS    1: move tiles with plain loads even when TMA applies
  * A forced combination the library is not built for falls back to automatic.
  * Returns SSM_OK or SSM_ERR_ARG.
@@ -154,9 +155,10 @@ SSM_API int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int 
 enum {
     SSM_KNOB_WAIT_NS = 1,
     SSM_KNOB_FORCE_TIMEOUT = 2,
-    SSM_KNOB_LANES = 3,
-    SSM_KNOB_CHANNELS_PER_LANE = 4,
-    SSM_KNOB_PLAIN_LOADS = 5
+    SSM_KNOB_STATE_GROUPS = 3,
+    SSM_KNOB_CHUNK = 4,
+    SSM_KNOB_PLAIN_LOADS = 5,
+    SSM_KNOB_STAGES = 6
 };
 SSM_API int ssm_set_knob(int key, int64_t value);
 

@@ -10,24 +10,26 @@
 // itwiki page ("Mamba의 선택 메커니즘") and the Obsidian "Mamba" note (5.1)
 // describe; the way it is mapped onto B300 here is our own.
 //
-// Work decomposition (one thread block = 4 warps):
-//   * a block owns one batch row b and a tile of DT consecutive channels and
-//     walks the sequence in chunks of TC = 32 timesteps;
-//   * a warp owns 32/S channel groups; the S lanes of a group share KC channels
-//     and split their N states, NPT per lane (N <= S * NPT), so a lane keeps
-//     KC x NPT states in registers for the whole sequence;
+// Work decomposition:
+//   * a block owns one batch row b and a tile of DT = 32 * WC consecutive
+//     channels and walks the sequence in chunks of TC = 32 timesteps;
+//   * its warps are WC channel tiles x WS state groups: lane = channel, and a
+//     warp's state group holds NPT states of each of its 32 channels in
+//     registers for the whole sequence (N <= WS * NPT);
 //   * per chunk, TMA (cp.async.bulk.tensor, 3-D maps over (dim, L, batch), with
 //     the 32/64/128-byte swizzle that matches the tile's row width) brings the
 //     u / delta / z tiles and the B / C rows into a two-stage ring tracked by
-//     mbarriers, one chunk ahead; the block widens B and C to fp32 once;
-//   * then each warp runs its own pipeline over groups of S steps: every lane
-//     computes dt = softplus(delta + bias), dt*u, the gate silu(z) and the skip
-//     D*u*silu(z) for ONE (step, channel) item of the group and shares dt, dt*u
-//     with the group through a small shared buffer; all lanes advance their
-//     states over the S steps; a transposed shuffle reduction of the partial
-//     readouts <C, h> leaves each lane the full readout of exactly the item it
-//     prepared, so skip and gate apply in registers and y goes to a swizzled
-//     output tile that one thread stores with a TMA bulk tensor store.
+//     mbarriers, up to three chunks ahead;
+//   * PREP: every thread handles (step, channel pair) items: B and C widened to
+//     fp32, dt = softplus(delta + bias), dt*u, the gate silu(z) and the skip
+//     D*u*silu(z), written to shared memory once per (t, d);
+//   * SCAN: every warp advances its states over the chunk; the B and C values a
+//     step needs are the same for the whole warp (uniform shared reads), dt and
+//     dt*u are one 64-bit read per lane, and each lane stores one partial
+//     readout per step;
+//   * POST: every (step, pair) item sums its WS partials, applies skip and gate,
+//     and writes y to a swizzled tile that one thread stores with a TMA bulk
+//     tensor store.
 // Shapes TMA cannot describe (rows not a multiple of 16 bytes, misaligned
 // pointers, L = 0) take the same kernel with plain loads and stores.
 //
@@ -52,8 +54,7 @@
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kStages = 2;
+constexpr int kMaxStages = 4;  // deepest TMA ring; chunks in flight per block = stages - 1
 constexpr size_t kMaxSmem = 227 * 1024;  // opt-in shared memory per block on sm_103
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -219,6 +220,8 @@ template <> struct Act<float> {
         return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)));
     }
     __device__ static float silu(float z) { return z / (1.f + expf(-z)); }
+    __device__ static float2 softplus2(float2 x) { return make_float2(softplus(x.x), softplus(x.y)); }
+    __device__ static float2 silu2(float2 z) { return make_float2(silu(z.x), silu(z.y)); }
 };
 template <> struct Act<__nv_bfloat16> {
     __device__ static float softplus(float x) {
@@ -228,6 +231,21 @@ template <> struct Act<__nv_bfloat16> {
     __device__ static float silu(float z) {
         // 1 + e^-z overflows to +inf for very negative z; rcp(inf) = 0 -> silu = -0.
         return z * rcp_approx(1.f + ex2_approx(-z * kLog2e));
+    }
+    // The same on a pair of channels, with packed f32x2 arithmetic.
+    __device__ static float2 softplus2(float2 x) {
+        const float2 a = __fmul2_rn(x, make_float2(kLog2e, kLog2e));
+        const float2 e1 = __fadd2_rn(make_float2(1.f, 1.f),
+                                     make_float2(ex2_approx(a.x), ex2_approx(a.y)));
+        const float2 l = __fmul2_rn(make_float2(lg2_approx(e1.x), lg2_approx(e1.y)),
+                                    make_float2(kLn2, kLn2));
+        return make_float2(x.x > 15.f ? x.x : l.x, x.y > 15.f ? x.y : l.y);
+    }
+    __device__ static float2 silu2(float2 z) {
+        const float2 a = __fmul2_rn(z, make_float2(-kLog2e, -kLog2e));
+        const float2 d = __fadd2_rn(make_float2(1.f, 1.f),
+                                    make_float2(ex2_approx(a.x), ex2_approx(a.y)));
+        return __fmul2_rn(z, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
     }
 };
 
@@ -264,28 +282,6 @@ struct Tile {
     }
 };
 
-// Transposed reduction of each lane's partial readouts over the S lanes that
-// share a channel group: on entry v[k][q] is this lane's partial for channel k
-// at step q of the group; on exit v[k][0] holds the full sum for step q = sl.
-// Each round halves the steps a lane keeps and exchanges the other half with
-// its partner, so S - 1 shuffles per channel replace S log2(S) of a butterfly.
-template <int S, int KC>
-__device__ __forceinline__ void reduce_transposed(float (&v)[KC][S], int sl) {
-#pragma unroll
-    for (int m = S / 2; m >= 1; m >>= 1) {
-        const bool up = (sl & m) != 0;
-#pragma unroll
-        for (int k = 0; k < KC; ++k) {
-#pragma unroll
-            for (int i = 0; i < m; ++i) {
-                const float send = up ? v[k][i] : v[k][i + m];
-                const float keep = up ? v[k][i + m] : v[k][i];
-                v[k][i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-            }
-        }
-    }
-}
-
 __host__ __device__ constexpr size_t round1k(size_t x) { return (x + 1023) & ~size_t(1023); }
 
 struct KParams {
@@ -306,52 +302,100 @@ struct KParams {
     int tma_udz;   // u / delta / z / y tiles move by TMA
     int tma_bc;    // B / C tiles move by TMA
     int force_timeout;
+    int stages;    // TMA ring depth (2 .. kMaxStages)
 };
 
-constexpr int kWarps = kThreads / 32;
-
 // Compile-time geometry of one block.
-//   A block has kWarps warps.  A warp has 32/S channel groups of S lanes; a lane
-//   holds KC channels x NPT states, so a group covers KC channels x S*NPT states.
-template <typename T, int NPT, int S, int KC, int TC>
+//   The block owns DT = WC*32 channels of one batch row.  Its warps form WC
+//   channel tiles x WS state groups: lane = channel, and the warp's state group
+//   sg holds states sg*NPT .. sg*NPT + NPT - 1 (N <= WS*NPT).  So every lane of a
+//   warp needs the same B and C values (a uniform shared-memory read) and its own
+//   channel's dt, dt*u (a distinct read), and partial readouts of the WS state
+//   groups are summed once per (t, d).
+template <typename T, int NPT, int WS, int TC>
 struct Geo {
     static constexpr int ES = int(sizeof(T));
-    static constexpr int CGW = 32 / S;        // channel groups per warp
-    static constexpr int CW = CGW * KC;       // channels per warp
-    static constexpr int DT = kWarps * CW;    // channels per block
-    static constexpr int NP = NPT * S;        // states per group (>= N)
-    static constexpr int WB = DT * ES;        // tile row bytes
+    static constexpr int WC = WS >= 4 ? 1 : 4 / WS;  // channel tiles per block
+    static constexpr int NW = WC * WS;               // warps per block
+    static constexpr int NT = NW * 32;               // threads per block
+    static constexpr int DT = WC * 32;               // channels per block
+    static constexpr int NP = NPT * WS;              // padded states per channel
+    static constexpr int WB = DT * ES;               // tile row bytes
+    static constexpr int NPAIR = DT / 2;             // channel pairs
+    static constexpr int ITEMS = TC * NPAIR / NT;    // (step, pair) items per thread
     using TileT = Tile<WB>;
     static constexpr size_t TILE = round1k(size_t(TC) * WB);
-    static constexpr size_t DD_WARP = size_t(TC) * KC * CGW * 16;  // a chunk's (dt,dt,dtu,dtu)
-    static_assert(TC % S == 0, "chunk must hold whole groups");
+    static_assert(NT % NPAIR == 0 && (TC * NPAIR) % NT == 0, "item mapping");
     static_assert(WB % 16 == 0 && (WB <= 128 || WB % 128 == 0), "tile rows");
 };
 
 // Shared-memory layout of one block (bytes from a 1024-byte aligned base).
-//   raw ring  kStages x { u, delta, z : tile ; B, C : [TC][N] T }
-//   s_B, s_C  [TC][NP] fp32            B, C widened (rows past L are zero)
-//   s_dd      kWarps x [TC][KC][CGW] float4   (dt, dt, dt*u, dt*u) per step
-//   s_y       2 x tile                  output tiles for the TMA store
-template <typename T, int NPT, int S, int KC, int TC>
+//   raw ring  stages x { u, delta, z : tile ; B, C : [TC][N] T }
+//   s_B, s_C  [TC][NP] fp32          B, C widened (rows past L and states past N are zero)
+//   s_dd      [TC][DT] float2        (dt, dt*u); zeros on padded steps
+//   s_gs      [TC][DT] float2        (g, D*u*g), g = silu(z) or 1
+//   s_part    [WS][TC][DT] fp32      each state group's partial readout
+//   s_y       2 x tile               output tiles for the TMA store
+template <typename T, int NPT, int WS, int TC>
 struct Layout {
-    using G = Geo<T, NPT, S, KC, TC>;
-    size_t tile_bc, stage, off_raw, off_bf, off_cf, off_dd, off_y, off_bar, total;
-    __host__ __device__ explicit Layout(int64_t N) {
+    using G = Geo<T, NPT, WS, TC>;
+    size_t tile_bc, stage, off_raw, off_bf, off_cf, off_dd, off_gs, off_part, off_y, off_bar, total;
+    __host__ __device__ Layout(int64_t N, int stages) {
         tile_bc = round1k(size_t(TC) * size_t(N) * G::ES);
         stage = 3 * G::TILE + 2 * tile_bc;
         off_raw = 0;
-        off_bf = off_raw + kStages * stage;
+        off_bf = off_raw + size_t(stages) * stage;
         off_cf = off_bf + round1k(size_t(TC) * G::NP * 4);
         off_dd = off_cf + round1k(size_t(TC) * G::NP * 4);
-        off_y = off_dd + round1k(kWarps * G::DD_WARP);
+        off_gs = off_dd + round1k(size_t(TC) * G::DT * 8);
+        off_part = off_gs + round1k(size_t(TC) * G::DT * 8);
+        off_y = off_part + round1k(size_t(WS) * TC * G::DT * 4);
         off_bar = off_y + 2 * G::TILE;
         total = off_bar + 64;
     }
 };
 
-template <typename T, int NPT, int S, int KC, int TC>
-__global__ void __launch_bounds__(kThreads)
+// The scan over one chunk for one lane: channel c (dd, part already offset to
+// it), states sg*NPT.. (Bs, Cs already offset).  Restrict-qualified so the
+// compiler may move later steps' loads above earlier steps' partial stores.
+template <int NPT, int NP, int DT, int TC>
+__device__ __forceinline__ void scan_chunk(const float2* __restrict__ dd,
+                                           const float* __restrict__ Bs,
+                                           const float* __restrict__ Cs,
+                                           float* __restrict__ part, const float (&a2)[NPT],
+                                           float (&h)[NPT]) {
+#pragma unroll 8
+    for (int t = 0; t < TC; ++t) {
+        const float2 v = dd[t * DT];
+        float bb[NPT], cc[NPT];
+        ld_states<NPT>(Bs + t * NP, bb);
+        ld_states<NPT>(Cs + t * NP, cc);
+        float p;
+        if constexpr (NPT == 1) {
+            const float e = ex2_approx(v.x * a2[0]);
+            h[0] = fmaf(e, h[0], v.y * bb[0]);
+            p = cc[0] * h[0];
+        } else {
+            const float2 vx = make_float2(v.x, v.x), vy = make_float2(v.y, v.y);
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < NPT; j += 2) {
+                const float2 x = __fmul2_rn(vx, make_float2(a2[j], a2[j + 1]));
+                const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                const float2 w = __fmul2_rn(vy, make_float2(bb[j], bb[j + 1]));
+                const float2 hh = __ffma2_rn(e, make_float2(h[j], h[j + 1]), w);
+                h[j] = hh.x;
+                h[j + 1] = hh.y;
+                acc = __ffma2_rn(make_float2(cc[j], cc[j + 1]), hh, acc);
+            }
+            p = acc.x + acc.y;
+        }
+        part[t * DT] = p;
+    }
+}
+
+template <typename T, int NPT, int WS, int TC>
+__global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
     ssm_scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u,
                         const __grid_constant__ CUtensorMap tm_dt,
                         const __grid_constant__ CUtensorMap tm_z,
@@ -359,24 +403,25 @@ __global__ void __launch_bounds__(kThreads)
                         const __grid_constant__ CUtensorMap tm_C,
                         const __grid_constant__ CUtensorMap tm_y, const KParams p) {
     using E = Elt<T>;
-    using G = Geo<T, NPT, S, KC, TC>;
+    using G = Geo<T, NPT, WS, TC>;
     using TT = typename G::TileT;
-    constexpr int DT = G::DT, NP = G::NP, CGW = G::CGW, CW = G::CW, ES = G::ES;
+    constexpr int DT = G::DT, NP = G::NP, ES = G::ES, NT = G::NT;
     constexpr int RS = TT::RS, NB = TT::NB;
-    constexpr int NG = TC / S;  // groups per chunk
+    constexpr int NPAIR = G::NPAIR, ITEMS = G::ITEMS, TSTEP = NT / NPAIR;
 
     extern __shared__ unsigned char smem_raw[];
     __shared__ int s_abort;
     unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const Layout<T, NPT, S, KC, TC> lay(p.N);
+    const Layout<T, NPT, WS, TC> lay(p.N, p.stages);
+    const int nst = p.stages;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int q = lane / S, sl = lane % S;         // channel group in warp, lane in group
+    const int ct = warp / WS, sg = warp % WS;  // channel tile, state group
+    const int c = ct * 32 + lane;              // this lane's channel in the tile
     const int64_t N = p.N, L = p.L, dim = p.dim;
     const int64_t b = blockIdx.x / p.nblk_d;
     const int64_t d0 = (blockIdx.x % p.nblk_d) * DT;
-    const int cl0 = warp * CW + q * KC;            // first channel of this lane in the tile
 
     unsigned char* const raw0 = base + lay.off_raw;
     const uint32_t stage_b = uint32_t(lay.stage), tbc = uint32_t(lay.tile_bc);
@@ -388,10 +433,12 @@ __global__ void __launch_bounds__(kThreads)
     auto raw_C = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + 3 * TILE + tbc); };
     float* const s_B = reinterpret_cast<float*>(base + lay.off_bf);
     float* const s_C = reinterpret_cast<float*>(base + lay.off_cf);
-    float4* const s_dd = reinterpret_cast<float4*>(base + lay.off_dd);
+    float2* const s_dd = reinterpret_cast<float2*>(base + lay.off_dd);
+    float2* const s_gs = reinterpret_cast<float2*>(base + lay.off_gs);
+    float* const s_part = reinterpret_cast<float*>(base + lay.off_part);
     unsigned char* const s_y0 = base + lay.off_y;
     const uint32_t bar0 = smem_u32(base + lay.off_bar);
-    const uint32_t bar_never = bar0 + 8 * kStages;  // a barrier nothing ever completes
+    const uint32_t bar_never = bar0 + 8 * kMaxStages;  // a barrier nothing ever completes
 
     const bool has_z = p.z != nullptr;
     const int64_t nchunks = (L + TC - 1) / TC;
@@ -401,7 +448,7 @@ __global__ void __launch_bounds__(kThreads)
 
     if (tid == 0) {
         s_abort = 0;
-        for (int s = 0; s <= kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+        for (int s = 0; s <= kMaxStages; ++s) mbar_init(bar0 + 8 * s, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -424,21 +471,29 @@ __global__ void __launch_bounds__(kThreads)
         }
     };
 
-    // ---- this lane's channels: parameters, state
-    float a2[KC][NPT], h[KC][NPT];
-    float bias[KC], dsk[KC];
+    // ---- SCAN role: channel c of the tile, states sg*NPT + j
+    const int64_t d_scan = d0 + c;
+    const bool scan_ok = d_scan < dim;
+    float a2[NPT], h[NPT];
 #pragma unroll
-    for (int k = 0; k < KC; ++k) {
-        const int64_t d = d0 + cl0 + k;
-        const bool ok = d < dim;
-        bias[k] = (p.bias != nullptr && ok) ? p.bias[d] : 0.f;
-        dsk[k] = (p.D != nullptr && ok) ? p.D[d] : 0.f;
+    for (int j = 0; j < NPT; ++j) {
+        const int64_t n = int64_t(sg) * NPT + j;
+        a2[j] = (scan_ok && n < N) ? p.A[d_scan * N + n] * kLog2e : 0.f;
+        h[j] = 0.f;
+    }
+
+    // ---- PREP / POST role: channel pair pp (channels 2pp, 2pp+1), steps
+    //      tq0, tq0 + TSTEP, ... (ITEMS of them per chunk)
+    const int pp = tid % NPAIR;
+    const int tq0 = tid / NPAIR;
+    float bias2[2], dsk2[2];
+    bool okp[2];
 #pragma unroll
-        for (int j = 0; j < NPT; ++j) {
-            const int64_t n = int64_t(sl) * NPT + j;
-            a2[k][j] = (ok && n < N) ? p.A[d * N + n] * kLog2e : 0.f;
-            h[k][j] = 0.f;
-        }
+    for (int k = 0; k < 2; ++k) {
+        const int64_t d = d0 + 2 * pp + k;
+        okp[k] = d < dim;
+        bias2[k] = (p.bias != nullptr && okp[k]) ? p.bias[d] : 0.f;
+        dsk2[k] = (p.D != nullptr && okp[k]) ? p.D[d] : 0.f;
     }
 
     const T* gu = static_cast<const T*>(p.u);
@@ -448,18 +503,24 @@ __global__ void __launch_bounds__(kThreads)
     const T* gC = static_cast<const T*>(p.C);
     T* gy = static_cast<T*>(p.y);
 
-    if (p.tma_udz && tid == 0 && nchunks > 0) issue_loads(0, 0);
+    if (p.tma_udz && tid == 0)
+        for (int64_t cc = 0; cc < nst - 1 && cc < nchunks; ++cc) issue_loads(cc, int(cc));
 
-    for (int64_t c = 0; c < nchunks; ++c) {
-        const int st = int(c % kStages);
-        const int64_t t0 = c * TC;
+    // Ring position of this chunk (st), its mbarrier phase parity (ph), and the
+    // stage the prefetch refills (sa), advanced without divisions.
+    int st = 0, sa = nst - 1;
+    uint32_t ph = 0;
+    for (int64_t chunk = 0; chunk < nchunks; ++chunk) {
+        const int64_t t0 = chunk * TC;
         const int tv = int(L - t0 < TC ? L - t0 : int64_t(TC));
 
         if (p.tma_udz) {
-            if (tid == 0 && c + 1 < nchunks) issue_loads(c + 1, int((c + 1) % kStages));
+            // Refill the stage the previous chunk released (nst - 1 chunks ahead).
+            const int64_t ahead = chunk + nst - 1;
+            if (tid == 0 && ahead < nchunks) issue_loads(ahead, sa);
             bool ok = true;
-            if (p.force_timeout && c == 0) ok = mbar_wait_bounded(bar_never, 0, p.wait_ns);
-            if (ok) ok = mbar_wait_bounded(bar0 + 8 * st, uint32_t((c / kStages) & 1), p.wait_ns);
+            if (p.force_timeout && chunk == 0) ok = mbar_wait_bounded(bar_never, 0, p.wait_ns);
+            if (ok) ok = mbar_wait_bounded(bar0 + 8 * st, ph, p.wait_ns);
             if (!ok) {
                 atomicOr(&g_ssm_status, kDevTimeout);
                 *reinterpret_cast<volatile int*>(&s_abort) = 1;
@@ -467,7 +528,7 @@ __global__ void __launch_bounds__(kThreads)
         } else {
             // Plain loads of the chunk's u / delta / z tiles, same swizzled layout,
             // zero outside the tensor.
-            for (int i = tid; i < TC * DT; i += kThreads) {
+            for (int i = tid; i < TC * DT; i += NT) {
                 const int t = i / DT, k = i % DT;
                 const int64_t gt = t0 + t, gd = d0 + k;
                 const bool in = gt < L && gd < dim;
@@ -477,19 +538,21 @@ __global__ void __launch_bounds__(kThreads)
                 *reinterpret_cast<T*>(raw_dt(st) + o) = in ? gdt[off] : E::from_f(0.f);
                 if (has_z) *reinterpret_cast<T*>(raw_z(st) + o) = in ? gz[off] : E::from_f(0.f);
             }
+            __syncthreads();
         }
 
-        // B, C widened to fp32 (rows past L are zero: TMA fills them, or we do).
+        // ---------------- PREP
+        // B, C widened to fp32 (rows past L and states past N are zero).
         if (bc_vec) {
             const int items = TC * NP / 4;
-            for (int i = tid; i < 2 * items; i += kThreads) {
+            for (int i = tid; i < 2 * items; i += NT) {
                 const bool isC = i >= items;
                 const int j = (isC ? i - items : i) * 4;
                 const float4 qv = ld_quad<T>((isC ? raw_C(st) : raw_B(st)) + j);
                 *reinterpret_cast<float4*>((isC ? s_C : s_B) + j) = qv;
             }
         } else {
-            for (int i = tid; i < TC * NP; i += kThreads) {
+            for (int i = tid; i < TC * NP; i += NT) {
                 const int t = i / NP, n = i % NP;
                 float bv = 0.f, cv = 0.f;
                 if (n < N && t < tv) {
@@ -506,17 +569,49 @@ __global__ void __launch_bounds__(kThreads)
                 s_C[i] = cv;
             }
         }
+        // dt = softplus(delta + bias), dt*u, g = silu(z) and D*u*g per (step,
+        // channel pair), packed f32x2 arithmetic on the pair.
+        {
+            const unsigned char* ru = raw_u(st);
+            const unsigned char* rdt = raw_dt(st);
+            const unsigned char* rz = raw_z(st);
+            const float2 b2 = make_float2(bias2[0], bias2[1]);
+            const float2 d2 = make_float2(dsk2[0], dsk2[1]);
+#pragma unroll
+            for (int it = 0; it < ITEMS; ++it) {
+                const int t = tq0 + it * TSTEP;
+                const uint32_t o = TT::off(t, 2 * pp * ES, TC);
+                float xr[2], uu[2], zz[2];
+                ld_k<T, 2>(rdt + o, xr);
+                ld_k<T, 2>(ru + o, uu);
+                const float2 u2 = make_float2(uu[0], uu[1]);
+                float2 x = __fadd2_rn(make_float2(xr[0], xr[1]), b2);
+                if (p.softplus) x = Act<T>::softplus2(x);
+                const float2 xu = __fmul2_rn(x, u2);
+                float2 g = make_float2(1.f, 1.f);
+                if (has_z) {
+                    ld_k<T, 2>(rz + o, zz);
+                    g = Act<T>::silu2(make_float2(zz[0], zz[1]));
+                }
+                const float2 su = __fmul2_rn(__fmul2_rn(d2, u2), g);
+                const bool live = t < tv;
+                *reinterpret_cast<float4*>(s_dd + t * DT + 2 * pp) =
+                    live ? make_float4(x.x, xu.x, x.y, xu.y) : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4*>(s_gs + t * DT + 2 * pp) = make_float4(g.x, su.x, g.y, su.y);
+            }
+        }
         if (p.tma_udz && tid == 0) bulk_wait_read_le1();  // this chunk's output tile is free
         __syncthreads();
         if (*reinterpret_cast<volatile int*>(&s_abort)) {
             // Give up: wait (bounded) for this block's own loads in flight, then
             // for its bulk stores, and leave.  Outputs are incomplete.
             if (tid == 0) {
-                bool ok = mbar_wait_bounded(bar0 + 8 * st, uint32_t((c / kStages) & 1), p.wait_ns);
-                if (c + 1 < nchunks) {
-                    const int s1 = int((c + 1) % kStages);
-                    ok = mbar_wait_bounded(bar0 + 8 * s1, uint32_t(((c + 1) / kStages) & 1),
-                                           p.wait_ns) && ok;
+                bool ok = true;
+                int s2 = st;
+                uint32_t p2 = ph;
+                for (int64_t cc = chunk; cc < chunk + nst && cc < nchunks; ++cc) {
+                    ok = mbar_wait_bounded(bar0 + 8 * s2, p2, p.wait_ns) && ok;
+                    if (++s2 == nst) { s2 = 0; p2 ^= 1u; }
                 }
                 if (!ok) atomicOr(&g_ssm_status, kDevDrainTimeout);
                 bulk_wait_all();
@@ -524,98 +619,30 @@ __global__ void __launch_bounds__(kThreads)
             return;
         }
 
-        // ---------------- per-warp pipeline over the chunk, in four batched phases
-        // (batching keeps the long softplus / SiLU and shuffle latency chains of
-        // different groups independent, so they overlap):
-        // PREP: for each group g of S steps this lane computes step g*S + sl of
-        //   its KC channels -- dt and dt*u for the scan (shared with the group
-        //   through s_dd), the gate g and the skip D*u*g (kept in registers).
-        // SCAN: every lane advances its KC x NPT states over all TC steps and
-        //   keeps its partial readouts.
-        // REDUCE: per group, a transposed shuffle reduction leaves this lane the
-        //   full readout of exactly the item it prepared.
-        // POST: skip and gate in registers, y into the output tile.
-        unsigned char* yt = s_y0 + (c & 1) * TILE;
-        const unsigned char* ru = raw_u(st);
-        const unsigned char* rdt = raw_dt(st);
-        const unsigned char* rz = raw_z(st);
-        float4* const ddw = s_dd + warp * (TC * KC * CGW);
-        float gate[NG][KC], skip[NG][KC];
+        // ---------------- SCAN: all TC steps (padded ones are no-ops)
+        scan_chunk<NPT, NP, DT, TC>(s_dd + c, s_B + sg * NPT, s_C + sg * NPT,
+                                    s_part + sg * TC * DT + c, a2, h);
+        __syncthreads();
+
+        // ---------------- POST: y = (sum of the state groups' partials) g + D u g
+        unsigned char* yt = s_y0 + (chunk & 1) * TILE;
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-            const int t = g * S + sl;
-            const uint32_t o = TT::off(t, cl0 * ES, TC);
-            float xr[KC], uu[KC], zz[KC];
-            ld_k<T, KC>(rdt + o, xr);
-            ld_k<T, KC>(ru + o, uu);
-            if (has_z) ld_k<T, KC>(rz + o, zz);
-            const bool live = t < tv;
+        for (int it = 0; it < ITEMS; ++it) {
+            const int t = tq0 + it * TSTEP;
+            float2 acc = *reinterpret_cast<const float2*>(s_part + t * DT + 2 * pp);
 #pragma unroll
-            for (int k = 0; k < KC; ++k) {
-                float x = xr[k] + bias[k];
-                if (p.softplus) x = Act<T>::softplus(x);
-                const float xu = x * uu[k];
-                const float gg = has_z ? Act<T>::silu(zz[k]) : 1.f;
-                gate[g][k] = gg;
-                skip[g][k] = dsk[k] * uu[k] * gg;
-                ddw[(t * KC + k) * CGW + q] =
-                    live ? make_float4(x, x, xu, xu) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        __syncwarp();
-        float pv[NG][KC][S];
-#pragma unroll
-        for (int t = 0; t < TC; ++t) {
-            const int g = t / S, qq = t % S;
-            float bb[NPT], cc[NPT];
-            ld_states<NPT>(s_B + t * NP + sl * NPT, bb);
-            ld_states<NPT>(s_C + t * NP + sl * NPT, cc);
-#pragma unroll
-            for (int k = 0; k < KC; ++k) {
-                const float4 v = ddw[(t * KC + k) * CGW + q];
-                if constexpr (NPT == 1) {
-                    const float e = ex2_approx(v.x * a2[k][0]);
-                    h[k][0] = fmaf(e, h[k][0], v.z * bb[0]);
-                    pv[g][k][qq] = cc[0] * h[k][0];
-                } else {
-                    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int j = 0; j < NPT; j += 2) {
-                        const float2 x = __fmul2_rn(make_float2(v.x, v.y),
-                                                    make_float2(a2[k][j], a2[k][j + 1]));
-                        const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                        const float2 w = __fmul2_rn(make_float2(v.z, v.w),
-                                                    make_float2(bb[j], bb[j + 1]));
-                        const float2 hh = __ffma2_rn(e, make_float2(h[k][j], h[k][j + 1]), w);
-                        h[k][j] = hh.x;
-                        h[k][j + 1] = hh.y;
-                        acc = __ffma2_rn(make_float2(cc[j], cc[j + 1]), hh, acc);
-                    }
-                    pv[g][k][qq] = acc.x + acc.y;
-                }
-            }
-        }
-        if constexpr (S > 1) {
-#pragma unroll
-            for (int g = 0; g < NG; ++g) reduce_transposed<S, KC>(pv[g], sl);
-        }
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-            const int t = g * S + sl;
-            float yv[KC];
-#pragma unroll
-            for (int k = 0; k < KC; ++k) yv[k] = fmaf(pv[g][k][0], gate[g][k], skip[g][k]);
+            for (int s = 1; s < WS; ++s)
+                acc = __fadd2_rn(acc, *reinterpret_cast<const float2*>(s_part + (s * TC + t) * DT + 2 * pp));
+            const float4 gs = *reinterpret_cast<const float4*>(s_gs + t * DT + 2 * pp);
+            const float yv[2] = {fmaf(acc.x, gs.x, gs.y), fmaf(acc.y, gs.z, gs.w)};
             if (p.tma_udz) {
-                st_k<T, KC>(yt + TT::off(t, cl0 * ES, TC), yv);
+                st_k<T, 2>(yt + TT::off(t, 2 * pp * ES, TC), yv);
             } else if (t < tv) {
 #pragma unroll
-                for (int k = 0; k < KC; ++k)
-                    if (d0 + cl0 + k < dim)
-                        gy[(b * L + t0 + t) * dim + d0 + cl0 + k] = E::from_f(yv[k]);
+                for (int k = 0; k < 2; ++k)
+                    if (okp[k]) gy[(b * L + t0 + t) * dim + d0 + 2 * pp + k] = E::from_f(yv[k]);
             }
         }
-        __syncwarp();
-
         if (p.tma_udz) {
             fence_proxy_async_smem();
             __syncthreads();
@@ -629,19 +656,16 @@ __global__ void __launch_bounds__(kThreads)
         } else {
             __syncthreads();
         }
+        if (++st == nst) { st = 0; ph ^= 1u; }
+        if (++sa == nst) sa = 0;
     }
     if (p.tma_udz && tid == 0) bulk_wait_all();
 
-    if (p.h_last != nullptr) {
+    if (p.h_last != nullptr && scan_ok) {
 #pragma unroll
-        for (int k = 0; k < KC; ++k) {
-            const int64_t d = d0 + cl0 + k;
-            if (d >= dim) continue;
-#pragma unroll
-            for (int j = 0; j < NPT; ++j) {
-                const int64_t n = int64_t(sl) * NPT + j;
-                if (n < N) p.h_last[(b * dim + d) * N + n] = h[k][j];
-            }
+        for (int j = 0; j < NPT; ++j) {
+            const int64_t n = int64_t(sg) * NPT + j;
+            if (n < N) p.h_last[(b * dim + d_scan) * N + n] = h[j];
         }
     }
 }
@@ -649,8 +673,9 @@ __global__ void __launch_bounds__(kThreads)
 // ------------------------------------------------------------------ host side
 std::atomic<int64_t> g_wait_ns{2000000000LL};
 std::atomic<int> g_force_timeout{0};
-std::atomic<int> g_force_lanes{0};
-std::atomic<int> g_force_kc{0};
+std::atomic<int> g_force_groups{0};
+std::atomic<int> g_force_stages{0};
+std::atomic<int> g_force_chunk{0};
 std::atomic<int> g_plain_loads{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -682,10 +707,9 @@ bool encode3d(CUtensorMap* tm, CUtensorMapDataType ty, size_t es, const void* pt
     return r == CUDA_SUCCESS;
 }
 
-constexpr int kTC = 32;  // timesteps per chunk
 
 struct Plan {
-    int S = 1, NPT = 1, KC = 1, TC = kTC, DT = kThreads;
+    int WS = 1, NPT = 1, TC = 32, DT = 128, NT = 128, stages = 2;
     int64_t grid = 0;
     size_t smem = 0;
     int row_span = 16;
@@ -698,50 +722,47 @@ int supported_npt(int64_t need) {
     return 0;
 }
 
-// Relative cost model for the lane split (S lanes per channel group, KC
-// channels x NPT states per lane).  Per lane and time step: the state updates
-// (~3.3 issue slots per state with packed f32x2 math, plus per-step loads),
-// this lane's share of the per-(t, d) work, and the transposed reduction.  The
-// machine runs ceil(warps / schedulers) rounds; a round with fewer than two
-// warps per scheduler hides latency poorly.
-double plan_cost(int64_t channels, int S, int npt, int kc) {
+// Relative cost model for the number of state groups WS (NPT = N / WS states
+// per lane): per lane and time step, the state updates (~3.3 issue slots per
+// state with packed f32x2 math), the per-step loads, and this lane's share of
+// the per-(t, d) work; the machine runs ceil(warps / schedulers) rounds, and a
+// round with fewer than two warps per scheduler hides latency poorly.
+double plan_cost(int64_t channels, int WS, int npt) {
     const double slots = 148.0 * 4.0;
-    const double warps = std::ceil(double(channels) * S / (32.0 * kc));
+    const double warps = std::ceil(double(channels) / 32.0) * WS;
     const double rounds = std::ceil(warps / slots);
     const double per_sched = warps / slots;
     const double eff = per_sched >= 2.0 ? 1.0 : (0.55 + 0.225 * per_sched);
-    const double lg = S == 8 ? 3 : S == 4 ? 2 : S == 2 ? 1 : 0;
-    const double per_lane = kc * (npt * 3.3 + 1.5) + 2.0 * std::ceil(npt / 4.0) +
-                            kc * 24.0 / S + kc * 2.0 * lg;
+    const double per_lane = npt * 3.3 + 3.0 + std::ceil(npt / 4.0) + 20.0 / WS;
     return rounds * per_lane / eff;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-template <typename T, int NPT, int S, int KC>
-size_t smem_bytes(int64_t N) {
-    return Layout<T, NPT, S, KC, kTC>(N).total + 1024;
+template <typename T, int NPT, int WS>
+size_t smem_bytes(int64_t N, int stages, int TC) {
+    if (TC == 16) return Layout<T, NPT, WS, 16>(N, stages).total + 1024;
+    return Layout<T, NPT, WS, 32>(N, stages).total + 1024;
 }
 
-#define SSM_FOR_EACH_VARIANT(X)                                                          \
-    X(1, 1, 1) X(2, 1, 1) X(4, 1, 1) X(8, 1, 1) X(16, 1, 1)                              \
-    X(1, 2, 1) X(2, 2, 1) X(4, 2, 1) X(8, 2, 1) X(16, 2, 1)                              \
-    X(1, 4, 1) X(2, 4, 1) X(4, 4, 1) X(8, 4, 1) X(16, 4, 1)                              \
-    X(1, 8, 1) X(2, 8, 1) X(4, 8, 1) X(8, 8, 1) X(16, 8, 1)                              \
-    X(2, 2, 2) X(4, 2, 2) X(8, 2, 2) X(2, 4, 2) X(4, 4, 2) X(8, 4, 2) X(2, 8, 2) X(4, 8, 2)
+#define SSM_FOR_EACH_VARIANT(X)                            \
+    X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1)               \
+    X(1, 2) X(2, 2) X(4, 2) X(8, 2) X(16, 2)               \
+    X(1, 4) X(2, 4) X(4, 4) X(8, 4) X(16, 4)               \
+    X(4, 8) X(8, 8) X(16, 8)
 
-bool variant_exists(int npt, int S, int kc) {
-#define SSM_EXISTS(NPT_, S_, KC_) \
-    if (npt == NPT_ && S == S_ && kc == KC_) return true;
+bool variant_exists(int npt, int ws) {
+#define SSM_EXISTS(NPT_, WS_) \
+    if (npt == NPT_ && ws == WS_) return true;
     SSM_FOR_EACH_VARIANT(SSM_EXISTS)
 #undef SSM_EXISTS
     return false;
 }
 
 template <typename T>
-size_t variant_smem(int npt, int S, int kc, int64_t N) {
-#define SSM_SMEM(NPT_, S_, KC_) \
-    if (npt == NPT_ && S == S_ && kc == KC_) return smem_bytes<T, NPT_, S_, KC_>(N);
+size_t variant_smem(int npt, int ws, int64_t N, int stages, int TC) {
+#define SSM_SMEM(NPT_, WS_) \
+    if (npt == NPT_ && ws == WS_) return smem_bytes<T, NPT_, WS_>(N, stages, TC);
     SSM_FOR_EACH_VARIANT(SSM_SMEM)
 #undef SSM_SMEM
     return 0;
@@ -754,36 +775,48 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
     Plan pl;
     const int64_t channels = batch * dim;
     double best = 1e300;
-    const int forced_s = g_force_lanes.load(), forced_kc = g_force_kc.load();
-    for (int kc : {1, 2}) {
-        for (int S : {1, 2, 4, 8}) {
-            const int npt = supported_npt((N + S - 1) / S);
-            if (npt == 0 || !variant_exists(npt, S, kc)) continue;
-            if (S > 1 && N <= int64_t(S / 2) * npt) continue;  // a whole lane would be padding
-            if (forced_s != 0 && S != forced_s) continue;
-            if (forced_kc != 0 && kc != forced_kc) continue;
-            if (variant_smem<T>(npt, S, kc, N) > kMaxSmem) continue;
-            const double cst = plan_cost(channels, S, npt, kc);
-            if (cst < best) {
-                best = cst;
-                pl.S = S;
-                pl.NPT = npt;
-                pl.KC = kc;
-            }
+    const int forced = g_force_groups.load();
+    for (int ws : {1, 2, 4, 8}) {
+        const int npt = supported_npt((N + ws - 1) / ws);
+        if (npt == 0 || !variant_exists(npt, ws)) continue;
+        if (ws > 1 && N <= int64_t(ws - 1) * npt) continue;  // a whole state group would be padding
+        if (forced != 0 && ws != forced) continue;
+        if (variant_smem<T>(npt, ws, N, 2, 16) > kMaxSmem) continue;
+        const double cst = plan_cost(channels, ws, npt);
+        if (cst < best) {
+            best = cst;
+            pl.WS = ws;
+            pl.NPT = npt;
         }
     }
-    if (best == 1e300) {  // forced choice not available: fall back to automatic
-        pl.S = N > 64 ? 8 : N > 32 ? 4 : N > 16 ? 2 : 1;
-        pl.NPT = supported_npt((N + pl.S - 1) / pl.S);
-        pl.KC = 1;
+    if (best == 1e300) {  // a forced choice that does not exist: automatic
+        pl.WS = N > 64 ? 8 : N > 32 ? 4 : N > 16 ? 2 : 1;
+        pl.NPT = supported_npt((N + pl.WS - 1) / pl.WS);
     }
-    pl.TC = kTC;
-    pl.DT = kWarps * (32 / pl.S) * pl.KC;
-    pl.smem = variant_smem<T>(pl.NPT, pl.S, pl.KC, N);
-    const int wb = pl.DT * int(es);
-    pl.row_span = wb < 128 ? wb : 128;
+    const int wc = pl.WS >= 4 ? 1 : 4 / pl.WS;
+    pl.DT = wc * 32;
+    pl.NT = wc * pl.WS * 32;
     const int64_t nblk = (dim + pl.DT - 1) / pl.DT;
     pl.grid = nblk * batch;
+    // Chunk length: 32 steps unless the grid does not fit in one wave of blocks
+    // at that footprint (then 16 steps: half the shared memory per block).
+    auto resident = [&](int tc) {
+        const size_t sm = variant_smem<T>(pl.NPT, pl.WS, N, 2, tc);
+        const int64_t by_smem = int64_t((228 * 1024) / (sm + 1024));
+        const int64_t by_threads = 2048 / pl.NT;
+        return std::min(by_smem, by_threads) * 148;
+    };
+    pl.TC = (variant_smem<T>(pl.NPT, pl.WS, N, 2, 32) <= kMaxSmem && pl.grid <= resident(32)) ? 32 : 16;
+    const int ft = g_force_chunk.load();
+    if (ft == 16 || (ft == 32 && variant_smem<T>(pl.NPT, pl.WS, N, 2, 32) <= kMaxSmem)) pl.TC = ft;
+    // A third ring stage keeps two chunks in flight where it costs little
+    // shared memory; wide tiles keep two stages.
+    pl.stages = variant_smem<T>(pl.NPT, pl.WS, N, 3, pl.TC) <= 100 * 1024 ? 3 : 2;
+    const int fs = g_force_stages.load();
+    if (fs != 0 && variant_smem<T>(pl.NPT, pl.WS, N, fs, pl.TC) <= kMaxSmem) pl.stages = fs;
+    pl.smem = variant_smem<T>(pl.NPT, pl.WS, N, pl.stages, pl.TC);
+    const int wb = pl.DT * int(es);
+    pl.row_span = wb < 128 ? wb : 128;
     const bool plain = g_plain_loads.load() != 0;
     pl.tma_udz = !plain && L > 0 && get_encode() != nullptr && (dim * int64_t(es)) % 16 == 0 &&
                  aligned(u, 16) && aligned(dt, 16) && aligned(y, 16) &&
@@ -794,10 +827,11 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
     return pl;
 }
 
-template <typename T, int NPT, int S, int KC>
+template <typename T, int NPT, int WS, int TC>
 int launch_one(const Plan& pl, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
-    auto kern = ssm_scan_fwd_kernel<T, NPT, S, KC, kTC>;
-    const size_t smem = smem_bytes<T, NPT, S, KC>(kp.N);
+    using G = Geo<T, NPT, WS, TC>;
+    auto kern = ssm_scan_fwd_kernel<T, NPT, WS, TC>;
+    const size_t smem = smem_bytes<T, NPT, WS>(kp.N, kp.stages, TC);
     // The opt-in shared-memory limit is a per-device function attribute.
     static std::atomic<size_t> configured[64];
     int dev = 0;
@@ -809,15 +843,17 @@ int launch_one(const Plan& pl, const CUtensorMap* tms, const KParams& kp, cudaSt
             return SSM_ERR_LAUNCH;
         cfg.store(smem);
     }
-    kern<<<dim3(unsigned(pl.grid)), dim3(kThreads), smem, stream>>>(tms[0], tms[1], tms[2], tms[3],
-                                                                     tms[4], tms[5], kp);
+    kern<<<dim3(unsigned(pl.grid)), dim3(G::NT), smem, stream>>>(tms[0], tms[1], tms[2], tms[3],
+                                                                  tms[4], tms[5], kp);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
 template <typename T>
 int dispatch(const Plan& pl, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
-#define SSM_CASE(NPT_, S_, KC_) \
-    if (pl.NPT == NPT_ && pl.S == S_ && pl.KC == KC_) return launch_one<T, NPT_, S_, KC_>(pl, tms, kp, stream);
+#define SSM_CASE(NPT_, WS_)                                                     \
+    if (pl.NPT == NPT_ && pl.WS == WS_)                                         \
+        return pl.TC == 16 ? launch_one<T, NPT_, WS_, 16>(pl, tms, kp, stream)  \
+                           : launch_one<T, NPT_, WS_, 32>(pl, tms, kp, stream);
     SSM_FOR_EACH_VARIANT(SSM_CASE)
 #undef SSM_CASE
     return SSM_ERR_UNSUPPORTED_N;
@@ -917,6 +953,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     kp.tma_udz = tma_udz ? 1 : 0;
     kp.tma_bc = tma_bc ? 1 : 0;
     kp.force_timeout = (tma_udz && g_force_timeout.load()) ? 1 : 0;
+    kp.stages = pl.stages;
     return dispatch<T>(pl, tms, kp, stream);
 }
 
@@ -983,14 +1020,14 @@ int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype, i
     const void* al = reinterpret_cast<const void*>(uintptr_t(256));
     const Plan pl = dtype == 1 ? make_plan<__nv_bfloat16>(batch, L, dim, N, al, al, al, al, al, al)
                                : make_plan<float>(batch, L, dim, N, al, al, al, al, al, al);
-    plan[0] = pl.S;
+    plan[0] = pl.WS;
     plan[1] = pl.NPT;
     plan[2] = pl.TC;
     plan[3] = pl.DT;
-    plan[4] = kThreads;
+    plan[4] = pl.NT;
     plan[5] = pl.grid;
     plan[6] = int64_t(pl.smem);
-    plan[7] = pl.KC;
+    plan[7] = pl.tma_udz ? 1 : 0;
     return SSM_OK;
 }
 
@@ -1004,13 +1041,17 @@ int ssm_set_knob(int key, int64_t value) {
             if (value != 0 && value != 1) return SSM_ERR_ARG;
             g_force_timeout.store(int(value));
             return SSM_OK;
-        case SSM_KNOB_LANES:
+        case SSM_KNOB_STATE_GROUPS:
             if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return SSM_ERR_ARG;
-            g_force_lanes.store(int(value));
+            g_force_groups.store(int(value));
             return SSM_OK;
-        case SSM_KNOB_CHANNELS_PER_LANE:
-            if (value != 0 && value != 1 && value != 2) return SSM_ERR_ARG;
-            g_force_kc.store(int(value));
+        case SSM_KNOB_STAGES:
+            if (value != 0 && (value < 2 || value > kMaxStages)) return SSM_ERR_ARG;
+            g_force_stages.store(int(value));
+            return SSM_OK;
+        case SSM_KNOB_CHUNK:
+            if (value != 0 && value != 16 && value != 32) return SSM_ERR_ARG;
+            g_force_chunk.store(int(value));
             return SSM_OK;
         case SSM_KNOB_PLAIN_LOADS:
             if (value != 0 && value != 1) return SSM_ERR_ARG;

@@ -35,9 +35,10 @@ SSM_MAX_N = 128
 
 SSM_KNOB_WAIT_NS = 1
 SSM_KNOB_FORCE_TIMEOUT = 2
-SSM_KNOB_LANES = 3
-SSM_KNOB_CHANNELS_PER_LANE = 4
+SSM_KNOB_STATE_GROUPS = 3
+SSM_KNOB_CHUNK = 4
 SSM_KNOB_PLAIN_LOADS = 5
+SSM_KNOB_STAGES = 6
 
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_last_device_status",
             "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
@@ -96,8 +97,8 @@ def ssm_scan_plan(batch, L, dim, N, dtype: int):
     st = _lib.ssm_scan_plan(batch, L, dim, N, int(dtype), out)
     if st != SSM_OK:
         raise SSMError(st, "ssm_scan_plan")
-    keys = ("lanes", "states_per_lane", "chunk", "channels_per_block", "threads",
-            "blocks", "smem_bytes", "channels_per_lane")
+    keys = ("state_groups", "states_per_lane", "chunk", "channels_per_block", "threads",
+            "blocks", "smem_bytes", "tma")
     return dict(zip(keys, [int(v) for v in out]))
 
 

@@ -89,10 +89,10 @@ def test_empty_problems_launch_nothing(fn):
 def test_knobs_validate():
     K = ssmscan
     assert ssm.ssm_set_knob(K.SSM_KNOB_WAIT_NS, 10) == K.SSM_ERR_ARG
-    assert ssm.ssm_set_knob(K.SSM_KNOB_LANES, 3) == K.SSM_ERR_ARG
-    assert ssm.ssm_set_knob(K.SSM_KNOB_CHANNELS_PER_LANE, 3) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(K.SSM_KNOB_STATE_GROUPS, 3) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(K.SSM_KNOB_CHUNK, 24) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(99, 0) == K.SSM_ERR_ARG
-    assert ssm.ssm_set_knob(K.SSM_KNOB_LANES, 0) == K.SSM_OK
+    assert ssm.ssm_set_knob(K.SSM_KNOB_STATE_GROUPS, 0) == K.SSM_OK
     assert ssm.ssm_set_knob(K.SSM_KNOB_WAIT_NS, 2_000_000_000) == K.SSM_OK
 
 
@@ -103,10 +103,11 @@ def test_knobs_validate():
 def test_plans_cover_the_state(shape, dtype):
     pl = ssm.ssm_scan_plan(*shape, dtype)
     batch, L, dim, N = shape
-    S, npt, kc = pl["lanes"], pl["states_per_lane"], pl["channels_per_lane"]
-    assert S in (1, 2, 4, 8) and npt in (1, 2, 4, 8, 16) and kc in (1, 2)
-    assert S * npt >= N and (S == 1 or (S // 2) * npt < N)        # no all-padding lane
-    assert pl["threads"] == 128 and pl["channels_per_block"] * S == 128 * kc
+    ws, npt = pl["state_groups"], pl["states_per_lane"]
+    assert ws in (1, 2, 4, 8) and npt in (1, 2, 4, 8, 16)
+    assert ws * npt >= N and (ws == 1 or (ws - 1) * npt < N)      # no all-padding group
+    wc = 1 if ws >= 4 else 4 // ws
+    assert pl["threads"] == 32 * wc * ws and pl["channels_per_block"] == 32 * wc
     assert pl["blocks"] == batch * -(-dim // pl["channels_per_block"])
     assert 0 < pl["smem_bytes"] <= 227 * 1024
 

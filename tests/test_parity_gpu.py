@@ -24,7 +24,8 @@ def wl_for(dtype, batch, L, dim, N, **flags):
 @pytest.fixture(autouse=True)
 def _reset_knobs():
     yield
-    for k in (ssmscan.SSM_KNOB_LANES, ssmscan.SSM_KNOB_CHANNELS_PER_LANE, ssmscan.SSM_KNOB_PLAIN_LOADS,
+    for k in (ssmscan.SSM_KNOB_STATE_GROUPS, ssmscan.SSM_KNOB_PLAIN_LOADS, ssmscan.SSM_KNOB_STAGES,
+              ssmscan.SSM_KNOB_CHUNK,
               ssmscan.SSM_KNOB_FORCE_TIMEOUT):
         ssm.ssm_set_knob(k, 0)
     ssm.ssm_set_knob(ssmscan.SSM_KNOB_WAIT_NS, 2_000_000_000)
@@ -70,15 +71,25 @@ def test_h_last_optional(dtype):
     assert rel_err(y, yr) <= TOL[dtype]
 
 
-@pytest.mark.parametrize("lanes", [1, 2, 4, 8])
-@pytest.mark.parametrize("kc", [1, 2])
+@pytest.mark.parametrize("groups", [1, 2, 4, 8])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("N", [16, 5])
-def test_every_lane_split(lanes, kc, dtype, N):
-    ssm.ssm_set_knob(ssmscan.SSM_KNOB_LANES, lanes)
-    ssm.ssm_set_knob(ssmscan.SSM_KNOB_CHANNELS_PER_LANE, kc)
+@pytest.mark.parametrize("N", [16, 5, 40])
+@pytest.mark.parametrize("chunk", [16, 32])
+def test_every_state_split(groups, dtype, N, chunk):
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_STATE_GROUPS, groups)
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_CHUNK, chunk)
     wl = wl_for(dtype, 2, 150, 200, N)
-    check_full(W.make_inputs(wl, seed=lanes + kc + N), TOL[dtype], guard=64)
+    check_full(W.make_inputs(wl, seed=groups + N), TOL[dtype], guard=64)
+
+
+@pytest.mark.parametrize("stages", [2, 3, 4])
+def test_ring_depths_agree(stages):
+    wl = wl_for("bf16", 2, 333, 96, 16)
+    inp = W.make_inputs(wl, seed=12)
+    y0, h0 = run_gpu(inp)
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_STAGES, stages)
+    y1, h1 = run_gpu(inp, guard=64)
+    assert np.array_equal(y0, y1) and np.array_equal(h0, h1)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
