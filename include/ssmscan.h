@@ -36,7 +36,13 @@
  * with the skip vector D).  Every pointer is a DEVICE pointer owned by the
  * caller; the library never allocates, frees or keeps a pointer past the
  * call.  Work is enqueued on `stream` and the call returns without
- * synchronising.  y must not overlap any input.  Optional pointers may be
+ * synchronising.  The one exception to "never allocates": when the batch
+ * rows and channels alone leave most of the GPU idle (few channels, a long
+ * sequence), the sequence is cut into time segments (see below) and the call
+ * takes (segments - 1) * batch * dim * (N + 1) * 4 bytes of scratch with
+ * cudaMallocAsync on `stream` and returns it with cudaFreeAsync on the same
+ * stream; ssm_scan_plan() reports both numbers.  y must not overlap any
+ * input.  Optional pointers may be
  * NULL: D (no skip), z (no gate), delta_bias (bias 0), h_last (not written).
  * A required pointer may be NULL only when its tensor has no elements (for
  * example u, delta and y when L = 0, which still writes h_last = 0).
@@ -46,6 +52,18 @@
  * uint16_t) while A, D, delta_bias and h_last stay fp32; y is rounded to
  * nearest-even.  Results match an fp64 evaluation to |err| <= 1e-4 (1+|ref|)
  * for fp32 inputs and <= 2e-2 (1+|ref|) for bf16 inputs.
+ *
+ * Time segments
+ * -------------
+ * The recurrence h_t = a_t h_{t-1} + b_t composes associatively: two spans
+ * (a1, b1) then (a2, b2) act as (a1 a2, a2 b1 + b2) (the scan-operator
+ * description on the Obsidian "Mamba" note, section 5.1, "parallel scan").
+ * For one state, the product of a_t over a span is exp(A * sum of dt), so a
+ * span is summarised by its end state from zero and its sum of dt.  A first
+ * pass computes these summaries for every segment but the last; the second
+ * pass starts each segment from the fold of the summaries before it and
+ * produces y and h_last exactly as the sequential loop defines them (up to
+ * fp32 rounding order).
  *
  * Errors
  * ------
@@ -82,7 +100,8 @@ typedef enum {
     SSM_ERR_LAUNCH = 5,          /* the CUDA runtime refused the launch        */
     SSM_ERR_TIMEOUT = 6,         /* a bounded device-side wait ran out         */
     SSM_ERR_ALIAS = 7,           /* y overlaps an input                        */
-    SSM_ERR_ARG = 8              /* an invalid debug key or value              */
+    SSM_ERR_ARG = 8,             /* an invalid debug key or value              */
+    SSM_ERR_NOMEM = 9            /* stream-ordered scratch allocation failed   */
 } ssm_status;
 
 /* Largest state size N the kernels are built for. */
@@ -124,16 +143,17 @@ SSM_API const char *ssm_status_string(int status);
 
 /*
  * Launch plan the library would use for a problem, without launching.
- * dtype: 0 = fp32, 1 = bf16.  On SSM_OK, plan[0..7] receives:
+ * dtype: 0 = fp32, 1 = bf16.  On SSM_OK, plan[0..9] receives:
  *   [0] state groups WS                [1] states per lane NPT
  *   [2] timesteps per chunk            [3] channels per block
- *   [4] threads per block              [5] blocks in the grid
+ *   [4] threads per block              [5] blocks per time segment
  *   [6] dynamic shared bytes           [7] 1 if tiles move by TMA, else 0
+ *   [8] time segments (1: one pass)    [9] scratch bytes taken per call
  * Each channel's N states are split over WS warps (state groups), NPT states
  * per lane (N <= WS * NPT); a lane is a channel.
  */
 SSM_API int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype,
-                  int64_t plan[8]);
+                  int64_t plan[10]);
 
 /*
  * Process-wide knobs for tests and tuning sweeps (not for production use;
@@ -149,6 +169,8 @@ SSM_API int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int 
  *   SSM_KNOB_STAGES         force the TMA ring depth (2, 3 or 4); 0 = automatic
  *   SSM_KNOB_CHUNK          force timesteps per chunk (16 or 32); 0 = automatic
  *   SSM_KNOB_PLAIN_LOADS    1: move tiles with plain loads even when TMA applies
+ *   SSM_KNOB_SEGMENTS       force the number of time segments (1 .. 64,
+ *                           capped at the number of chunks); 0 = automatic
  * A forced combination the library is not built for falls back to automatic.
  * Returns SSM_OK or SSM_ERR_ARG.
  */
@@ -158,7 +180,8 @@ enum {
     SSM_KNOB_STATE_GROUPS = 3,
     SSM_KNOB_CHUNK = 4,
     SSM_KNOB_PLAIN_LOADS = 5,
-    SSM_KNOB_STAGES = 6
+    SSM_KNOB_STAGES = 6,
+    SSM_KNOB_SEGMENTS = 7
 };
 SSM_API int ssm_set_knob(int key, int64_t value);
 

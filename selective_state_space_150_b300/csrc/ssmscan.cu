@@ -55,6 +55,9 @@
 namespace {
 
 constexpr int kMaxStages = 4;  // deepest TMA ring; chunks in flight per block = stages - 1
+constexpr int kMaxSegments = 64;   // time segments of one call
+constexpr int kMinSegChunks = 8;   // shortest automatic segment, in chunks
+constexpr int kMinSegments = 8;    // fewest automatic segments once a split pays
 constexpr size_t kMaxSmem = 227 * 1024;  // opt-in shared memory per block on sm_103
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -303,6 +306,18 @@ struct KParams {
     int tma_bc;    // B / C tiles move by TMA
     int force_timeout;
     int stages;    // TMA ring depth (2 .. kMaxStages)
+    // Time split.  The sequence is cut into n_seg segments of seg_chunks
+    // chunks; block x works on segment x / (batch * nblk_d).  A summary pass
+    // (summary = 1) runs segments 0 .. n_seg-2 from a zero state without the
+    // readout and records each one's end state (hseg) and sum of dt (sseg);
+    // the main pass starts segment s from the composition of h0 and the
+    // summaries of segments 0 .. s-1.
+    int summary;
+    int n_seg;
+    int64_t seg_chunks;
+    float* hseg;        // [n_seg-1][batch][dim][N]
+    float* sseg;        // [n_seg-1][batch][dim]
+    const float* h0;    // [batch][dim][N] or null (zero initial state)
 };
 
 // Compile-time geometry of one block.
@@ -336,21 +351,22 @@ struct Geo {
 //   s_gs      [TC][DT] float2        (g, D*u*g), g = silu(z) or 1
 //   s_part    [WS][TC][DT] fp32      each state group's partial readout
 //   s_y       2 x tile               output tiles for the TMA store
-template <typename T, int NPT, int WS, int TC>
+//   The summary pass (SUM) keeps only u, delta, B in the ring, s_B and s_dd.
+template <typename T, int NPT, int WS, int TC, bool SUM = false>
 struct Layout {
     using G = Geo<T, NPT, WS, TC>;
     size_t tile_bc, stage, off_raw, off_bf, off_cf, off_dd, off_gs, off_part, off_y, off_bar, total;
     __host__ __device__ Layout(int64_t N, int stages) {
         tile_bc = round1k(size_t(TC) * size_t(N) * G::ES);
-        stage = 3 * G::TILE + 2 * tile_bc;
+        stage = (SUM ? 2 : 3) * G::TILE + (SUM ? 1 : 2) * tile_bc;
         off_raw = 0;
         off_bf = off_raw + size_t(stages) * stage;
         off_cf = off_bf + round1k(size_t(TC) * G::NP * 4);
-        off_dd = off_cf + round1k(size_t(TC) * G::NP * 4);
+        off_dd = off_cf + (SUM ? 0 : round1k(size_t(TC) * G::NP * 4));
         off_gs = off_dd + round1k(size_t(TC) * G::DT * 8);
-        off_part = off_gs + round1k(size_t(TC) * G::DT * 8);
-        off_y = off_part + round1k(size_t(WS) * TC * G::DT * 4);
-        off_bar = off_y + 2 * G::TILE;
+        off_part = off_gs + (SUM ? 0 : round1k(size_t(TC) * G::DT * 8));
+        off_y = off_part + (SUM ? 0 : round1k(size_t(WS) * TC * G::DT * 4));
+        off_bar = off_y + (SUM ? 0 : 2 * G::TILE);
         total = off_bar + 64;
     }
 };
@@ -358,6 +374,37 @@ struct Layout {
 // The scan over one chunk for one lane: channel c (dd, part already offset to
 // it), states sg*NPT.. (Bs, Cs already offset).  Restrict-qualified so the
 // compiler may move later steps' loads above earlier steps' partial stores.
+// Summary variant: the same state update without the readout; returns the
+// chunk's sum of dt for this channel (padded steps hold dt = 0).
+template <int NPT, int NP, int DT, int TC>
+__device__ __forceinline__ float scan_chunk_summary(const float2* __restrict__ dd,
+                                                   const float* __restrict__ Bs,
+                                                   const float (&a2)[NPT], float (&h)[NPT]) {
+    float sdt = 0.f;
+#pragma unroll 8
+    for (int t = 0; t < TC; ++t) {
+        const float2 v = dd[t * DT];
+        float bb[NPT];
+        ld_states<NPT>(Bs + t * NP, bb);
+        sdt += v.x;
+        if constexpr (NPT == 1) {
+            h[0] = fmaf(ex2_approx(v.x * a2[0]), h[0], v.y * bb[0]);
+        } else {
+            const float2 vx = make_float2(v.x, v.x), vy = make_float2(v.y, v.y);
+#pragma unroll
+            for (int j = 0; j < NPT; j += 2) {
+                const float2 x = __fmul2_rn(vx, make_float2(a2[j], a2[j + 1]));
+                const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                const float2 w = __fmul2_rn(vy, make_float2(bb[j], bb[j + 1]));
+                const float2 hh = __ffma2_rn(e, make_float2(h[j], h[j + 1]), w);
+                h[j] = hh.x;
+                h[j + 1] = hh.y;
+            }
+        }
+    }
+    return sdt;
+}
+
 template <int NPT, int NP, int DT, int TC>
 __device__ __forceinline__ void scan_chunk(const float2* __restrict__ dd,
                                            const float* __restrict__ Bs,
@@ -394,7 +441,7 @@ __device__ __forceinline__ void scan_chunk(const float2* __restrict__ dd,
     }
 }
 
-template <typename T, int NPT, int WS, int TC>
+template <typename T, int NPT, int WS, int TC, bool SUMMARY>
 __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
     ssm_scan_fwd_kernel(const __grid_constant__ CUtensorMap tm_u,
                         const __grid_constant__ CUtensorMap tm_dt,
@@ -412,7 +459,7 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
     extern __shared__ unsigned char smem_raw[];
     __shared__ int s_abort;
     unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const Layout<T, NPT, WS, TC> lay(p.N, p.stages);
+    const Layout<T, NPT, WS, TC, SUMMARY> lay(p.N, p.stages);
     const int nst = p.stages;
 
     const int tid = threadIdx.x;
@@ -420,17 +467,21 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
     const int ct = warp / WS, sg = warp % WS;  // channel tile, state group
     const int c = ct * 32 + lane;              // this lane's channel in the tile
     const int64_t N = p.N, L = p.L, dim = p.dim;
-    const int64_t b = blockIdx.x / p.nblk_d;
+    const int64_t rowblk = blockIdx.x / p.nblk_d;
+    const int64_t b = rowblk % p.batch;
+    const int64_t seg = rowblk / p.batch;
     const int64_t d0 = (blockIdx.x % p.nblk_d) * DT;
+    constexpr bool summary = SUMMARY;
 
     unsigned char* const raw0 = base + lay.off_raw;
     const uint32_t stage_b = uint32_t(lay.stage), tbc = uint32_t(lay.tile_bc);
     constexpr uint32_t TILE = uint32_t(G::TILE);
+    constexpr uint32_t NTILE = SUMMARY ? 2 : 3;  // u, delta (, z) tiles per stage
     auto raw_u = [=](int s) { return raw0 + s * stage_b; };
     auto raw_dt = [=](int s) { return raw0 + s * stage_b + TILE; };
     auto raw_z = [=](int s) { return raw0 + s * stage_b + 2 * TILE; };
-    auto raw_B = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + 3 * TILE); };
-    auto raw_C = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + 3 * TILE + tbc); };
+    auto raw_B = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + NTILE * TILE); };
+    auto raw_C = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + NTILE * TILE + tbc); };
     float* const s_B = reinterpret_cast<float*>(base + lay.off_bf);
     float* const s_C = reinterpret_cast<float*>(base + lay.off_cf);
     float2* const s_dd = reinterpret_cast<float2*>(base + lay.off_dd);
@@ -440,10 +491,13 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
     const uint32_t bar0 = smem_u32(base + lay.off_bar);
     const uint32_t bar_never = bar0 + 8 * kMaxStages;  // a barrier nothing ever completes
 
-    const bool has_z = p.z != nullptr;
+    const bool has_z = p.z != nullptr && !summary;
     const int64_t nchunks = (L + TC - 1) / TC;
+    // This block's chunks: c_begin .. c_begin + nloc - 1 (its time segment).
+    const int64_t c_begin = seg * p.seg_chunks;
+    const int64_t nloc = (nchunks - c_begin < p.seg_chunks) ? nchunks - c_begin : p.seg_chunks;
     const uint32_t tx_bytes = uint32_t((has_z ? 3 : 2) * TC * G::WB) +
-                              (p.tma_bc ? uint32_t(2 * TC * N * ES) : 0u);
+                              (p.tma_bc ? uint32_t((summary ? 1 : 2) * TC * N * ES) : 0u);
     const bool bc_vec = p.tma_bc && N == NP && (N % 4) == 0;
 
     if (tid == 0) {
@@ -467,7 +521,7 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
         }
         if (p.tma_bc) {
             tma_load_3d(smem_u32(raw_B(ss)), &tm_B, 0, t0, int(b), bar);
-            tma_load_3d(smem_u32(raw_C(ss)), &tm_C, 0, t0, int(b), bar);
+            if (!summary) tma_load_3d(smem_u32(raw_C(ss)), &tm_C, 0, t0, int(b), bar);
         }
     };
 
@@ -479,8 +533,24 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
     for (int j = 0; j < NPT; ++j) {
         const int64_t n = int64_t(sg) * NPT + j;
         a2[j] = (scan_ok && n < N) ? p.A[d_scan * N + n] * kLog2e : 0.f;
-        h[j] = 0.f;
+        h[j] = (p.h0 != nullptr && !summary && scan_ok && n < N) ? p.h0[(b * dim + d_scan) * N + n]
+                                                                : 0.f;
     }
+    // Entry state of a later segment: fold the earlier segments' summaries,
+    // h <- exp(A * sum dt) h + h_seg, in time order.
+    if (!summary && scan_ok) {
+        for (int64_t k = 0; k < seg; ++k) {
+            const int64_t r = (k * p.batch + b) * dim + d_scan;
+            const float sdt = p.sseg[r];
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) {
+                const int64_t n = int64_t(sg) * NPT + j;
+                if (n < N) h[j] = fmaf(ex2_approx(a2[j] * sdt), h[j], p.hseg[r * N + n]);
+            }
+        }
+    }
+    double sdt_seg = 0.0;  // summary pass: this segment's sum of dt
+    (void)sdt_seg;
 
     // ---- PREP / POST role: channel pair pp (channels 2pp, 2pp+1), steps
     //      tq0, tq0 + TSTEP, ... (ITEMS of them per chunk)
@@ -504,22 +574,23 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
     T* gy = static_cast<T*>(p.y);
 
     if (p.tma_udz && tid == 0)
-        for (int64_t cc = 0; cc < nst - 1 && cc < nchunks; ++cc) issue_loads(cc, int(cc));
+        for (int64_t cc = 0; cc < nst - 1 && cc < nloc; ++cc) issue_loads(c_begin + cc, int(cc));
 
     // Ring position of this chunk (st), its mbarrier phase parity (ph), and the
     // stage the prefetch refills (sa), advanced without divisions.
     int st = 0, sa = nst - 1;
     uint32_t ph = 0;
-    for (int64_t chunk = 0; chunk < nchunks; ++chunk) {
+    for (int64_t ci = 0; ci < nloc; ++ci) {
+        const int64_t chunk = c_begin + ci;
         const int64_t t0 = chunk * TC;
         const int tv = int(L - t0 < TC ? L - t0 : int64_t(TC));
 
         if (p.tma_udz) {
             // Refill the stage the previous chunk released (nst - 1 chunks ahead).
-            const int64_t ahead = chunk + nst - 1;
-            if (tid == 0 && ahead < nchunks) issue_loads(ahead, sa);
+            const int64_t ahead = ci + nst - 1;
+            if (tid == 0 && ahead < nloc) issue_loads(c_begin + ahead, sa);
             bool ok = true;
-            if (p.force_timeout && chunk == 0) ok = mbar_wait_bounded(bar_never, 0, p.wait_ns);
+            if (p.force_timeout && ci == 0) ok = mbar_wait_bounded(bar_never, 0, p.wait_ns);
             if (ok) ok = mbar_wait_bounded(bar0 + 8 * st, ph, p.wait_ns);
             if (!ok) {
                 atomicOr(&g_ssm_status, kDevTimeout);
@@ -545,7 +616,7 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
         // B, C widened to fp32 (rows past L and states past N are zero).
         if (bc_vec) {
             const int items = TC * NP / 4;
-            for (int i = tid; i < 2 * items; i += NT) {
+            for (int i = tid; i < (summary ? 1 : 2) * items; i += NT) {
                 const bool isC = i >= items;
                 const int j = (isC ? i - items : i) * 4;
                 const float4 qv = ld_quad<T>((isC ? raw_C(st) : raw_B(st)) + j);
@@ -558,15 +629,15 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
                 if (n < N && t < tv) {
                     if (p.tma_bc) {
                         bv = E::to_f(raw_B(st)[t * N + n]);
-                        cv = E::to_f(raw_C(st)[t * N + n]);
+                        if (!summary) cv = E::to_f(raw_C(st)[t * N + n]);
                     } else {
                         const int64_t off = (b * L + t0 + t) * N + n;
                         bv = E::to_f(gB[off]);
-                        cv = E::to_f(gC[off]);
+                        if (!summary) cv = E::to_f(gC[off]);
                     }
                 }
                 s_B[i] = bv;
-                s_C[i] = cv;
+                if constexpr (!summary) s_C[i] = cv;
             }
         }
         // dt = softplus(delta + bias), dt*u, g = silu(z) and D*u*g per (step,
@@ -597,7 +668,9 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
                 const bool live = t < tv;
                 *reinterpret_cast<float4*>(s_dd + t * DT + 2 * pp) =
                     live ? make_float4(x.x, xu.x, x.y, xu.y) : make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4*>(s_gs + t * DT + 2 * pp) = make_float4(g.x, su.x, g.y, su.y);
+                if constexpr (!summary)  // the summary layout has no s_gs
+                    *reinterpret_cast<float4*>(s_gs + t * DT + 2 * pp) =
+                        make_float4(g.x, su.x, g.y, su.y);
             }
         }
         if (p.tma_udz && tid == 0) bulk_wait_read_le1();  // this chunk's output tile is free
@@ -609,7 +682,7 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
                 bool ok = true;
                 int s2 = st;
                 uint32_t p2 = ph;
-                for (int64_t cc = chunk; cc < chunk + nst && cc < nchunks; ++cc) {
+                for (int64_t cc = ci; cc < ci + nst && cc < nloc; ++cc) {
                     ok = mbar_wait_bounded(bar0 + 8 * s2, p2, p.wait_ns) && ok;
                     if (++s2 == nst) { s2 = 0; p2 ^= 1u; }
                 }
@@ -620,12 +693,19 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
         }
 
         // ---------------- SCAN: all TC steps (padded ones are no-ops)
+        if constexpr (summary) {
+            sdt_seg += double(scan_chunk_summary<NPT, NP, DT, TC>(s_dd + c, s_B + sg * NPT, a2, h));
+            __syncthreads();  // the next PREP overwrites s_dd, s_B
+            if (++st == nst) { st = 0; ph ^= 1u; }
+            if (++sa == nst) sa = 0;
+            continue;
+        }
         scan_chunk<NPT, NP, DT, TC>(s_dd + c, s_B + sg * NPT, s_C + sg * NPT,
                                     s_part + sg * TC * DT + c, a2, h);
         __syncthreads();
 
         // ---------------- POST: y = (sum of the state groups' partials) g + D u g
-        unsigned char* yt = s_y0 + (chunk & 1) * TILE;
+        unsigned char* yt = s_y0 + (ci & 1) * TILE;
 #pragma unroll
         for (int it = 0; it < ITEMS; ++it) {
             const int t = tq0 + it * TSTEP;
@@ -661,7 +741,20 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
     }
     if (p.tma_udz && tid == 0) bulk_wait_all();
 
-    if (p.h_last != nullptr && scan_ok) {
+    if constexpr (summary) {
+        if (scan_ok) {
+            const int64_t r = (seg * p.batch + b) * dim + d_scan;
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) {
+                const int64_t n = int64_t(sg) * NPT + j;
+                if (n < N) p.hseg[r * N + n] = h[j];
+            }
+            if (sg == 0) p.sseg[r] = float(sdt_seg);
+        }
+        return;
+    }
+    // Only the last segment holds the final state.
+    if (p.h_last != nullptr && scan_ok && seg == p.n_seg - 1) {
 #pragma unroll
         for (int j = 0; j < NPT; ++j) {
             const int64_t n = int64_t(sg) * NPT + j;
@@ -676,6 +769,7 @@ std::atomic<int> g_force_timeout{0};
 std::atomic<int> g_force_groups{0};
 std::atomic<int> g_force_stages{0};
 std::atomic<int> g_force_chunk{0};
+std::atomic<int> g_force_segments{0};
 std::atomic<int> g_plain_loads{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -710,7 +804,9 @@ bool encode3d(CUtensorMap* tm, CUtensorMapDataType ty, size_t es, const void* pt
 
 struct Plan {
     int WS = 1, NPT = 1, TC = 32, DT = 128, NT = 128, stages = 2;
-    int64_t grid = 0;
+    int64_t grid = 0;       // blocks of one time segment (batch x channel tiles)
+    int n_seg = 1;          // time segments
+    int64_t seg_chunks = 0; // chunks per segment
     size_t smem = 0;
     int row_span = 16;
     bool tma_udz = false, tma_bc = false;
@@ -739,10 +835,10 @@ double plan_cost(int64_t channels, int WS, int npt) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-template <typename T, int NPT, int WS>
+template <typename T, int NPT, int WS, bool SUM = false>
 size_t smem_bytes(int64_t N, int stages, int TC) {
-    if (TC == 16) return Layout<T, NPT, WS, 16>(N, stages).total + 1024;
-    return Layout<T, NPT, WS, 32>(N, stages).total + 1024;
+    if (TC == 16) return Layout<T, NPT, WS, 16, SUM>(N, stages).total + 1024;
+    return Layout<T, NPT, WS, 32, SUM>(N, stages).total + 1024;
 }
 
 #define SSM_FOR_EACH_VARIANT(X)                            \
@@ -815,6 +911,26 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
     const int fs = g_force_stages.load();
     if (fs != 0 && variant_smem<T>(pl.NPT, pl.WS, N, fs, pl.TC) <= kMaxSmem) pl.stages = fs;
     pl.smem = variant_smem<T>(pl.NPT, pl.WS, N, pl.stages, pl.TC);
+    // Time split: when the (batch, channel) blocks fill less than half of one
+    // wave, cut the sequence into segments: as many as fill one wave, and at
+    // least kMinSegments (the summary pass then has enough blocks too and the
+    // main pass's last wave is small), each segment at least kMinSegChunks
+    // chunks long.
+    const int64_t nchunks = (L + pl.TC - 1) / pl.TC;
+    {
+        const int64_t by_smem = int64_t((228 * 1024) / (pl.smem + 1024));
+        const int64_t cap = std::min<int64_t>(by_smem, 2048 / pl.NT) * 148;
+        int64_t ns = 1;
+        if (pl.grid > 0 && 2 * pl.grid <= cap) ns = std::max<int64_t>(kMinSegments, cap / pl.grid);
+        ns = std::min<int64_t>(ns, kMaxSegments);
+        ns = std::min<int64_t>(ns, nchunks / kMinSegChunks);
+        const int fseg = g_force_segments.load();
+        if (fseg > 0) ns = std::min<int64_t>(fseg, nchunks);
+        if (ns < 2) ns = 1;
+        pl.seg_chunks = ns > 1 ? (nchunks + ns - 1) / ns : nchunks;
+        pl.n_seg = ns > 1 ? int((nchunks + pl.seg_chunks - 1) / pl.seg_chunks) : 1;
+        if (pl.seg_chunks < 1) pl.seg_chunks = 1;
+    }
     const int wb = pl.DT * int(es);
     pl.row_span = wb < 128 ? wb : 128;
     const bool plain = g_plain_loads.load() != 0;
@@ -827,11 +943,11 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
     return pl;
 }
 
-template <typename T, int NPT, int WS, int TC>
-int launch_one(const Plan& pl, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
+template <typename T, int NPT, int WS, int TC, bool SUMMARY>
+int launch_one(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
     using G = Geo<T, NPT, WS, TC>;
-    auto kern = ssm_scan_fwd_kernel<T, NPT, WS, TC>;
-    const size_t smem = smem_bytes<T, NPT, WS>(kp.N, kp.stages, TC);
+    auto kern = ssm_scan_fwd_kernel<T, NPT, WS, TC, SUMMARY>;
+    const size_t smem = smem_bytes<T, NPT, WS, SUMMARY>(kp.N, kp.stages, TC);
     // The opt-in shared-memory limit is a per-device function attribute.
     static std::atomic<size_t> configured[64];
     int dev = 0;
@@ -843,17 +959,22 @@ int launch_one(const Plan& pl, const CUtensorMap* tms, const KParams& kp, cudaSt
             return SSM_ERR_LAUNCH;
         cfg.store(smem);
     }
-    kern<<<dim3(unsigned(pl.grid)), dim3(G::NT), smem, stream>>>(tms[0], tms[1], tms[2], tms[3],
-                                                                  tms[4], tms[5], kp);
+    kern<<<dim3(unsigned(grid)), dim3(G::NT), smem, stream>>>(tms[0], tms[1], tms[2], tms[3],
+                                                               tms[4], tms[5], kp);
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
 template <typename T>
-int dispatch(const Plan& pl, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
-#define SSM_CASE(NPT_, WS_)                                                     \
-    if (pl.NPT == NPT_ && pl.WS == WS_)                                         \
-        return pl.TC == 16 ? launch_one<T, NPT_, WS_, 16>(pl, tms, kp, stream)  \
-                           : launch_one<T, NPT_, WS_, 32>(pl, tms, kp, stream);
+int dispatch(const Plan& pl, int64_t grid, const CUtensorMap* tms, const KParams& kp,
+             cudaStream_t stream) {
+#define SSM_CASE(NPT_, WS_)                                                            \
+    if (pl.NPT == NPT_ && pl.WS == WS_) {                                              \
+        if (kp.summary)                                                                \
+            return pl.TC == 16 ? launch_one<T, NPT_, WS_, 16, true>(grid, tms, kp, stream)  \
+                               : launch_one<T, NPT_, WS_, 32, true>(grid, tms, kp, stream); \
+        return pl.TC == 16 ? launch_one<T, NPT_, WS_, 16, false>(grid, tms, kp, stream)     \
+                           : launch_one<T, NPT_, WS_, 32, false>(grid, tms, kp, stream);    \
+    }
     SSM_FOR_EACH_VARIANT(SSM_CASE)
 #undef SSM_CASE
     return SSM_ERR_UNSUPPORTED_N;
@@ -911,7 +1032,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     if (batch == 0 || dim == 0) return SSM_OK;  // nothing to compute
 
     const Plan pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C);
-    if (pl.grid > int64_t(0x7fffffff)) return SSM_ERR_SIZE;
+    if (pl.grid * pl.n_seg > int64_t(0x7fffffff)) return SSM_ERR_SIZE;
 
     CUtensorMap tms[6];
     std::memset(tms, 0, sizeof(tms));
@@ -954,7 +1075,33 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     kp.tma_bc = tma_bc ? 1 : 0;
     kp.force_timeout = (tma_udz && g_force_timeout.load()) ? 1 : 0;
     kp.stages = pl.stages;
-    return dispatch<T>(pl, tms, kp, stream);
+    kp.summary = 0;
+    kp.n_seg = pl.n_seg;
+    kp.seg_chunks = pl.seg_chunks;
+    kp.hseg = nullptr;
+    kp.sseg = nullptr;
+    kp.h0 = nullptr;
+    if (pl.n_seg == 1) return dispatch<T>(pl, pl.grid, tms, kp, stream);
+
+    // Segment summaries live in stream-ordered scratch from the device's
+    // default memory pool, released on the stream after the main pass.
+    const int64_t nsum = int64_t(pl.n_seg - 1) * batch * dim;
+    void* scratch = nullptr;
+    if (cudaMallocAsync(&scratch, size_t(nsum) * size_t(N + 1) * 4, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SSM_ERR_NOMEM;
+    }
+    kp.hseg = static_cast<float*>(scratch);
+    kp.sseg = kp.hseg + nsum * N;
+    KParams ks = kp;
+    ks.summary = 1;
+    ks.z = nullptr;
+    ks.h_last = nullptr;
+    ks.force_timeout = 0;
+    int st = dispatch<T>(pl, pl.grid * (pl.n_seg - 1), tms, ks, stream);
+    if (st == SSM_OK) st = dispatch<T>(pl, pl.grid * pl.n_seg, tms, kp, stream);
+    if (cudaFreeAsync(scratch, stream) != cudaSuccess && st == SSM_OK) st = SSM_ERR_LAUNCH;
+    return st;
 }
 
 }  // namespace
@@ -1007,11 +1154,12 @@ const char* ssm_status_string(int status) {
         case SSM_ERR_TIMEOUT: return "a bounded device-side wait ran out";
         case SSM_ERR_ALIAS: return "an output overlaps an input";
         case SSM_ERR_ARG: return "invalid knob key or value";
+        case SSM_ERR_NOMEM: return "stream-ordered scratch allocation failed";
         default: return "unknown status";
     }
 }
 
-int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype, int64_t plan[8]) {
+int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype, int64_t plan[10]) {
     if (!plan) return SSM_ERR_NULL;
     if (batch < 0 || L < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED_N;
@@ -1028,6 +1176,8 @@ int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype, i
     plan[5] = pl.grid;
     plan[6] = int64_t(pl.smem);
     plan[7] = pl.tma_udz ? 1 : 0;
+    plan[8] = pl.n_seg;
+    plan[9] = pl.n_seg > 1 ? int64_t(pl.n_seg - 1) * batch * dim * (N + 1) * 4 : 0;
     return SSM_OK;
 }
 
@@ -1056,6 +1206,10 @@ int ssm_set_knob(int key, int64_t value) {
         case SSM_KNOB_PLAIN_LOADS:
             if (value != 0 && value != 1) return SSM_ERR_ARG;
             g_plain_loads.store(int(value));
+            return SSM_OK;
+        case SSM_KNOB_SEGMENTS:
+            if (value < 0 || value > kMaxSegments) return SSM_ERR_ARG;
+            g_force_segments.store(int(value));
             return SSM_OK;
         default:
             return SSM_ERR_ARG;

@@ -31,6 +31,7 @@ SSM_ERR_LAUNCH = 5
 SSM_ERR_TIMEOUT = 6
 SSM_ERR_ALIAS = 7
 SSM_ERR_ARG = 8
+SSM_ERR_NOMEM = 9
 SSM_MAX_N = 128
 
 SSM_KNOB_WAIT_NS = 1
@@ -39,6 +40,7 @@ SSM_KNOB_STATE_GROUPS = 3
 SSM_KNOB_CHUNK = 4
 SSM_KNOB_PLAIN_LOADS = 5
 SSM_KNOB_STAGES = 6
+SSM_KNOB_SEGMENTS = 7
 
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_last_device_status",
             "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
@@ -93,12 +95,12 @@ def ssm_status_string(status: int) -> str:
 
 def ssm_scan_plan(batch, L, dim, N, dtype: int):
     """Launch plan as a dict (see include/ssmscan.h); raises on a bad argument."""
-    out = (_i64 * 8)()
+    out = (_i64 * 10)()
     st = _lib.ssm_scan_plan(batch, L, dim, N, int(dtype), out)
     if st != SSM_OK:
         raise SSMError(st, "ssm_scan_plan")
     keys = ("state_groups", "states_per_lane", "chunk", "channels_per_block", "threads",
-            "blocks", "smem_bytes", "tma")
+            "blocks", "smem_bytes", "tma", "segments", "scratch_bytes")
     return dict(zip(keys, [int(v) for v in out]))
 
 

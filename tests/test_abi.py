@@ -91,6 +91,8 @@ def test_knobs_validate():
     assert ssm.ssm_set_knob(K.SSM_KNOB_WAIT_NS, 10) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(K.SSM_KNOB_STATE_GROUPS, 3) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(K.SSM_KNOB_CHUNK, 24) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(K.SSM_KNOB_SEGMENTS, -1) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(K.SSM_KNOB_SEGMENTS, 65) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(99, 0) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(K.SSM_KNOB_STATE_GROUPS, 0) == K.SSM_OK
     assert ssm.ssm_set_knob(K.SSM_KNOB_WAIT_NS, 2_000_000_000) == K.SSM_OK
@@ -110,6 +112,32 @@ def test_plans_cover_the_state(shape, dtype):
     assert pl["threads"] == 32 * wc * ws and pl["channels_per_block"] == 32 * wc
     assert pl["blocks"] == batch * -(-dim // pl["channels_per_block"])
     assert 0 < pl["smem_bytes"] <= 227 * 1024
+    nchunks = -(-L // pl["chunk"])
+    seg = pl["segments"]
+    assert 1 <= seg <= max(1, nchunks // 8)           # every automatic segment >= 8 chunks
+    assert pl["scratch_bytes"] == (seg - 1) * batch * dim * (N + 1) * 4
+
+
+def test_time_split_only_where_channels_leave_the_gpu_idle():
+    # 8 x 1536 channels fill the GPU: one pass, no scratch
+    assert ssm.ssm_scan_plan(8, 2048, 1536, 16, 1)["segments"] == 1
+    # one row of 5120 channels over 131072 steps: split in time
+    assert ssm.ssm_scan_plan(1, 131072, 5120, 16, 1)["segments"] > 1
+
+
+@pytest.mark.parametrize("forced,L,expect", [(5, 1000, 5), (64, 100, 4), (3, 32, 1), (1, 5000, 1)])
+def test_forced_segments_are_capped_by_chunks(forced, L, expect):
+    K = ssmscan
+    try:
+        assert ssm.ssm_set_knob(K.SSM_KNOB_SEGMENTS, forced) == K.SSM_OK
+        pl = ssm.ssm_scan_plan(1, L, 64, 16, 1)
+        nchunks = -(-L // pl["chunk"])
+        per = -(-nchunks // min(forced, nchunks))
+        assert pl["segments"] == (-(-nchunks // per) if min(forced, nchunks) > 1 else 1)
+        if pl["chunk"] == 32:
+            assert pl["segments"] == expect
+    finally:
+        ssm.ssm_set_knob(K.SSM_KNOB_SEGMENTS, 0)
 
 
 def test_plan_rejects_bad_arguments():

@@ -25,7 +25,7 @@ def wl_for(dtype, batch, L, dim, N, **flags):
 def _reset_knobs():
     yield
     for k in (ssmscan.SSM_KNOB_STATE_GROUPS, ssmscan.SSM_KNOB_PLAIN_LOADS, ssmscan.SSM_KNOB_STAGES,
-              ssmscan.SSM_KNOB_CHUNK,
+              ssmscan.SSM_KNOB_CHUNK, ssmscan.SSM_KNOB_SEGMENTS,
               ssmscan.SSM_KNOB_FORCE_TIMEOUT):
         ssm.ssm_set_knob(k, 0)
     ssm.ssm_set_knob(ssmscan.SSM_KNOB_WAIT_NS, 2_000_000_000)
@@ -103,6 +103,62 @@ def test_plain_load_path_matches_tma_path(dtype):
     assert np.array_equal(y_tma, y_pl) and np.array_equal(h_tma, h_pl)
     yr, hr = oracle_ref(W.decoded(inp))
     assert rel_err(y_pl, yr) <= TOL[dtype]
+
+
+# ---------------------------------------------------------------- time segments
+# Shapes with ragged chunk tails, segments that do not divide the chunks, the
+# segment count capped by the chunk count (64 forced on 66 chunks), and N not a
+# multiple of the states per lane.
+SEG_CASES = [(2, (2, 130, 72, 16)), (3, (1, 1000, 40, 16)), (5, (2, 333, 96, 5)),
+             (7, (1, 517, 33, 40)), (64, (1, 2100, 64, 16)), (4, (1, 300, 24, 128))]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("segs,shape", SEG_CASES)
+def test_time_segments_match_the_sequential_definition(dtype, segs, shape):
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, segs)
+    pl = ssm.ssm_scan_plan(*shape, 1 if dtype == "bf16" else 0)
+    assert pl["segments"] > 1
+    wl = wl_for(dtype, *shape)
+    check_full(W.make_inputs(wl, seed=segs), TOL[dtype], guard=64)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_time_segments_carry_long_memory(dtype):
+    """dt around 1e-4: the state hardly decays over the whole sequence, so
+    every segment's entry state depends on all earlier segments."""
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, 6)
+    wl = wl_for(dtype, 2, 600, 64, 16, softplus=False, delta_bias=False,
+                delta_kind="loguniform_td")
+    inp = W.make_inputs(wl, seed=21)
+    if dtype == "bf16":
+        small = W.decode(inp["delta"]) * 1e-3
+        inp["delta"] = W.f32_to_bf16_bits(small.astype(np.float32))
+    else:
+        inp["delta"] = (inp["delta"] * 1e-3).astype(np.float32)
+    check_full(inp, TOL[dtype], guard=64)
+
+
+@pytest.mark.parametrize("flags", [
+    dict(softplus=True, delta_bias=True, gate=True, skip=True, delta_kind="normal_raw"),
+    dict(softplus=False, delta_bias=False, gate=False, skip=False, delta_kind="loguniform_td"),
+])
+def test_time_segments_with_optional_arguments(flags):
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, 4)
+    wl = wl_for("bf16", 2, 400, 48, 16, **flags)
+    check_full(W.make_inputs(wl, seed=22), TOL["bf16"], guard=64)
+
+
+def test_time_segments_deterministic_and_plain_loads_agree():
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, 3)
+    wl = wl_for("bf16", 1, 700, 64, 16)
+    inp = W.make_inputs(wl, seed=23)
+    y1, h1 = run_gpu(inp)
+    y2, h2 = run_gpu(inp)
+    assert np.array_equal(y1, y2) and np.array_equal(h1, h2)
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_PLAIN_LOADS, 1)
+    y3, h3 = run_gpu(inp, guard=64)
+    assert np.array_equal(y1, y3) and np.array_equal(h1, h3)
 
 
 def test_deterministic():
