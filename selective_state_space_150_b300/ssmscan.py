@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libssmscan.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"libssmscan.so not found at {LIB_PATH}; build it with "
-        "`python -m selective_state_space_150_b300.build` (nvcc, sm_103a)")
+        "`python selective_state_space_150_b300/build.py` (nvcc, sm_103a)")
 
 _lib = ctypes.CDLL(LIB_PATH)
 
