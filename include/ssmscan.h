@@ -101,7 +101,9 @@ typedef enum {
     SSM_ERR_TIMEOUT = 6,         /* a bounded device-side wait ran out         */
     SSM_ERR_ALIAS = 7,           /* y overlaps an input                        */
     SSM_ERR_ARG = 8,             /* an invalid debug key or value              */
-    SSM_ERR_NOMEM = 9            /* stream-ordered scratch allocation failed   */
+    SSM_ERR_NOMEM = 9,           /* stream-ordered scratch allocation failed   */
+    SSM_ERR_SCRATCH = 10         /* the no-alloc entry point's static buffer   */
+                                 /* is too small for this problem              */
 } ssm_status;
 
 /* Largest state size N the kernels are built for. */
@@ -127,6 +129,41 @@ SSM_API int ssm_scan_fwd_bf16(const uint16_t *u, const uint16_t *delta, const fl
                       const uint16_t *B, const uint16_t *C, const float *D,
                       const uint16_t *z, const float *delta_bias, int softplus_flag,
                       uint16_t *y, float *h_last,
+                      int64_t batch, int64_t L, int64_t dim, int64_t N,
+                      cudaStream_t stream);
+
+/*
+ * No-allocation variant of ssm_scan_fwd_bf16 (an engineering addition: the
+ * pages describe nothing like it).  Same arguments, same kernels, same
+ * results bit for bit; the only difference is where the time-segment
+ * summaries live.  Instead of cudaMallocAsync scratch they go to one static
+ * device buffer of SSM_NOALLOC_SCRATCH_FLOATS fp32 words (8 MiB) that is part
+ * of the library's module image, so the call makes no allocation of any kind.
+ *
+ * For callers that cannot allocate inside the call: a process that has handed
+ * (almost) all device memory to its own caching allocator up front, so the
+ * driver's pool has no room for cudaMallocAsync; a latency-critical loop that
+ * must not enter an allocator (growing a pool maps new pages); and devices
+ * where the stream-ordered allocator is unavailable.
+ *
+ * Limit: a problem the plan runs in one pass (ssm_scan_plan: segments = 1)
+ * needs no scratch and is accepted at any size.  A segmented problem needs
+ * (segments - 1) * batch * dim * (N + 1) words; above
+ * SSM_NOALLOC_SCRATCH_FLOATS the call returns SSM_ERR_SCRATCH and launches
+ * nothing.  The summary pass writes every word the main pass reads, so
+ * nothing in the buffer has to start at zero and the call clears nothing.
+ *
+ * The buffer is shared by every call on a device: two calls in flight at the
+ * same time (other streams, other host threads) race on it and give wrong
+ * results.  Calls in one stream are ordered and safe.  The first call on a
+ * device looks up the buffer's address (cudaGetSymbolAddress, with that device
+ * current) and keeps it; make that first call before any stream capture.
+ */
+#define SSM_NOALLOC_SCRATCH_FLOATS 2097152
+SSM_API int ssm_scan_fwd_bf16_noalloc(const uint16_t *u, const uint16_t *delta,
+                      const float *A, const uint16_t *B, const uint16_t *C,
+                      const float *D, const uint16_t *z, const float *delta_bias,
+                      int softplus_flag, uint16_t *y, float *h_last,
                       int64_t batch, int64_t L, int64_t dim, int64_t N,
                       cudaStream_t stream);
 

@@ -8,6 +8,7 @@ from .ssmscan import (  # noqa: F401
     selective_scan_fwd,
     ssm_scan_fwd,
     ssm_scan_fwd_bf16,
+    ssm_scan_fwd_bf16_noalloc,
     ssm_scan_last_device_status,
     ssm_scan_plan,
     ssm_set_knob,

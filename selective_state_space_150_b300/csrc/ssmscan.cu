@@ -70,6 +70,13 @@ constexpr unsigned kDevDrainTimeout = 2u;  // ... and so did the drain after it
 
 __device__ unsigned int g_ssm_status = 0;
 
+// Segment scratch of ssm_scan_fwd_bf16_noalloc: one fixed buffer per device,
+// part of the module image, so that entry point never allocates.  Every call
+// through it on a device shares this buffer.
+constexpr int64_t kStaticScratchFloats = SSM_NOALLOC_SCRATCH_FLOATS;  // 8 MiB
+static_assert(kStaticScratchFloats == (int64_t(1) << 21), "8 MiB of fp32");
+static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
+
 namespace {
 
 // ------------------------------------------------------------------ PTX helpers
@@ -997,10 +1004,34 @@ bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
     return a0 < b0 + uintptr_t(nb) && b0 < a0 + uintptr_t(na);
 }
 
+// Device address of g_static_scratch on the current device, looked up once
+// per device (with that device current) and kept.
+int static_scratch(float** out) {
+    static std::mutex mu;
+    static float* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SSM_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
+            (void)cudaGetLastError();
+            return SSM_ERR_LAUNCH;
+        }
+        addr[dev] = static_cast<float*>(ptr);
+    }
+    *out = addr[dev];
+    return SSM_OK;
+}
+
+// fixed_scratch: false = segment scratch from cudaMallocAsync on the stream;
+// true = from g_static_scratch (nothing allocated; a problem whose segment
+// summaries do not fit is refused with SSM_ERR_SCRATCH before any launch).
 template <typename T>
 int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C, const float* D,
              const T* z, const float* delta_bias, int softplus_flag, T* y, float* h_last,
-             int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream) {
+             int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream,
+             bool fixed_scratch = false) {
     if (batch < 0 || L < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
     // A pointer may be NULL only when its tensor has no elements.
     if ((batch > 0 && L > 0 && dim > 0) && (!u || !delta || !y)) return SSM_ERR_NULL;
@@ -1084,10 +1115,18 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     if (pl.n_seg == 1) return dispatch<T>(pl, pl.grid, tms, kp, stream);
 
     // Segment summaries live in stream-ordered scratch from the device's
-    // default memory pool, released on the stream after the main pass.
+    // default memory pool, released on the stream after the main pass (or in
+    // the static buffer).  The summary pass writes every word the main pass
+    // reads, so nothing needs clearing.
     const int64_t nsum = int64_t(pl.n_seg - 1) * batch * dim;
     void* scratch = nullptr;
-    if (cudaMallocAsync(&scratch, size_t(nsum) * size_t(N + 1) * 4, stream) != cudaSuccess) {
+    if (fixed_scratch) {
+        if (nsum * (N + 1) > kStaticScratchFloats) return SSM_ERR_SCRATCH;
+        float* fs = nullptr;
+        const int st = static_scratch(&fs);
+        if (st != SSM_OK) return st;
+        scratch = fs;
+    } else if (cudaMallocAsync(&scratch, size_t(nsum) * size_t(N + 1) * 4, stream) != cudaSuccess) {
         (void)cudaGetLastError();
         return SSM_ERR_NOMEM;
     }
@@ -1100,7 +1139,8 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     ks.force_timeout = 0;
     int st = dispatch<T>(pl, pl.grid * (pl.n_seg - 1), tms, ks, stream);
     if (st == SSM_OK) st = dispatch<T>(pl, pl.grid * pl.n_seg, tms, kp, stream);
-    if (cudaFreeAsync(scratch, stream) != cudaSuccess && st == SSM_OK) st = SSM_ERR_LAUNCH;
+    if (!fixed_scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && st == SSM_OK)
+        st = SSM_ERR_LAUNCH;
     return st;
 }
 
@@ -1126,6 +1166,19 @@ int ssm_scan_fwd_bf16(const uint16_t* u, const uint16_t* delta, const float* A,
                         reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
                         reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
                         reinterpret_cast<bf*>(y), h_last, batch, L, dim, N, stream);
+}
+
+int ssm_scan_fwd_bf16_noalloc(const uint16_t* u, const uint16_t* delta, const float* A,
+                              const uint16_t* B, const uint16_t* C, const float* D,
+                              const uint16_t* z, const float* delta_bias, int softplus_flag,
+                              uint16_t* y, float* h_last, int64_t batch, int64_t L, int64_t dim,
+                              int64_t N, cudaStream_t stream) {
+    using bf = __nv_bfloat16;
+    return scan_fwd<bf>(reinterpret_cast<const bf*>(u), reinterpret_cast<const bf*>(delta), A,
+                        reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
+                        reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
+                        reinterpret_cast<bf*>(y), h_last, batch, L, dim, N, stream,
+                        /*fixed_scratch=*/true);
 }
 
 int ssm_scan_last_device_status(cudaStream_t stream) {
@@ -1155,6 +1208,8 @@ const char* ssm_status_string(int status) {
         case SSM_ERR_ALIAS: return "an output overlaps an input";
         case SSM_ERR_ARG: return "invalid knob key or value";
         case SSM_ERR_NOMEM: return "stream-ordered scratch allocation failed";
+        case SSM_ERR_SCRATCH:
+            return "segment summaries exceed the 8 MiB static buffer of the no-alloc entry point";
         default: return "unknown status";
     }
 }

@@ -32,6 +32,8 @@ SSM_ERR_TIMEOUT = 6
 SSM_ERR_ALIAS = 7
 SSM_ERR_ARG = 8
 SSM_ERR_NOMEM = 9
+SSM_ERR_SCRATCH = 10
+SSM_NOALLOC_SCRATCH_FLOATS = 2097152
 SSM_MAX_N = 128
 
 SSM_KNOB_WAIT_NS = 1
@@ -42,14 +44,14 @@ SSM_KNOB_PLAIN_LOADS = 5
 SSM_KNOB_STAGES = 6
 SSM_KNOB_SEGMENTS = 7
 
-EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_last_device_status",
-            "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
+EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc",
+            "ssm_scan_last_device_status", "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
 _FWD_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp,
              _i64, _i64, _i64, _i64, _vp]
-for _name in ("ssm_scan_fwd", "ssm_scan_fwd_bf16"):
+for _name in ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc"):
     getattr(_lib, _name).argtypes = _FWD_ARGS
     getattr(_lib, _name).restype = ctypes.c_int
 _lib.ssm_scan_last_device_status.argtypes = [_vp]
@@ -83,6 +85,16 @@ def ssm_scan_fwd_bf16(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, h_l
     return _lib.ssm_scan_fwd_bf16(u or None, delta or None, A or None, B or None, C or None,
                                   D or None, z or None, delta_bias or None, int(softplus_flag),
                                   y or None, h_last or None, batch, L, dim, N, stream or None)
+
+
+def ssm_scan_fwd_bf16_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, h_last,
+                              batch, L, dim, N, stream) -> int:
+    """bf16 entry point with segment scratch in the library's static device
+    buffer (no allocation); pointer arguments are ints (0 for NULL)."""
+    return _lib.ssm_scan_fwd_bf16_noalloc(u or None, delta or None, A or None, B or None,
+                                          C or None, D or None, z or None, delta_bias or None,
+                                          int(softplus_flag), y or None, h_last or None,
+                                          batch, L, dim, N, stream or None)
 
 
 def ssm_scan_last_device_status(stream=0) -> int:

@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for st in range(0, 9):
+    for st in range(0, 11):
         s = ssm.ssm_status_string(st)
         assert s and s != "unknown status"
     assert ssm.ssm_status_string(99) == "unknown status"
@@ -49,13 +49,15 @@ def fwd(fn, **kw):
     return fn(**args)
 
 
-@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16])
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16,
+                                ssm.ssm_scan_fwd_bf16_noalloc])
 def test_null_pointers(fn):
     for k in ("u", "delta", "A", "B", "C", "y"):
         assert fwd(fn, **{k: 0}) == ssmscan.SSM_ERR_NULL, k
 
 
-@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16])
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16,
+                                ssm.ssm_scan_fwd_bf16_noalloc])
 def test_bad_sizes(fn):
     assert fwd(fn, batch=-1) == ssmscan.SSM_ERR_SIZE
     assert fwd(fn, L=-3) == ssmscan.SSM_ERR_SIZE
@@ -72,7 +74,8 @@ def test_misaligned_pointers():
     assert fwd(ssm.ssm_scan_fwd_bf16, h_last=Q + 0x100002) == ssmscan.SSM_ERR_ALIGN
 
 
-@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16])
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16,
+                                ssm.ssm_scan_fwd_bf16_noalloc])
 def test_outputs_must_not_alias_inputs(fn):
     assert fwd(fn, y=P + 0x100000) == ssmscan.SSM_ERR_ALIAS            # y == delta
     assert fwd(fn, y=P + 0x10) == ssmscan.SSM_ERR_ALIAS                # y inside u
@@ -80,7 +83,8 @@ def test_outputs_must_not_alias_inputs(fn):
     assert fwd(fn, h_last=Q + 0x8) == ssmscan.SSM_ERR_ALIAS            # h_last inside y
 
 
-@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16])
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd, ssm.ssm_scan_fwd_bf16,
+                                ssm.ssm_scan_fwd_bf16_noalloc])
 def test_empty_problems_launch_nothing(fn):
     assert fwd(fn, batch=0) == ssmscan.SSM_OK
     assert fwd(fn, dim=0) == ssmscan.SSM_OK
