@@ -322,6 +322,9 @@ def run_ours(args, wl, world, rank, local):
         if st != 0:
             raise RuntimeError(ssm.ssm_status_string(st))
 
+    plan = ssm.ssm_scan_plan(wl.batch, wl.L, wl.dim, wl.N, 1 if bf else 0)
+    # a call runs one kernel, or two (segment summaries, then the main pass)
+    launches_per_call = 2 if plan["segments"] > 1 else 1
     working_set = 2 * (algorithmic_bytes(wl))
     l2_note = (f"inputs and outputs rotate over 2 resident copies "
                f"({working_set / 1e6:.0f} MB > 126 MB L2); no flush")
@@ -398,6 +401,7 @@ def run_ours(args, wl, world, rank, local):
     roof["mufu_ops_per_launch"] = mufu
     roof["fp32_ops_per_launch"] = fp32
     roof["kernel_ms"] = kern_ms
+    roof["launches_per_call"] = launches_per_call
 
     # ---- end to end through the C ABI: pinned host inputs -> device -> kernel
     #      -> y and h_last back to pinned host memory, every step
@@ -444,11 +448,11 @@ def run_ours(args, wl, world, rank, local):
         "pipe_peaks": peaks,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke,
-                "path": "pinned host -> cudaMemcpyAsync -> ssm_scan_fwd_bf16 (C ABI) -> "
+                "path": f"pinned host -> cudaMemcpyAsync -> {fn.__name__} (C ABI) -> "
                         "pinned host, one stream"},
-        "gpu_launches": K,
+        "gpu_launches": K * launches_per_call,
         "clocks": sampler.summary(),
-        "plan": ssm.ssm_scan_plan(wl.batch, wl.L, wl.dim, wl.N, 1 if bf else 0),
+        "plan": plan,
         "impl": "ours",
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
