@@ -180,17 +180,22 @@ SSM_API const char *ssm_status_string(int status);
 
 /*
  * Launch plan the library would use for a problem, without launching.
- * dtype: 0 = fp32, 1 = bf16.  On SSM_OK, plan[0..9] receives:
+ * dtype: 0 = fp32, 1 = bf16.  On SSM_OK, plan[0..10] receives:
  *   [0] state groups WS                [1] states per lane NPT
  *   [2] timesteps per chunk            [3] channels per block
  *   [4] threads per block              [5] blocks per time segment
  *   [6] dynamic shared bytes           [7] 1 if tiles move by TMA, else 0
  *   [8] time segments (1: one pass)    [9] scratch bytes taken per call
+ *   [10] kernel: 1 = phase kernel (every warp prepares, scans and finishes
+ *        each chunk in turn), 2 = warp-specialised kernel (a producer warp,
+ *        2 prepare warps, the scan warps and 2 finish warps work on
+ *        consecutive chunks at the same time; threads [4] include the 5
+ *        warps besides the scan warps)
  * Each channel's N states are split over WS warps (state groups), NPT states
  * per lane (N <= WS * NPT); a lane is a channel.
  */
 SSM_API int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype,
-                  int64_t plan[10]);
+                  int64_t plan[11]);
 
 /*
  * Process-wide knobs for tests and tuning sweeps (not for production use;
@@ -208,6 +213,8 @@ SSM_API int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int 
  *   SSM_KNOB_PLAIN_LOADS    1: move tiles with plain loads even when TMA applies
  *   SSM_KNOB_SEGMENTS       force the number of time segments (1 .. 64,
  *                           capped at the number of chunks); 0 = automatic
+ *   SSM_KNOB_KERNEL         1: the phase kernel; 2 (or 0, automatic): the
+ *                           warp-specialised kernel where tiles move by TMA
  * A forced combination the library is not built for falls back to automatic.
  * Returns SSM_OK or SSM_ERR_ARG.
  */
@@ -218,7 +225,8 @@ enum {
     SSM_KNOB_CHUNK = 4,
     SSM_KNOB_PLAIN_LOADS = 5,
     SSM_KNOB_STAGES = 6,
-    SSM_KNOB_SEGMENTS = 7
+    SSM_KNOB_SEGMENTS = 7,
+    SSM_KNOB_KERNEL = 8
 };
 SSM_API int ssm_set_knob(int key, int64_t value);
 

@@ -54,7 +54,7 @@
 
 namespace {
 
-constexpr int kMaxStages = 4;  // deepest TMA ring; chunks in flight per block = stages - 1
+constexpr int kMaxStages = 8;  // deepest TMA ring
 constexpr int kMaxSegments = 64;   // time segments of one call
 constexpr int kMinSegChunks = 8;   // shortest automatic segment, in chunks
 constexpr int kMinSegments = 8;    // fewest automatic segments once a split pays
@@ -374,77 +374,91 @@ struct Layout {
         off_part = off_gs + (SUM ? 0 : round1k(size_t(TC) * G::DT * 8));
         off_y = off_part + (SUM ? 0 : round1k(size_t(WS) * TC * G::DT * 4));
         off_bar = off_y + (SUM ? 0 : 2 * G::TILE);
-        total = off_bar + 64;
+        total = off_bar + 8 * (kMaxStages + 1);
     }
 };
 
-// The scan over one chunk for one lane: channel c (dd, part already offset to
-// it), states sg*NPT.. (Bs, Cs already offset).  Restrict-qualified so the
-// compiler may move later steps' loads above earlier steps' partial stores.
+// Steps per register block of the scan: a block's steps are unrolled with all
+// their loads free to issue early; more states per lane, shorter blocks.
+template <int NPT>
+__host__ __device__ constexpr int scan_block() { return NPT >= 16 ? 4 : (NPT >= 8 ? 8 : 16); }
+
+// One step of the state update for the NPT states of this lane: h <- e h + w,
+// e = 2^(dt a2), w = (dt u) B.  Returns the partial readout sum_j C_j h_j
+// (when WITH_C) or 0.
+template <int NPT, bool WITH_C>
+__device__ __forceinline__ float scan_step(float2 v, const float (&bb)[NPT], const float (&cc)[NPT],
+                                           const float (&a2)[NPT], float (&h)[NPT]) {
+    if constexpr (NPT == 1) {
+        const float e = ex2_approx(v.x * a2[0]);
+        h[0] = fmaf(e, h[0], v.y * bb[0]);
+        return WITH_C ? cc[0] * h[0] : 0.f;
+    } else {
+        const float2 vx = make_float2(v.x, v.x), vy = make_float2(v.y, v.y);
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < NPT; j += 2) {
+            const float2 x = __fmul2_rn(vx, make_float2(a2[j], a2[j + 1]));
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            const float2 w = __fmul2_rn(vy, make_float2(bb[j], bb[j + 1]));
+            const float2 hh = __ffma2_rn(e, make_float2(h[j], h[j + 1]), w);
+            h[j] = hh.x;
+            h[j + 1] = hh.y;
+            if constexpr (WITH_C) acc = __ffma2_rn(make_float2(cc[j], cc[j + 1]), hh, acc);
+        }
+        return WITH_C ? acc.x + acc.y : 0.f;
+    }
+}
+
 // Summary variant: the same state update without the readout; returns the
 // chunk's sum of dt for this channel (padded steps hold dt = 0).
 template <int NPT, int NP, int DT, int TC>
 __device__ __forceinline__ float scan_chunk_summary(const float2* __restrict__ dd,
                                                    const float* __restrict__ Bs,
                                                    const float (&a2)[NPT], float (&h)[NPT]) {
+    constexpr int SB = scan_block<NPT>() < TC ? scan_block<NPT>() : TC;
     float sdt = 0.f;
-#pragma unroll 8
-    for (int t = 0; t < TC; ++t) {
-        const float2 v = dd[t * DT];
-        float bb[NPT];
-        ld_states<NPT>(Bs + t * NP, bb);
-        sdt += v.x;
-        if constexpr (NPT == 1) {
-            h[0] = fmaf(ex2_approx(v.x * a2[0]), h[0], v.y * bb[0]);
-        } else {
-            const float2 vx = make_float2(v.x, v.x), vy = make_float2(v.y, v.y);
+#pragma unroll 1
+    for (int t0 = 0; t0 < TC; t0 += SB) {
 #pragma unroll
-            for (int j = 0; j < NPT; j += 2) {
-                const float2 x = __fmul2_rn(vx, make_float2(a2[j], a2[j + 1]));
-                const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                const float2 w = __fmul2_rn(vy, make_float2(bb[j], bb[j + 1]));
-                const float2 hh = __ffma2_rn(e, make_float2(h[j], h[j + 1]), w);
-                h[j] = hh.x;
-                h[j + 1] = hh.y;
-            }
+        for (int i = 0; i < SB; ++i) {
+            const int t = t0 + i;
+            const float2 v = dd[t * DT];
+            float bb[NPT];
+            ld_states<NPT>(Bs + t * NP, bb);
+            sdt += v.x;
+            scan_step<NPT, false>(v, bb, bb, a2, h);
         }
     }
     return sdt;
 }
 
+// The scan over one chunk for one lane: channel c (dd, part already offset to
+// it), states sg*NPT.. (Bs, Cs already offset).  A block's partial readouts
+// stay in registers until its steps are done: a shared store between steps
+// would keep the compiler from issuing later steps' loads ahead of it and
+// serialise the steps.
 template <int NPT, int NP, int DT, int TC>
 __device__ __forceinline__ void scan_chunk(const float2* __restrict__ dd,
                                            const float* __restrict__ Bs,
                                            const float* __restrict__ Cs,
                                            float* __restrict__ part, const float (&a2)[NPT],
                                            float (&h)[NPT]) {
-#pragma unroll 8
-    for (int t = 0; t < TC; ++t) {
-        const float2 v = dd[t * DT];
-        float bb[NPT], cc[NPT];
-        ld_states<NPT>(Bs + t * NP, bb);
-        ld_states<NPT>(Cs + t * NP, cc);
-        float p;
-        if constexpr (NPT == 1) {
-            const float e = ex2_approx(v.x * a2[0]);
-            h[0] = fmaf(e, h[0], v.y * bb[0]);
-            p = cc[0] * h[0];
-        } else {
-            const float2 vx = make_float2(v.x, v.x), vy = make_float2(v.y, v.y);
-            float2 acc = make_float2(0.f, 0.f);
+    constexpr int SB = scan_block<NPT>() < TC ? scan_block<NPT>() : TC;
+    static_assert(TC % SB == 0, "register blocks");
+#pragma unroll 1
+    for (int t0 = 0; t0 < TC; t0 += SB) {
+        float pv[SB];
 #pragma unroll
-            for (int j = 0; j < NPT; j += 2) {
-                const float2 x = __fmul2_rn(vx, make_float2(a2[j], a2[j + 1]));
-                const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-                const float2 w = __fmul2_rn(vy, make_float2(bb[j], bb[j + 1]));
-                const float2 hh = __ffma2_rn(e, make_float2(h[j], h[j + 1]), w);
-                h[j] = hh.x;
-                h[j + 1] = hh.y;
-                acc = __ffma2_rn(make_float2(cc[j], cc[j + 1]), hh, acc);
-            }
-            p = acc.x + acc.y;
+        for (int i = 0; i < SB; ++i) {
+            const int t = t0 + i;
+            float bb[NPT], cc[NPT];
+            ld_states<NPT>(Bs + t * NP, bb);
+            ld_states<NPT>(Cs + t * NP, cc);
+            pv[i] = scan_step<NPT, true>(dd[t * DT], bb, cc, a2, h);
         }
-        part[t * DT] = p;
+#pragma unroll
+        for (int i = 0; i < SB; ++i) part[(t0 + i) * DT] = pv[i];
     }
 }
 
@@ -770,6 +784,455 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
     }
 }
 
+// ============================================================ warp-specialised
+// The same computation with the work of a chunk split by role instead of by
+// phase, as a pipeline of warps that hand buffers over through mbarriers:
+//   producer (1 warp)   TMA loads of chunk k into ring stage k % stages, once
+//                       the prepare warps released that stage (EMPTY)
+//   prepare  (2 warps)  dt, dt*u and widened B, C of chunk k into buffer
+//                       k & 1 (FULL), once chunk k-2 is finished (PEMPTY)
+//   scan     (NSW)      the recurrence of chunk k (lane = channel, warp =
+//                       channel tile x state group), partials into s_part
+//                       buffer k & 1 (DONE)
+//   finish   (2 warps)  y of chunk k from the partials and the chunk's u, z
+//                       in the ring (gate and skip), into an output tile
+//                       stored by TMA; then buffer k & 1 is free (PEMPTY)
+// A ring stage is refilled once the prepare and the finish warps are done
+// with it (EMPTY).
+// Every stage may run up to two chunks ahead of the next.  Each wait is
+// bounded and also gives up once another warp has raised the block's abort
+// flag; the only named barriers are among the finish warps, which all run
+// the same trip count and vote on aborting.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity,
+                                                   uint64_t limit_ns, const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t start = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_ns() - start > limit_ns) return false;
+    }
+}
+
+// Barrier `id` over `n` threads of the block.
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Barrier `id` over `n` threads that also returns the OR of `v` over them.
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(uint32_t(v)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+template <typename T, int NPT, int WS, int TC>
+struct GeoW {
+    static constexpr int ES = int(sizeof(T));
+    static constexpr int WC = WS >= 4 ? 1 : 4 / WS;  // channel tiles per block
+    static constexpr int NSW = WC * WS;              // scan warps
+    static constexpr int NPW = 2, NQW = 2;           // prepare warps, finish warps
+    static constexpr int NS = NSW * 32, NPR = NPW * 32, NQ = NQW * 32;
+    static constexpr int NT = NS + NPR + NQ + 32;    // + the producer warp
+    static constexpr int DT = WC * 32;               // channels per block
+    static constexpr int NP = NPT * WS;              // padded states per channel
+    static constexpr int WB = DT * ES;               // tile row bytes
+    static constexpr int NPAIR = DT / 2;             // channel pairs
+    static constexpr int ITEMS_P = TC * NPAIR / NPR; // (step, pair) items per prepare thread
+    static constexpr int ITEMS_Q = TC * NPAIR / NQ;  // ... per finish thread
+    using TileT = Tile<WB>;
+    static constexpr size_t TILE = round1k(size_t(TC) * WB);
+    static_assert(NPR % NPAIR == 0 && NQ % NPAIR == 0 && (TC * NPAIR) % NPR == 0 &&
+                      (TC * NPAIR) % NQ == 0,
+                  "item mapping");
+    static_assert(WB % 16 == 0 && (WB <= 128 || WB % 128 == 0), "tile rows");
+};
+
+// Shared memory of one warp-specialised block (bytes from a 1024-byte aligned base).
+//   raw ring  stages x { u, delta, z : tile ; B, C : [TC][N] T }   (summary: u, delta, B)
+//   s_B, s_C  2 x [TC][NP] fp32        (summary: no s_C)
+//   s_dd      2 x [TC][DT] float2      (dt, dt*u)
+//   s_part    2 x [WS][TC][DT] fp32                        (summary: none)
+//   s_y       2 x tile                                     (summary: none)
+//   barriers  TMA[kMaxStages], EMPTY[kMaxStages], FULL[2], DONE[2], PEMPTY[2],
+//             and one that nothing completes
+template <typename T, int NPT, int WS, int TC, bool SUM>
+struct LayoutW {
+    using G = GeoW<T, NPT, WS, TC>;
+    size_t tile_bc, stage, bc, dd, part, off_raw, off_bf, off_cf, off_dd, off_part, off_y,
+        off_bar, total;
+    __host__ __device__ LayoutW(int64_t N, int stages) {
+        tile_bc = round1k(size_t(TC) * size_t(N) * G::ES);
+        stage = (SUM ? 2 : 3) * G::TILE + (SUM ? 1 : 2) * tile_bc;
+        bc = round1k(size_t(TC) * G::NP * 4);
+        dd = round1k(size_t(TC) * G::DT * 8);
+        part = round1k(size_t(WS) * TC * G::DT * 4);
+        off_raw = 0;
+        off_bf = off_raw + size_t(stages) * stage;
+        off_cf = off_bf + 2 * bc;
+        off_dd = off_cf + (SUM ? 0 : 2 * bc);
+        off_part = off_dd + 2 * dd;
+        off_y = off_part + (SUM ? 0 : 2 * part);
+        off_bar = off_y + (SUM ? 0 : 2 * G::TILE);
+        total = off_bar + 256;
+    }
+};
+
+template <typename T, int NPT, int WS, int TC, bool SUMMARY>
+__global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
+    ssm_scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u,
+                       const __grid_constant__ CUtensorMap tm_dt,
+                       const __grid_constant__ CUtensorMap tm_z,
+                       const __grid_constant__ CUtensorMap tm_B,
+                       const __grid_constant__ CUtensorMap tm_C,
+                       const __grid_constant__ CUtensorMap tm_y, const KParams p) {
+    using E = Elt<T>;
+    using G = GeoW<T, NPT, WS, TC>;
+    using TT = typename G::TileT;
+    constexpr int DT = G::DT, NP = G::NP, ES = G::ES;
+    constexpr int RS = TT::RS, NB = TT::NB, NPAIR = G::NPAIR;
+    constexpr bool summary = SUMMARY;
+    constexpr int kBarFinishA = 1, kBarFinishB = 2;  // named barriers (finish warps only)
+
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ int s_abort;
+    volatile int* const abort_flag = &s_abort;
+    unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const LayoutW<T, NPT, WS, TC, SUMMARY> lay(p.N, p.stages);
+    const int nst = p.stages;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t N = p.N, L = p.L, dim = p.dim;
+    const int64_t rowblk = blockIdx.x / p.nblk_d;
+    const int64_t b = rowblk % p.batch;
+    const int64_t seg = rowblk / p.batch;
+    const int64_t d0 = (blockIdx.x % p.nblk_d) * DT;
+
+    unsigned char* const raw0 = base + lay.off_raw;
+    const uint32_t stage_b = uint32_t(lay.stage), tbc = uint32_t(lay.tile_bc);
+    constexpr uint32_t TILE = uint32_t(G::TILE);
+    constexpr uint32_t NTILE = SUMMARY ? 2 : 3;
+    auto raw_u = [=](int s) { return raw0 + s * stage_b; };
+    auto raw_dt = [=](int s) { return raw0 + s * stage_b + TILE; };
+    auto raw_z = [=](int s) { return raw0 + s * stage_b + 2 * TILE; };
+    auto raw_B = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + NTILE * TILE); };
+    auto raw_C = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + NTILE * TILE + tbc); };
+    const uint32_t bcb = uint32_t(lay.bc), ddb = uint32_t(lay.dd), ptb = uint32_t(lay.part);
+    auto s_B = [=](int k) { return reinterpret_cast<float*>(base + lay.off_bf + k * bcb); };
+    auto s_C = [=](int k) { return reinterpret_cast<float*>(base + lay.off_cf + k * bcb); };
+    auto s_dd = [=](int k) { return reinterpret_cast<float2*>(base + lay.off_dd + k * ddb); };
+    auto s_part = [=](int k) { return reinterpret_cast<float*>(base + lay.off_part + k * ptb); };
+    unsigned char* const s_y0 = base + lay.off_y;
+    const uint32_t bar0 = smem_u32(base + lay.off_bar);
+    auto bar_tma = [=](int s) { return bar0 + 8 * s; };
+    auto bar_empty = [=](int s) { return bar0 + 8 * (kMaxStages + s); };
+    auto bar_full = [=](int k) { return bar0 + 8 * (2 * kMaxStages + k); };
+    auto bar_done = [=](int k) { return bar0 + 8 * (2 * kMaxStages + 2 + k); };
+    auto bar_pempty = [=](int k) { return bar0 + 8 * (2 * kMaxStages + 4 + k); };
+    const uint32_t bar_never = bar0 + 8 * (2 * kMaxStages + 6);
+
+    const bool has_z = p.z != nullptr && !summary;
+    const int64_t nchunks = (L + TC - 1) / TC;
+    const int64_t c_begin = seg * p.seg_chunks;
+    const int64_t nloc = (nchunks - c_begin < p.seg_chunks) ? nchunks - c_begin : p.seg_chunks;
+
+    if (tid == 0) {
+        s_abort = 0;
+        for (int s = 0; s < kMaxStages; ++s) {
+            mbar_init(bar_tma(s), 1);
+            mbar_init(bar_empty(s), G::NPW + G::NQW);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(bar_full(k), G::NPW);
+            mbar_init(bar_done(k), G::NSW);
+            mbar_init(bar_pempty(k), G::NQW);
+        }
+        mbar_init(bar_never, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();  // the last block-wide barrier: the roles part here
+
+    auto give_up = [&]() {
+        if (!*abort_flag) atomicOr(&g_ssm_status, kDevTimeout);
+        *abort_flag = 1;
+    };
+
+    if (warp < G::NSW) {
+        // ================================================================ SCAN
+        // lane = channel c of channel tile ct; states sg*NPT + j
+        const int ct = warp / WS, sg = warp % WS;
+        const int c = ct * 32 + lane;
+        const int64_t d_scan = d0 + c;
+        const bool scan_ok = d_scan < dim;
+        float a2[NPT], h[NPT];
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) {
+            const int64_t n = int64_t(sg) * NPT + j;
+            a2[j] = (scan_ok && n < N) ? p.A[d_scan * N + n] * kLog2e : 0.f;
+            h[j] = (p.h0 != nullptr && !summary && scan_ok && n < N)
+                       ? p.h0[(b * dim + d_scan) * N + n]
+                       : 0.f;
+        }
+        if (!summary && scan_ok) {
+            for (int64_t q = 0; q < seg; ++q) {
+                const int64_t r = (q * p.batch + b) * dim + d_scan;
+                const float sdt = p.sseg[r];
+#pragma unroll
+                for (int j = 0; j < NPT; ++j) {
+                    const int64_t n = int64_t(sg) * NPT + j;
+                    if (n < N) h[j] = fmaf(ex2_approx(a2[j] * sdt), h[j], p.hseg[r * N + n]);
+                }
+            }
+        }
+        double sdt_seg = 0.0;
+        (void)sdt_seg;
+        for (int64_t k = 0; k < nloc; ++k) {
+            const int bf = int(k & 1);
+            if (!mbar_wait_or_abort(bar_full(bf), uint32_t(k >> 1) & 1u, p.wait_ns, abort_flag)) {
+                give_up();
+                return;
+            }
+            if constexpr (summary) {
+                sdt_seg += double(scan_chunk_summary<NPT, NP, DT, TC>(s_dd(bf) + c,
+                                                                      s_B(bf) + sg * NPT, a2, h));
+            } else {
+                scan_chunk<NPT, NP, DT, TC>(s_dd(bf) + c, s_B(bf) + sg * NPT, s_C(bf) + sg * NPT,
+                                            s_part(bf) + sg * TC * DT + c, a2, h);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_done(bf));
+        }
+        if constexpr (summary) {
+            if (scan_ok) {
+                const int64_t r = (seg * p.batch + b) * dim + d_scan;
+#pragma unroll
+                for (int j = 0; j < NPT; ++j) {
+                    const int64_t n = int64_t(sg) * NPT + j;
+                    if (n < N) p.hseg[r * N + n] = h[j];
+                }
+                if (sg == 0) p.sseg[r] = float(sdt_seg);
+            }
+        } else if (p.h_last != nullptr && scan_ok && seg == p.n_seg - 1) {
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) {
+                const int64_t n = int64_t(sg) * NPT + j;
+                if (n < N) p.h_last[(b * dim + d_scan) * N + n] = h[j];
+            }
+        }
+        return;
+    }
+
+    if (warp == G::NSW + G::NPW + G::NQW) {
+        // ============================================================ PRODUCER
+        if (lane != 0) return;
+        const uint32_t tx_bytes = uint32_t((has_z ? 3 : 2) * TC * G::WB) +
+                                  (p.tma_bc ? uint32_t((summary ? 1 : 2) * TC * N * ES) : 0u);
+        int s = 0;
+        uint32_t use = 0;  // how often stage s was filled before
+        int64_t issued = 0;
+        for (; issued < nloc; ++issued) {
+            if (use > 0 && !mbar_wait_or_abort(bar_empty(s), (use - 1) & 1u, p.wait_ns, abort_flag)) {
+                give_up();
+                break;
+            }
+            const uint32_t bar = bar_tma(s);
+            const int t0 = int((c_begin + issued) * TC);
+            mbar_arrive_expect_tx(bar, tx_bytes);
+#pragma unroll
+            for (int cb = 0; cb < NB; ++cb) {
+                const int x = int(d0) + cb * (RS / ES);
+                const uint32_t o = uint32_t(cb * TC * RS);
+                tma_load_3d(smem_u32(raw_u(s) + o), &tm_u, x, t0, int(b), bar);
+                tma_load_3d(smem_u32(raw_dt(s) + o), &tm_dt, x, t0, int(b), bar);
+                if (has_z) tma_load_3d(smem_u32(raw_z(s) + o), &tm_z, x, t0, int(b), bar);
+            }
+            if (p.tma_bc) {
+                tma_load_3d(smem_u32(raw_B(s)), &tm_B, 0, t0, int(b), bar);
+                if (!summary) tma_load_3d(smem_u32(raw_C(s)), &tm_C, 0, t0, int(b), bar);
+            }
+            if (++s == nst) { s = 0; ++use; }
+        }
+        // Before leaving, wait (bounded) for the last load issued into every
+        // stage: it completed already, or it is this block's copy in flight.
+        bool ok = true;
+        for (int64_t cc = issued > nst ? issued - nst : 0; cc < issued; ++cc)
+            ok = mbar_wait_bounded(bar_tma(int(cc % nst)), uint32_t(cc / nst) & 1u, p.wait_ns) && ok;
+        if (!ok) atomicOr(&g_ssm_status, kDevDrainTimeout);
+        return;
+    }
+
+    if (warp < G::NSW + G::NPW) {
+        // ============================================================= PREPARE
+        constexpr int NPR = G::NPR, ITEMS = G::ITEMS_P, TSTEP = NPR / NPAIR;
+        const int pt = tid - G::NS;  // 0 .. NPR-1
+        const int pp = pt % NPAIR, tq0 = pt / NPAIR;
+        float bias2[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int64_t d = d0 + 2 * pp + k;
+            bias2[k] = (p.bias != nullptr && d < dim) ? p.bias[d] : 0.f;
+        }
+        const float2 b2 = make_float2(bias2[0], bias2[1]);
+        const T* gB = static_cast<const T*>(p.B);
+        const T* gC = static_cast<const T*>(p.C);
+        const bool bc_vec = p.tma_bc && N == NP && (N % 4) == 0;
+        int s = 0;
+        uint32_t ph = 0;
+        for (int64_t k = 0; k < nloc; ++k) {
+            const int bf = int(k & 1);
+            const int64_t t0 = (c_begin + k) * TC;
+            const int tv = int(L - t0 < TC ? L - t0 : int64_t(TC));
+            bool ok = true;
+            if (p.force_timeout && k == 0) ok = mbar_wait_bounded(bar_never, 0, p.wait_ns);
+            if (ok) ok = mbar_wait_or_abort(bar_tma(s), ph, p.wait_ns, abort_flag);
+            // buffer bf is free once chunk k-2 is finished
+            if (ok && k >= 2)
+                ok = mbar_wait_or_abort(bar_pempty(bf), uint32_t((k >> 1) - 1) & 1u, p.wait_ns,
+                                        abort_flag);
+            if (!ok) {
+                give_up();
+                return;
+            }
+            float* const sB = s_B(bf);
+            float* const sC = s_C(bf);
+            if (bc_vec) {
+                const int items = TC * NP / 4;
+                for (int i = pt; i < (summary ? 1 : 2) * items; i += NPR) {
+                    const bool isC = i >= items;
+                    const int j = (isC ? i - items : i) * 4;
+                    const float4 qv = ld_quad<T>((isC ? raw_C(s) : raw_B(s)) + j);
+                    *reinterpret_cast<float4*>((isC ? sC : sB) + j) = qv;
+                }
+            } else {
+                for (int i = pt; i < TC * NP; i += NPR) {
+                    const int t = i / NP, n = i % NP;
+                    float bv = 0.f, cv = 0.f;
+                    if (n < N && t < tv) {
+                        if (p.tma_bc) {
+                            bv = E::to_f(raw_B(s)[t * N + n]);
+                            if (!summary) cv = E::to_f(raw_C(s)[t * N + n]);
+                        } else {
+                            const int64_t off = (b * L + t0 + t) * N + n;
+                            bv = E::to_f(gB[off]);
+                            if (!summary) cv = E::to_f(gC[off]);
+                        }
+                    }
+                    sB[i] = bv;
+                    if constexpr (!summary) sC[i] = cv;
+                }
+            }
+            const unsigned char* ru = raw_u(s);
+            const unsigned char* rdt = raw_dt(s);
+            float2* const sdd = s_dd(bf);
+#pragma unroll
+            for (int it = 0; it < ITEMS; ++it) {
+                const int t = tq0 + it * TSTEP;
+                const uint32_t o = TT::off(t, 2 * pp * ES, TC);
+                float xr[2], uu[2];
+                ld_k<T, 2>(rdt + o, xr);
+                ld_k<T, 2>(ru + o, uu);
+                float2 x = __fadd2_rn(make_float2(xr[0], xr[1]), b2);
+                if (p.softplus) x = Act<T>::softplus2(x);
+                const float2 xu = __fmul2_rn(x, make_float2(uu[0], uu[1]));
+                *reinterpret_cast<float4*>(sdd + t * DT + 2 * pp) =
+                    t < tv ? make_float4(x.x, xu.x, x.y, xu.y) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar_full(bf));
+                mbar_arrive(bar_empty(s));  // this warp is done with ring stage s
+            }
+            if (++s == nst) { s = 0; ph ^= 1u; }
+        }
+        return;
+    }
+
+    // ================================================================= FINISH
+    constexpr int NQ = G::NQ, ITEMS = G::ITEMS_Q, TSTEP = NQ / NPAIR;
+    const int qt = tid - G::NS - G::NPR;  // 0 .. NQ-1
+    const bool leader = qt == 0;
+    const int pp = qt % NPAIR, tq0 = qt / NPAIR;
+    float dsk2[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int64_t d = d0 + 2 * pp + k;
+        dsk2[k] = (p.D != nullptr && d < dim) ? p.D[d] : 0.f;
+    }
+    const float2 d2 = make_float2(dsk2[0], dsk2[1]);
+    bool failed = false;
+    int s = 0;  // ring stage of chunk k, and its TMA phase
+    uint32_t ph = 0;
+    for (int64_t k = 0; k < nloc; ++k) {
+        const int bf = int(k & 1);
+        if (!mbar_wait_or_abort(bar_done(bf), uint32_t(k >> 1) & 1u, p.wait_ns, abort_flag))
+            failed = true;
+        // the chunk's u and z (complete: the prepare warps waited for them, and
+        // the stage is not refilled before this warp releases it)
+        if (!summary && !failed && !mbar_wait_or_abort(bar_tma(s), ph, p.wait_ns, abort_flag))
+            failed = true;
+        if (!summary && leader) bulk_wait_read_le1();  // output tile bf is free again
+        if (named_sync_or(kBarFinishA, NQ, failed || *abort_flag)) break;
+        if constexpr (!summary) {
+            // y = (sum of the state groups' partials) g + D u g, g = silu(z) or 1
+            const int64_t t0 = (c_begin + k) * TC;
+            unsigned char* yt = s_y0 + bf * TILE;
+            const float* part = s_part(bf);
+            const unsigned char* ru = raw_u(s);
+            const unsigned char* rz = raw_z(s);
+#pragma unroll
+            for (int it = 0; it < ITEMS; ++it) {
+                const int t = tq0 + it * TSTEP;
+                const uint32_t o = TT::off(t, 2 * pp * ES, TC);
+                float2 acc = *reinterpret_cast<const float2*>(part + t * DT + 2 * pp);
+#pragma unroll
+                for (int sgi = 1; sgi < WS; ++sgi)
+                    acc = __fadd2_rn(acc, *reinterpret_cast<const float2*>(part + (sgi * TC + t) * DT + 2 * pp));
+                float uu[2];
+                ld_k<T, 2>(ru + o, uu);
+                float2 g = make_float2(1.f, 1.f);
+                if (has_z) {
+                    float zz[2];
+                    ld_k<T, 2>(rz + o, zz);
+                    g = Act<T>::silu2(make_float2(zz[0], zz[1]));
+                }
+                const float2 su = __fmul2_rn(__fmul2_rn(d2, make_float2(uu[0], uu[1])), g);
+                const float yv[2] = {fmaf(acc.x, g.x, su.x), fmaf(acc.y, g.y, su.y)};
+                st_k<T, 2>(yt + o, yv);
+            }
+            fence_proxy_async_smem();
+            named_sync(kBarFinishB, NQ);
+            if (leader) {
+#pragma unroll
+                for (int cb = 0; cb < NB; ++cb)
+                    tma_store_3d(&tm_y, int(d0) + cb * (RS / ES), int(t0), int(b),
+                                 smem_u32(yt + cb * TC * RS));
+                bulk_commit();
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(bar_pempty(bf));  // buffers bf may take chunk k + 2
+            mbar_arrive(bar_empty(s));    // this warp is done with ring stage s
+        }
+        if (++s == nst) { s = 0; ph ^= 1u; }
+    }
+    // A failure in the last iteration has not been voted on yet.
+    if (named_sync_or(kBarFinishA, NQ, failed) && leader) give_up();
+    if (leader) bulk_wait_all();
+}
+
 // ------------------------------------------------------------------ host side
 std::atomic<int64_t> g_wait_ns{2000000000LL};
 std::atomic<int> g_force_timeout{0};
@@ -777,6 +1240,7 @@ std::atomic<int> g_force_groups{0};
 std::atomic<int> g_force_stages{0};
 std::atomic<int> g_force_chunk{0};
 std::atomic<int> g_force_segments{0};
+std::atomic<int> g_force_kernel{0};
 std::atomic<int> g_plain_loads{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -817,6 +1281,7 @@ struct Plan {
     size_t smem = 0;
     int row_span = 16;
     bool tma_udz = false, tma_bc = false;
+    bool ws = false;        // warp-specialised kernel (needs the TMA path)
 };
 
 int supported_npt(int64_t need) {
@@ -848,6 +1313,12 @@ size_t smem_bytes(int64_t N, int stages, int TC) {
     return Layout<T, NPT, WS, 32, SUM>(N, stages).total + 1024;
 }
 
+template <typename T, int NPT, int WS, bool SUM = false>
+size_t smem_bytes_w(int64_t N, int stages, int TC) {
+    if (TC == 16) return LayoutW<T, NPT, WS, 16, SUM>(N, stages).total + 1024;
+    return LayoutW<T, NPT, WS, 32, SUM>(N, stages).total + 1024;
+}
+
 #define SSM_FOR_EACH_VARIANT(X)                            \
     X(1, 1) X(2, 1) X(4, 1) X(8, 1) X(16, 1)               \
     X(1, 2) X(2, 2) X(4, 2) X(8, 2) X(16, 2)               \
@@ -872,8 +1343,21 @@ size_t variant_smem(int npt, int ws, int64_t N, int stages, int TC) {
 }
 
 template <typename T>
+size_t variant_smem_w(int npt, int ws, int64_t N, int stages, int TC) {
+#define SSM_SMEM_W(NPT_, WS_) \
+    if (npt == NPT_ && ws == WS_) return smem_bytes_w<T, NPT_, WS_>(N, stages, TC);
+    SSM_FOR_EACH_VARIANT(SSM_SMEM_W)
+#undef SSM_SMEM_W
+    return 0;
+}
+
+// Shared memory per warp-specialised block that still lets three blocks share an SM.
+constexpr size_t kWsSmemTarget = 60 * 1024;
+
+template <typename T>
 Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, const void* dt,
-               const void* z, const void* y, const void* Bp, const void* Cp) {
+               const void* z, const void* y, const void* Bp, const void* Cp,
+               bool allow_tma = true) {
     const size_t es = sizeof(T);
     Plan pl;
     const int64_t channels = batch * dim;
@@ -901,23 +1385,52 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
     pl.NT = wc * pl.WS * 32;
     const int64_t nblk = (dim + pl.DT - 1) / pl.DT;
     pl.grid = nblk * batch;
-    // Chunk length: 32 steps unless the grid does not fit in one wave of blocks
-    // at that footprint (then 16 steps: half the shared memory per block).
-    auto resident = [&](int tc) {
-        const size_t sm = variant_smem<T>(pl.NPT, pl.WS, N, 2, tc);
-        const int64_t by_smem = int64_t((228 * 1024) / (sm + 1024));
-        const int64_t by_threads = 2048 / pl.NT;
-        return std::min(by_smem, by_threads) * 148;
-    };
-    pl.TC = (variant_smem<T>(pl.NPT, pl.WS, N, 2, 32) <= kMaxSmem && pl.grid <= resident(32)) ? 32 : 16;
+    const int wb = pl.DT * int(es);
+    pl.row_span = wb < 128 ? wb : 128;
+    const bool plain = g_plain_loads.load() != 0 || !allow_tma;
+    pl.tma_udz = !plain && L > 0 && get_encode() != nullptr && (dim * int64_t(es)) % 16 == 0 &&
+                 aligned(u, 16) && aligned(dt, 16) && aligned(y, 16) &&
+                 (z == nullptr || aligned(z, 16)) && L < (int64_t(1) << 31) &&
+                 dim < (int64_t(1) << 31) && batch < (int64_t(1) << 31);
+    pl.tma_bc = pl.tma_udz && (N * int64_t(es)) % 16 == 0 && N <= 256 && aligned(Bp, 16) &&
+                aligned(Cp, 16);
     const int ft = g_force_chunk.load();
-    if (ft == 16 || (ft == 32 && variant_smem<T>(pl.NPT, pl.WS, N, 2, 32) <= kMaxSmem)) pl.TC = ft;
-    // A third ring stage keeps two chunks in flight where it costs little
-    // shared memory; wide tiles keep two stages.
-    pl.stages = variant_smem<T>(pl.NPT, pl.WS, N, 3, pl.TC) <= 100 * 1024 ? 3 : 2;
     const int fs = g_force_stages.load();
-    if (fs != 0 && variant_smem<T>(pl.NPT, pl.WS, N, fs, pl.TC) <= kMaxSmem) pl.stages = fs;
-    pl.smem = variant_smem<T>(pl.NPT, pl.WS, N, pl.stages, pl.TC);
+    // The warp-specialised kernel wherever its tiles can move by TMA.
+    pl.ws = pl.tma_udz && g_force_kernel.load() != 1 &&
+            variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 16) <= kMaxSmem;
+    if (pl.ws) {
+        pl.NT = (wc * pl.WS + 5) * 32;  // + 2 prepare, 2 finish and 1 producer warp
+        pl.TC = (ft == 32 && variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 32) <= kMaxSmem) ? 32 : 16;
+        // The deepest ring (chunks in flight) within the footprint target.
+        pl.stages = 2;
+        for (int st : {6, 5, 4, 3})
+            if (variant_smem_w<T>(pl.NPT, pl.WS, N, st, pl.TC) <= kWsSmemTarget) {
+                pl.stages = st;
+                break;
+            }
+        if (fs != 0 && variant_smem_w<T>(pl.NPT, pl.WS, N, fs, pl.TC) <= kMaxSmem) pl.stages = fs;
+        pl.smem = variant_smem_w<T>(pl.NPT, pl.WS, N, pl.stages, pl.TC);
+    } else {
+        // Chunk length: 32 steps unless the grid does not fit in one wave of
+        // blocks at that footprint (then 16 steps: half the shared memory).
+        auto resident = [&](int tc) {
+            const size_t sm = variant_smem<T>(pl.NPT, pl.WS, N, 2, tc);
+            const int64_t by_smem = int64_t((228 * 1024) / (sm + 1024));
+            const int64_t by_threads = 2048 / pl.NT;
+            return std::min(by_smem, by_threads) * 148;
+        };
+        pl.TC = (variant_smem<T>(pl.NPT, pl.WS, N, 2, 32) <= kMaxSmem && pl.grid <= resident(32))
+                    ? 32
+                    : 16;
+        if (ft == 16 || (ft == 32 && variant_smem<T>(pl.NPT, pl.WS, N, 2, 32) <= kMaxSmem))
+            pl.TC = ft;
+        // A third ring stage keeps two chunks in flight where it costs little
+        // shared memory; wide tiles keep two stages.
+        pl.stages = variant_smem<T>(pl.NPT, pl.WS, N, 3, pl.TC) <= 100 * 1024 ? 3 : 2;
+        if (fs != 0 && variant_smem<T>(pl.NPT, pl.WS, N, fs, pl.TC) <= kMaxSmem) pl.stages = fs;
+        pl.smem = variant_smem<T>(pl.NPT, pl.WS, N, pl.stages, pl.TC);
+    }
     // Time split: when the (batch, channel) blocks fill less than half of one
     // wave, cut the sequence into segments: as many as fill one wave, and at
     // least kMinSegments (the summary pass then has enough blocks too and the
@@ -938,15 +1451,6 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
         pl.n_seg = ns > 1 ? int((nchunks + pl.seg_chunks - 1) / pl.seg_chunks) : 1;
         if (pl.seg_chunks < 1) pl.seg_chunks = 1;
     }
-    const int wb = pl.DT * int(es);
-    pl.row_span = wb < 128 ? wb : 128;
-    const bool plain = g_plain_loads.load() != 0;
-    pl.tma_udz = !plain && L > 0 && get_encode() != nullptr && (dim * int64_t(es)) % 16 == 0 &&
-                 aligned(u, 16) && aligned(dt, 16) && aligned(y, 16) &&
-                 (z == nullptr || aligned(z, 16)) && L < (int64_t(1) << 31) &&
-                 dim < (int64_t(1) << 31) && batch < (int64_t(1) << 31);
-    pl.tma_bc = pl.tma_udz && (N * int64_t(es)) % 16 == 0 && N <= 256 && aligned(Bp, 16) &&
-                aligned(Cp, 16);
     return pl;
 }
 
@@ -961,8 +1465,38 @@ int launch_one(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStre
     if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_LAUNCH;
     std::atomic<size_t>& cfg = configured[dev & 63];
     if (cfg.load() < smem) {
+        // Opt in to this block's dynamic shared memory and ask for the
+        // largest shared-memory carveout, so that as many blocks as the
+        // footprint allows can share an SM.
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-            cudaSuccess)
+                cudaSuccess ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 int(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+            return SSM_ERR_LAUNCH;
+        cfg.store(smem);
+    }
+    kern<<<dim3(unsigned(grid)), dim3(G::NT), smem, stream>>>(tms[0], tms[1], tms[2], tms[3],
+                                                               tms[4], tms[5], kp);
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+template <typename T, int NPT, int WS, int TC, bool SUMMARY>
+int launch_one_w(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
+    using G = GeoW<T, NPT, WS, TC>;
+    auto kern = ssm_scan_ws_kernel<T, NPT, WS, TC, SUMMARY>;
+    const size_t smem = smem_bytes_w<T, NPT, WS, SUMMARY>(kp.N, kp.stages, TC);
+    static std::atomic<size_t> configured[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_LAUNCH;
+    std::atomic<size_t>& cfg = configured[dev & 63];
+    if (cfg.load() < smem) {
+        // Opt in to this block's dynamic shared memory and ask for the
+        // largest shared-memory carveout, so that as many blocks as the
+        // footprint allows can share an SM.
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 int(cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
             return SSM_ERR_LAUNCH;
         cfg.store(smem);
     }
@@ -974,6 +1508,19 @@ int launch_one(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStre
 template <typename T>
 int dispatch(const Plan& pl, int64_t grid, const CUtensorMap* tms, const KParams& kp,
              cudaStream_t stream) {
+    if (pl.ws) {
+#define SSM_CASE_W(NPT_, WS_)                                                                  \
+    if (pl.NPT == NPT_ && pl.WS == WS_) {                                                      \
+        if (kp.summary)                                                                        \
+            return pl.TC == 16 ? launch_one_w<T, NPT_, WS_, 16, true>(grid, tms, kp, stream)  \
+                               : launch_one_w<T, NPT_, WS_, 32, true>(grid, tms, kp, stream); \
+        return pl.TC == 16 ? launch_one_w<T, NPT_, WS_, 16, false>(grid, tms, kp, stream)     \
+                           : launch_one_w<T, NPT_, WS_, 32, false>(grid, tms, kp, stream);    \
+    }
+        SSM_FOR_EACH_VARIANT(SSM_CASE_W)
+#undef SSM_CASE_W
+        return SSM_ERR_UNSUPPORTED_N;
+    }
 #define SSM_CASE(NPT_, WS_)                                                            \
     if (pl.NPT == NPT_ && pl.WS == WS_) {                                              \
         if (kp.summary)                                                                \
@@ -1062,7 +1609,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     if (overlaps(y, by, h_last, bh)) return SSM_ERR_ALIAS;
     if (batch == 0 || dim == 0) return SSM_OK;  // nothing to compute
 
-    const Plan pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C);
+    Plan pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C);
     if (pl.grid * pl.n_seg > int64_t(0x7fffffff)) return SSM_ERR_SIZE;
 
     CUtensorMap tms[6];
@@ -1082,6 +1629,11 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
                      encode3d(&tms[4], ty, es, C, N, L, batch, int(N), pl.TC,
                               CU_TENSOR_MAP_SWIZZLE_NONE);
         if (!tma_udz) tma_bc = false;
+        if (!tma_udz) {
+            // The tensor maps could not be encoded: plan again for plain loads.
+            pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C, /*allow_tma=*/false);
+            tma_bc = false;
+        }
     }
 
     KParams kp;
@@ -1214,7 +1766,7 @@ const char* ssm_status_string(int status) {
     }
 }
 
-int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype, int64_t plan[10]) {
+int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype, int64_t plan[11]) {
     if (!plan) return SSM_ERR_NULL;
     if (batch < 0 || L < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED_N;
@@ -1233,6 +1785,7 @@ int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int dtype, i
     plan[7] = pl.tma_udz ? 1 : 0;
     plan[8] = pl.n_seg;
     plan[9] = pl.n_seg > 1 ? int64_t(pl.n_seg - 1) * batch * dim * (N + 1) * 4 : 0;
+    plan[10] = pl.ws ? 2 : 1;
     return SSM_OK;
 }
 
@@ -1265,6 +1818,10 @@ int ssm_set_knob(int key, int64_t value) {
         case SSM_KNOB_SEGMENTS:
             if (value < 0 || value > kMaxSegments) return SSM_ERR_ARG;
             g_force_segments.store(int(value));
+            return SSM_OK;
+        case SSM_KNOB_KERNEL:
+            if (value < 0 || value > 2) return SSM_ERR_ARG;
+            g_force_kernel.store(int(value));
             return SSM_OK;
         default:
             return SSM_ERR_ARG;

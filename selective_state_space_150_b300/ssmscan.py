@@ -43,6 +43,7 @@ SSM_KNOB_CHUNK = 4
 SSM_KNOB_PLAIN_LOADS = 5
 SSM_KNOB_STAGES = 6
 SSM_KNOB_SEGMENTS = 7
+SSM_KNOB_KERNEL = 8
 
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc",
             "ssm_scan_last_device_status", "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
@@ -107,12 +108,12 @@ def ssm_status_string(status: int) -> str:
 
 def ssm_scan_plan(batch, L, dim, N, dtype: int):
     """Launch plan as a dict (see include/ssmscan.h); raises on a bad argument."""
-    out = (_i64 * 10)()
+    out = (_i64 * 11)()
     st = _lib.ssm_scan_plan(batch, L, dim, N, int(dtype), out)
     if st != SSM_OK:
         raise SSMError(st, "ssm_scan_plan")
     keys = ("state_groups", "states_per_lane", "chunk", "channels_per_block", "threads",
-            "blocks", "smem_bytes", "tma", "segments", "scratch_bytes")
+            "blocks", "smem_bytes", "tma", "segments", "scratch_bytes", "kernel")
     return dict(zip(keys, [int(v) for v in out]))
 
 

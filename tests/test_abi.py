@@ -97,6 +97,7 @@ def test_knobs_validate():
     assert ssm.ssm_set_knob(K.SSM_KNOB_CHUNK, 24) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(K.SSM_KNOB_SEGMENTS, -1) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(K.SSM_KNOB_SEGMENTS, 65) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(K.SSM_KNOB_KERNEL, 3) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(99, 0) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(K.SSM_KNOB_STATE_GROUPS, 0) == K.SSM_OK
     assert ssm.ssm_set_knob(K.SSM_KNOB_WAIT_NS, 2_000_000_000) == K.SSM_OK
@@ -113,7 +114,9 @@ def test_plans_cover_the_state(shape, dtype):
     assert ws in (1, 2, 4, 8) and npt in (1, 2, 4, 8, 16)
     assert ws * npt >= N and (ws == 1 or (ws - 1) * npt < N)      # no all-padding group
     wc = 1 if ws >= 4 else 4 // ws
-    assert pl["threads"] == 32 * wc * ws and pl["channels_per_block"] == 32 * wc
+    helpers = 5 if pl["kernel"] == 2 else 0          # warp-specialised: producer, 2 prepare, 2 finish
+    assert pl["kernel"] in (1, 2) and (pl["kernel"] == 1 or pl["tma"] == 1)
+    assert pl["threads"] == 32 * (wc * ws + helpers) and pl["channels_per_block"] == 32 * wc
     assert pl["blocks"] == batch * -(-dim // pl["channels_per_block"])
     assert 0 < pl["smem_bytes"] <= 227 * 1024
     nchunks = -(-L // pl["chunk"])

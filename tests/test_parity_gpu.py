@@ -25,7 +25,7 @@ def wl_for(dtype, batch, L, dim, N, **flags):
 def _reset_knobs():
     yield
     for k in (ssmscan.SSM_KNOB_STATE_GROUPS, ssmscan.SSM_KNOB_PLAIN_LOADS, ssmscan.SSM_KNOB_STAGES,
-              ssmscan.SSM_KNOB_CHUNK, ssmscan.SSM_KNOB_SEGMENTS,
+              ssmscan.SSM_KNOB_CHUNK, ssmscan.SSM_KNOB_SEGMENTS, ssmscan.SSM_KNOB_KERNEL,
               ssmscan.SSM_KNOB_FORCE_TIMEOUT):
         ssm.ssm_set_knob(k, 0)
     ssm.ssm_set_knob(ssmscan.SSM_KNOB_WAIT_NS, 2_000_000_000)
@@ -150,6 +150,8 @@ def test_time_segments_with_optional_arguments(flags):
 
 
 def test_time_segments_deterministic_and_plain_loads_agree():
+    # one chunk length for both paths, so the segments start at the same steps
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_CHUNK, 16)
     ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, 3)
     wl = wl_for("bf16", 1, 700, 64, 16)
     inp = W.make_inputs(wl, seed=23)
@@ -159,6 +161,31 @@ def test_time_segments_deterministic_and_plain_loads_agree():
     ssm.ssm_set_knob(ssmscan.SSM_KNOB_PLAIN_LOADS, 1)
     y3, h3 = run_gpu(inp, guard=64)
     assert np.array_equal(y1, y3) and np.array_equal(h1, h3)
+
+
+# ------------------------------------------------- the two kernels agree bit for bit
+# The phase kernel and the warp-specialised kernel do the same arithmetic in
+# the same order; with the same chunk length (hence the same segment
+# boundaries) their outputs are identical.
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape,segs", [((2, 130, 72, 16), 1), ((1, 333, 96, 5), 1),
+                                        ((2, 97, 256, 64), 1), ((1, 70, 16, 128), 1),
+                                        ((1, 900, 64, 16), 5), ((2, 517, 40, 40), 3),
+                                        ((3, 61, 200, 16), 1), ((1, 250, 136, 32), 2)])
+def test_warp_specialised_kernel_matches_phase_kernel(dtype, shape, segs):
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_CHUNK, 16)
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, segs)
+    wl = wl_for(dtype, *shape)
+    inp = W.make_inputs(wl, seed=40 + segs)
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_KERNEL, 2)
+    assert ssm.ssm_scan_plan(*shape, 1 if dtype == "bf16" else 0)["kernel"] == 2
+    y2, h2 = run_gpu(inp, guard=64)
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_KERNEL, 1)
+    assert ssm.ssm_scan_plan(*shape, 1 if dtype == "bf16" else 0)["kernel"] == 1
+    y1, h1 = run_gpu(inp, guard=64)
+    assert np.array_equal(y1, y2) and np.array_equal(h1, h2)
+    yr, hr = oracle_ref(W.decoded(inp))
+    assert rel_err(y2, yr) <= TOL[dtype] and rel_err(h2, hr) <= TOL[dtype]
 
 
 def test_deterministic():
