@@ -59,11 +59,13 @@ def load(path: str | None = None):
 
 def _declare(lib):
     dp = ctypes.POINTER(ctypes.c_double)
+    i64 = ctypes.c_int64
     lib.ssm_oracle_fwd.restype = ctypes.c_int
     lib.ssm_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
-                                   dp, dp,
-                                   ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
-                                   ctypes.c_int64]
+                                   dp, dp, i64, i64, i64, i64]
+    lib.ssm_oracle_fwd_h0.restype = ctypes.c_int
+    lib.ssm_oracle_fwd_h0.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
+                                      dp, dp, i64, i64, i64, i64]
 
 
 def _f64(a):
@@ -79,17 +81,18 @@ def _ptr(a):
 
 
 def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                       softplus=False, lib=None):
+                       softplus=False, lib=None, h0=None):
     """Selective-scan forward in fp64.
 
     u, delta, z: (batch, L, dim); A: (dim, N); B, C: (batch, L, N);
-    D, delta_bias: (dim,).  D, z, delta_bias may be None.
+    D, delta_bias: (dim,); h0: (batch, dim, N) initial state.  D, z,
+    delta_bias and h0 may be None (h0 None = zero state).
     Inputs are converted to float64 exactly (fp32 or decoded bf16 values).
     Returns (y (batch, L, dim) float64, h_last (batch, dim, N) float64).
     """
     lib = lib or load()
     u, delta, A, B, C = map(_f64, (u, delta, A, B, C))
-    D, z, delta_bias = map(_f64, (D, z, delta_bias))
+    D, z, delta_bias, h0 = map(_f64, (D, z, delta_bias, h0))
     batch, L, dim = u.shape
     N = A.shape[1]
     assert delta.shape == (batch, L, dim)
@@ -103,12 +106,30 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
         assert z.shape == (batch, L, dim)
     y = np.zeros((batch, L, dim), dtype=np.float64)
     h = np.zeros((batch, dim, N), dtype=np.float64)
-    rc = lib.ssm_oracle_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
-                            _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)),
-                            _ptr(y), _ptr(h), batch, L, dim, N)
+    if h0 is None:
+        rc = lib.ssm_oracle_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)),
+                                _ptr(y), _ptr(h), batch, L, dim, N)
+    else:
+        assert h0.shape == (batch, dim, N)
+        rc = lib.ssm_oracle_fwd_h0(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                   _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0),
+                                   int(bool(softplus)), _ptr(y), _ptr(h), batch, L, dim, N)
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (rc={rc})")
     return y, h
+
+
+def selective_scan_step(h, u, delta, A, B, C, D=None, z=None, delta_bias=None,
+                        softplus=False, lib=None):
+    """One recurrent (decode) step: the definition above at L = 1, starting
+    from state h.  u, delta, z: (batch, dim); B, C: (batch, N); h: (batch,
+    dim, N).  Returns (y (batch, dim), new state (batch, dim, N))."""
+    u, delta, B, C, z = map(_f64, (u, delta, B, C, z))
+    y, hn = selective_scan_fwd(u[:, None], delta[:, None], A, B[:, None], C[:, None], D,
+                               None if z is None else z[:, None], delta_bias, softplus,
+                               lib=lib, h0=h)
+    return y[:, 0], hn
 
 
 def selective_scan_fwd_threads(u, delta, A, B, C, D=None, z=None, delta_bias=None,

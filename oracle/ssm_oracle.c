@@ -9,8 +9,11 @@
  *
  * What it computes (one (b, d) channel at a time, state h of N entries):
  *
- *   h[n] = 0                                             (initial state: zeros in
- *                                                         every listing of the pages)
+ *   h[n] = h0[b,d,n], or 0 when h0 is NULL               (initial state: zeros in
+ *                                                         every listing of the pages;
+ *                                                         a given h0 continues a
+ *                                                         sequence whose earlier part
+ *                                                         ended in state h0)
  *   for t = 0 .. L-1:
  *     dt = delta[b,t,d] + (delta_bias ? delta_bias[d] : 0)
  *     if softplus_flag: dt = softplus(dt) = log(1 + exp(dt))
@@ -37,6 +40,10 @@
  *  - The discretisation of B is the simplified (Euler) form Delta * B used by
  *    every code listing on the pages (not the exact zero-order-hold form the
  *    itwiki page prints in its "이산화" section).
+ *  - Obsidian "Mamba" note, section 4.2: recurrent (generation-time) inference
+ *    carries only the hidden state from one token to the next, so a sequence
+ *    split in two gives the same outputs when the second part starts from the
+ *    first part's final state.  That is what the optional h0 means.
  *
  * Every operation is done in double precision on the exact values of the
  * inputs (the caller passes fp32 values, or bf16 values decoded exactly, as
@@ -69,16 +76,17 @@ static double silu(double z)
  *   B, C        : (batch, L, N)
  *   D, delta_bias : (dim), may be NULL
  *   z           : may be NULL (no gate)
+ *   h0          : (batch, dim, N) initial state, may be NULL (zeros)
  *   y           : (batch, L, dim) output
  *   h_last      : (batch, dim, N) output, may be NULL
  * Returns 0, or -1 when a required pointer is NULL, a size is negative or
  * the N-entry state cannot be allocated.
  */
-int ssm_oracle_fwd(const double *u, const double *delta, const double *A,
-                   const double *B, const double *C, const double *D,
-                   const double *z, const double *delta_bias, int softplus_flag,
-                   double *y, double *h_last,
-                   int64_t batch, int64_t L, int64_t dim, int64_t N)
+int ssm_oracle_fwd_h0(const double *u, const double *delta, const double *A,
+                      const double *B, const double *C, const double *D,
+                      const double *z, const double *delta_bias, const double *h0,
+                      int softplus_flag, double *y, double *h_last,
+                      int64_t batch, int64_t L, int64_t dim, int64_t N)
 {
     if (!u || !delta || !A || !B || !C || !y)
         return -1;
@@ -92,7 +100,7 @@ int ssm_oracle_fwd(const double *u, const double *delta, const double *A,
         for (int64_t d = 0; d < dim; ++d) {
             double *h = work;
             for (int64_t n = 0; n < N; ++n)
-                h[n] = 0.0;
+                h[n] = h0 ? h0[(b * dim + d) * N + n] : 0.0;
 
             for (int64_t t = 0; t < L; ++t) {
                 const int64_t i_bld = (b * L + t) * dim + d;   /* index into (B,L,D) */
@@ -126,4 +134,15 @@ int ssm_oracle_fwd(const double *u, const double *delta, const double *A,
     }
     free(work);
     return 0;
+}
+
+/* The same with a zero initial state. */
+int ssm_oracle_fwd(const double *u, const double *delta, const double *A,
+                   const double *B, const double *C, const double *D,
+                   const double *z, const double *delta_bias, int softplus_flag,
+                   double *y, double *h_last,
+                   int64_t batch, int64_t L, int64_t dim, int64_t N)
+{
+    return ssm_oracle_fwd_h0(u, delta, A, B, C, D, z, delta_bias, NULL, softplus_flag, y,
+                             h_last, batch, L, dim, N);
 }

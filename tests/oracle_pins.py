@@ -25,6 +25,15 @@ What each pin rests on:
                   (itwiki "Mamba의 선택 메커니즘": small Delta keeps the state);
                   z = 0 gives y = 0; A < 0, delta > 0 keeps h bounded.
   golden          tests/golden/hand_worked.json, worked by hand.
+  bruteforce_h0   the closed form with an initial state h0, whose term
+                  C_t[n] exp(A[n] * sum_{r=0..t} dt_r) h0[n] is added to y_t
+                  (the state h0 decays through every step, step 0 included).
+  chaining        a sequence run in two parts, the second starting from the
+                  first part's final state, equals the run in one part; and
+                  L single recurrent steps equal one L-step scan (the
+                  generation-time recurrence of the Obsidian "Mamba" note,
+                  4.2, carries only the state).
+Pins that pass an initial state call ``scan(..., h0=h0)``.
 """
 from __future__ import annotations
 
@@ -64,14 +73,16 @@ def random_problem(rng, batch, L, dim, N, softplus=True, bias=True, gate=True, s
     return dict(u=u, delta=delta, A=A, B=B, C=C, D=D, z=z, delta_bias=db, softplus=softplus)
 
 
-def _call(scan, p):
-    return scan(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
-                p["delta_bias"], p["softplus"])
+def _call(scan, p, h0=None):
+    args = (p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"], p["delta_bias"],
+            p["softplus"])
+    return scan(*args) if h0 is None else scan(*args, h0=h0)
 
 
 # ---------------------------------------------------------------- brute force
-def bruteforce(p, dps=40):
-    """Unrolled closed form in high precision (see module docstring)."""
+def bruteforce(p, dps=40, h0=None):
+    """Unrolled closed form in high precision (see module docstring); h0 is an
+    optional initial state (batch, dim, N)."""
     mpmath.mp.dps = dps
     u, delta, A, B, C = p["u"], p["delta"], p["A"], p["B"], p["C"]
     D, z, db, sp = p["D"], p["z"], p["delta_bias"], p["softplus"]
@@ -90,6 +101,11 @@ def bruteforce(p, dps=40):
                 dts.append(x)
             for t in range(L):
                 acc = mpf(0)
+                if h0 is not None:                            # the initial state's share
+                    head = sum(dts[:t + 1], mpf(0))           # sum of dt over [0, t]
+                    for n in range(N):
+                        acc += (mpf(float(C[b, t, n])) * mpmath.exp(mpf(float(A[d, n])) * head)
+                                * mpf(float(h0[b, d, n])))
                 for s in range(t + 1):
                     tail = sum(dts[s + 1:t + 1], mpf(0))     # sum of dt over (s, t]
                     for n in range(N):
@@ -105,6 +121,8 @@ def bruteforce(p, dps=40):
             for n in range(N):
                 a = mpf(float(A[d, n]))
                 hn = mpf(0)
+                if h0 is not None:
+                    hn = mpmath.exp(a * sum(dts, mpf(0))) * mpf(float(h0[b, d, n]))
                 for s in range(L):
                     tail = sum(dts[s + 1:L], mpf(0))
                     hn += (mpmath.exp(a * tail) * dts[s] * mpf(float(B[b, s, n]))
@@ -276,6 +294,48 @@ def pin_golden(scan):
     return worst
 
 
+# ---------------------------------------------------------------- initial state
+def pin_bruteforce_h0(scan, seed=6):
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for kw in (dict(), dict(softplus=False, bias=False, gate=False, skip=False),
+               dict(softplus=True, bias=True, gate=True, skip=True, a_neg=False)):
+        p = random_problem(rng, batch=2, L=5, dim=3, N=4, **kw)
+        h0 = rng.standard_normal((2, 3, 4))
+        y, h = _call(scan, p, h0=h0)
+        yr, hr = bruteforce(p, h0=h0)
+        worst = max(worst, _rel_err(y, yr), _rel_err(h, hr))
+    return worst
+
+
+def pin_chaining(scan, seed=7):
+    """Two parts chained through the state equal one part; and L steps of one
+    token each equal one L-step scan."""
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for split in (1, 5, 12):
+        p = random_problem(rng, batch=2, L=13, dim=4, N=6)
+        h0 = rng.standard_normal((2, 4, 6))
+        y, h = _call(scan, p, h0=h0)
+        pre = {k: (v[:, :split] if isinstance(v, np.ndarray) and v.ndim == 3 else v)
+               for k, v in p.items()}
+        suf = {k: (v[:, split:] if isinstance(v, np.ndarray) and v.ndim == 3 else v)
+               for k, v in p.items()}
+        yp, hp = _call(scan, pre, h0=h0)
+        ys, hs = _call(scan, suf, h0=hp)
+        worst = max(worst, _rel_err(y[:, :split], yp), _rel_err(y[:, split:], ys),
+                    _rel_err(h, hs))
+    p = random_problem(rng, batch=2, L=7, dim=3, N=5)
+    y, h = _call(scan, p)
+    hk = np.zeros((2, 3, 5))
+    for t in range(7):
+        one = {k: (v[:, t:t + 1] if isinstance(v, np.ndarray) and v.ndim == 3 else v)
+               for k, v in p.items()}
+        yk, hk = _call(scan, one, h0=hk)
+        worst = max(worst, _rel_err(y[:, t:t + 1], yk))
+    return max(worst, _rel_err(h, hk))
+
+
 ALL_PINS = {
     "bruteforce": (pin_bruteforce, 1e-12),
     "lti_direct": (pin_lti_direct, 1e-9),
@@ -283,4 +343,6 @@ ALL_PINS = {
     "associativity": (pin_associativity, 1e-12),
     "special_cases": (pin_special_cases, 1e-12),
     "golden": (pin_golden, 1e-14),
+    "bruteforce_h0": (pin_bruteforce_h0, 1e-12),
+    "chaining": (pin_chaining, 1e-12),
 }

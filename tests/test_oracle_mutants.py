@@ -32,8 +32,12 @@ MUTANTS = {
                     acc += C[i_bln + n] * h[n];""", """                    acc += C[i_bln + n] * h[n];
                     h[n] = dA * h[n] + dBu;"""),
     "state_not_reset": ("""            for (int64_t n = 0; n < N; ++n)
-                h[n] = 0.0;
+                h[n] = h0 ? h0[(b * dim + d) * N + n] : 0.0;
 """, ""),
+    "h0_ignored": ("h0 ? h0[(b * dim + d) * N + n] : 0.0", "0.0"),
+    "h0_transposed": ("h0[(b * dim + d) * N + n]", "h0[(d * batch + b) * N + n]"),
+    "h0_not_decayed": ("h[n] = dA * h[n] + dBu;",
+                       "h[n] = (t == 0 ? 1.0 : dA) * h[n] + dBu;"),
     "B_index_uses_t_minus_1": ("B[i_bln + n]", "B[(i_bln >= N ? i_bln - N : i_bln) + n]"),
 }
 
@@ -56,8 +60,8 @@ def test_pins_catch_mutant(name, tmpdir_mod):
     oracle.build(force=True, src=cfile, out=sofile)
     lib = oracle.load(sofile)
 
-    def scan(*a):
-        return oracle.selective_scan_fwd(*a, lib=lib)
+    def scan(*a, **kw):
+        return oracle.selective_scan_fwd(*a, lib=lib, **kw)
 
     failures = []
     for pname, (fn, tol) in ALL_PINS.items():

@@ -48,3 +48,16 @@ def test_oracle_rejects_bad_arguments():
     lib = oracle.load()
     assert lib.ssm_oracle_fwd(None, None, None, None, None, None, None, None, 0,
                               None, None, 1, 1, 1, 1) == -1
+
+
+def test_oracle_decode_step_is_the_scan_at_one_token():
+    from tests.oracle_pins import random_problem
+    rng = np.random.default_rng(11)
+    p = random_problem(rng, 3, 4, 5, 6)
+    h = rng.standard_normal((3, 5, 6))
+    y_ref, h_ref = oracle.selective_scan_fwd(p["u"][:, :1], p["delta"][:, :1], p["A"],
+                                             p["B"][:, :1], p["C"][:, :1], p["D"],
+                                             p["z"][:, :1], p["delta_bias"], True, h0=h)
+    y, hn = oracle.selective_scan_step(h, p["u"][:, 0], p["delta"][:, 0], p["A"], p["B"][:, 0],
+                                       p["C"][:, 0], p["D"], p["z"][:, 0], p["delta_bias"], True)
+    assert np.array_equal(y, y_ref[:, 0]) and np.array_equal(hn, h_ref)
