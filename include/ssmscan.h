@@ -133,6 +133,57 @@ SSM_API int ssm_scan_fwd_bf16(const uint16_t *u, const uint16_t *delta, const fl
                       cudaStream_t stream);
 
 /*
+ * The scan from a given initial state h0 (batch, dim, N) fp32 instead of
+ * zeros: h before step 0 is h0, so a sequence run in two calls, the second
+ * with h0 = the first call's h_last, gives the outputs of one call over the
+ * whole sequence (up to fp32 rounding order).  This is the state the pages'
+ * recurrent inference carries from token to token (Obsidian "Mamba" note,
+ * section 4.2).  Same arguments as ssm_scan_fwd / ssm_scan_fwd_bf16 with h0
+ * after delta_bias; h0 may be NULL (zero state); it is a device pointer
+ * owned by the caller and must not overlap y or h_last (returns
+ * SSM_ERR_ALIAS): to continue a sequence in place, alternate two state
+ * buffers.
+ */
+SSM_API int ssm_scan_fwd_h0(const float *u, const float *delta, const float *A,
+                    const float *B, const float *C, const float *D,
+                    const float *z, const float *delta_bias, const float *h0,
+                    int softplus_flag, float *y, float *h_last,
+                    int64_t batch, int64_t L, int64_t dim, int64_t N,
+                    cudaStream_t stream);
+SSM_API int ssm_scan_fwd_bf16_h0(const uint16_t *u, const uint16_t *delta, const float *A,
+                    const uint16_t *B, const uint16_t *C, const float *D,
+                    const uint16_t *z, const float *delta_bias, const float *h0,
+                    int softplus_flag, uint16_t *y, float *h_last,
+                    int64_t batch, int64_t L, int64_t dim, int64_t N,
+                    cudaStream_t stream);
+
+/*
+ * One recurrent (decode) step for every channel: the scan at L = 1 from the
+ * state h, which is updated in place.
+ *   u, delta, z, y : (batch, dim)      B, C : (batch, N)
+ *   A : (dim, N) fp32    D, delta_bias : (dim,) fp32 (may be NULL)
+ *   h : (batch, dim, N) fp32, read and written
+ * For each (b, d): dt = softplus(delta + bias) (if softplus_flag);
+ *   h[n] = exp(dt A[d,n]) h[n] + dt B[b,n] u;  y = (sum_n C[b,n] h[n] + D u) silu(z).
+ * fp32 entry: all of u, delta, B, C, z, y fp32.  bf16 entry: those are bf16
+ * (16-bit patterns); A, D, delta_bias and h stay fp32.  y must not overlap an
+ * input or h, and h must not overlap an input (SSM_ERR_ALIAS).  z may be NULL
+ * (no gate).  Enqueued on `stream`; no allocation.  L steps of this call
+ * match one L-step ssm_scan_fwd_h0 from the same state within the tolerances
+ * above.
+ */
+SSM_API int ssm_scan_step(const float *u, const float *delta, const float *A,
+                  const float *B, const float *C, const float *D,
+                  const float *z, const float *delta_bias, int softplus_flag,
+                  float *h, float *y, int64_t batch, int64_t dim, int64_t N,
+                  cudaStream_t stream);
+SSM_API int ssm_scan_step_bf16(const uint16_t *u, const uint16_t *delta, const float *A,
+                  const uint16_t *B, const uint16_t *C, const float *D,
+                  const uint16_t *z, const float *delta_bias, int softplus_flag,
+                  float *h, uint16_t *y, int64_t batch, int64_t dim, int64_t N,
+                  cudaStream_t stream);
+
+/*
  * No-allocation variant of ssm_scan_fwd_bf16 (an engineering addition: the
  * pages describe nothing like it).  Same arguments, same kernels, same
  * results bit for bit; the only difference is where the time-segment

@@ -6,9 +6,14 @@ The computation lives in the CUDA library ``libssmscan.so`` (C ABI declared in
 from .ssmscan import (  # noqa: F401
     SSMError,
     selective_scan_fwd,
+    selective_scan_step,
     ssm_scan_fwd,
     ssm_scan_fwd_bf16,
     ssm_scan_fwd_bf16_noalloc,
+    ssm_scan_fwd_bf16_h0,
+    ssm_scan_fwd_h0,
+    ssm_scan_step,
+    ssm_scan_step_bf16,
     ssm_scan_last_device_status,
     ssm_scan_plan,
     ssm_set_knob,

@@ -1233,6 +1233,107 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     if (leader) bulk_wait_all();
 }
 
+// ============================================================ one recurrent step
+// The scan at L = 1 for every (b, d) channel, from state h (updated in place):
+// the generation-time recurrence, which carries only the state from one token
+// to the next (Obsidian "Mamba" note, section 4.2).
+//
+// Vector form, for N = 4 * 2^k <= 128: G = N / 4 adjacent threads share a
+// channel, each advancing four states with 16-byte loads and stores of h and A
+// (consecutive threads, consecutive 16-byte pieces of the state), and the
+// channel's readout is summed over the G threads with shuffles.  The scalar
+// form (other N) gives each thread one channel and walks its states in order.
+template <typename T>
+struct StepIn {
+    const T* u;
+    const T* delta;
+    const float* A;
+    const T* B;
+    const T* C;
+    const float* D;
+    const T* z;
+    const float* bias;
+    float* h;
+    T* y;
+    int64_t batch, dim, N;
+    int softplus;
+};
+
+template <typename T>
+__device__ __forceinline__ float step_dt(const StepIn<T>& q, int64_t i, int64_t d) {
+    float dt = Elt<T>::to_f(q.delta[i]);
+    if (q.bias != nullptr) dt += q.bias[d];
+    return q.softplus ? Act<T>::softplus(dt) : dt;
+}
+
+template <typename T>
+__device__ __forceinline__ float step_y(const StepIn<T>& q, int64_t i, int64_t d, float uu,
+                                        float acc) {
+    const float g = q.z != nullptr ? Act<T>::silu(Elt<T>::to_f(q.z[i])) : 1.f;
+    const float su = ((q.D != nullptr ? q.D[d] : 0.f) * uu) * g;
+    return fmaf(acc, g, su);
+}
+
+template <typename T, int G>
+__global__ void __launch_bounds__(128) ssm_step_vec_kernel(const StepIn<T> q) {
+    using E = Elt<T>;
+    const int64_t gt = int64_t(blockIdx.x) * 128 + threadIdx.x;
+    const int64_t i = gt / G;            // channel b * dim + d
+    const int part = int(gt % G);        // states 4 part .. 4 part + 3
+    const bool live = i < q.batch * q.dim;
+    float acc = 0.f, uu = 0.f;
+    int64_t d = 0;
+    if (live) {
+        const int64_t b = i / q.dim;
+        d = i - b * q.dim;
+        const float dt = step_dt(q, i, d);
+        uu = E::to_f(q.u[i]);
+        const float du = dt * uu;
+        float4* const hp = reinterpret_cast<float4*>(q.h + i * q.N) + part;
+        const float4 a = reinterpret_cast<const float4*>(q.A + d * q.N)[part];
+        const float4 hv = *hp;
+        const int64_t o = b * q.N + 4 * part;
+        const float bb[4] = {E::to_f(q.B[o]), E::to_f(q.B[o + 1]), E::to_f(q.B[o + 2]),
+                             E::to_f(q.B[o + 3])};
+        const float cc[4] = {E::to_f(q.C[o]), E::to_f(q.C[o + 1]), E::to_f(q.C[o + 2]),
+                             E::to_f(q.C[o + 3])};
+        const float av[4] = {a.x, a.y, a.z, a.w}, hin[4] = {hv.x, hv.y, hv.z, hv.w};
+        float hout[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            hout[j] = fmaf(ex2_approx(dt * (av[j] * kLog2e)), hin[j], du * bb[j]);
+            acc = fmaf(cc[j], hout[j], acc);
+        }
+        *hp = make_float4(hout[0], hout[1], hout[2], hout[3]);
+    }
+    // Sum over the G threads of the channel (aligned groups of G lanes; every
+    // lane takes part, live or not).
+#pragma unroll
+    for (int m = G / 2; m >= 1; m /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, m, G);
+    if (live && part == 0) q.y[i] = E::from_f(step_y(q, i, d, uu, acc));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) ssm_step_kernel(const StepIn<T> q) {
+    using E = Elt<T>;
+    const int64_t i = int64_t(blockIdx.x) * 128 + threadIdx.x;  // channel b * dim + d
+    if (i >= q.batch * q.dim) return;
+    const int64_t b = i / q.dim, d = i - b * q.dim;
+    const int64_t N = q.N;
+    const float dt = step_dt(q, i, d);
+    const float uu = E::to_f(q.u[i]);
+    const float du = dt * uu;
+    float* const hp = q.h + i * N;
+    const float* const ap = q.A + d * N;
+    float acc = 0.f;
+    for (int64_t n = 0; n < N; ++n) {
+        const float hn = fmaf(ex2_approx(dt * (ap[n] * kLog2e)), hp[n], du * E::to_f(q.B[b * N + n]));
+        hp[n] = hn;
+        acc = fmaf(E::to_f(q.C[b * N + n]), hn, acc);
+    }
+    q.y[i] = E::from_f(step_y(q, i, d, uu, acc));
+}
+
 // ------------------------------------------------------------------ host side
 std::atomic<int64_t> g_wait_ns{2000000000LL};
 std::atomic<int> g_force_timeout{0};
@@ -1578,7 +1679,7 @@ template <typename T>
 int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C, const float* D,
              const T* z, const float* delta_bias, int softplus_flag, T* y, float* h_last,
              int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream,
-             bool fixed_scratch = false) {
+             bool fixed_scratch = false, const float* h0 = nullptr) {
     if (batch < 0 || L < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
     // A pointer may be NULL only when its tensor has no elements.
     if ((batch > 0 && L > 0 && dim > 0) && (!u || !delta || !y)) return SSM_ERR_NULL;
@@ -1595,7 +1696,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
                             (const void*)z, (const void*)y})
         if (ptr && !aligned(ptr, es)) return SSM_ERR_ALIGN;
     for (const void* ptr : {(const void*)A, (const void*)D, (const void*)delta_bias,
-                            (const void*)h_last})
+                            (const void*)h_last, (const void*)h0})
         if (ptr && !aligned(ptr, 4)) return SSM_ERR_ALIGN;
     // Outputs must not overlap inputs or each other.
     const int64_t by = n_bld * int64_t(es), bh = n_bdn * 4;
@@ -1607,6 +1708,8 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
         if (overlaps(h_last, bh, in.p, in.n)) return SSM_ERR_ALIAS;
     }
     if (overlaps(y, by, h_last, bh)) return SSM_ERR_ALIAS;
+    // h0 is read by every time segment while the last one writes h_last.
+    if (overlaps(h0, bh, y, by) || overlaps(h0, bh, h_last, bh)) return SSM_ERR_ALIAS;
     if (batch == 0 || dim == 0) return SSM_OK;  // nothing to compute
 
     Plan pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C);
@@ -1663,7 +1766,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     kp.seg_chunks = pl.seg_chunks;
     kp.hseg = nullptr;
     kp.sseg = nullptr;
-    kp.h0 = nullptr;
+    kp.h0 = h0;
     if (pl.n_seg == 1) return dispatch<T>(pl, pl.grid, tms, kp, stream);
 
     // Segment summaries live in stream-ordered scratch from the device's
@@ -1696,6 +1799,60 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     return st;
 }
 
+// One recurrent step: checks, then one thread per channel.
+template <typename T>
+int scan_step(const T* u, const T* delta, const float* A, const T* B, const T* C, const float* D,
+              const T* z, const float* delta_bias, int softplus_flag, float* h, T* y,
+              int64_t batch, int64_t dim, int64_t N, cudaStream_t stream) {
+    if (batch < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
+    if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED_N;
+    if (batch == 0 || dim == 0) return SSM_OK;
+    if (!u || !delta || !A || !B || !C || !h || !y) return SSM_ERR_NULL;
+    const size_t es = sizeof(T);
+    int64_t n_bd, n_bn, n_dn, n_bdn;
+    if (!mul_ok(batch, dim, &n_bd) || !mul_ok(batch, N, &n_bn) || !mul_ok(dim, N, &n_dn) ||
+        !mul_ok(n_bd, N, &n_bdn))
+        return SSM_ERR_SIZE;
+    for (const void* ptr : {(const void*)u, (const void*)delta, (const void*)B, (const void*)C,
+                            (const void*)z, (const void*)y})
+        if (ptr && !aligned(ptr, es)) return SSM_ERR_ALIGN;
+    for (const void* ptr : {(const void*)A, (const void*)D, (const void*)delta_bias,
+                            (const void*)h})
+        if (ptr && !aligned(ptr, 4)) return SSM_ERR_ALIGN;
+    const int64_t by = n_bd * int64_t(es), bh = n_bdn * 4;
+    const struct { const void* p; int64_t n; } ins[] = {
+        {u, by}, {delta, by}, {z, z ? by : 0}, {B, n_bn * int64_t(es)}, {C, n_bn * int64_t(es)},
+        {A, n_dn * 4}, {D, D ? dim * 4 : 0}, {delta_bias, delta_bias ? dim * 4 : 0}};
+    for (const auto& in : ins) {
+        if (overlaps(y, by, in.p, in.n)) return SSM_ERR_ALIAS;
+        if (overlaps(h, bh, in.p, in.n)) return SSM_ERR_ALIAS;
+    }
+    if (overlaps(y, by, h, bh)) return SSM_ERR_ALIAS;
+    StepIn<T> q{u, delta, A, B, C, D, z, delta_bias, h, y, batch, dim, N, softplus_flag ? 1 : 0};
+    // Vector form: N = 4 G with G a power of two <= 32, and 16-byte aligned
+    // state rows.
+    const int64_t G = N / 4;
+    const bool vec = N % 4 == 0 && G <= 32 && (G & (G - 1)) == 0 && aligned(h, 16) &&
+                     aligned(A, 16);
+    const int64_t threads = vec ? n_bd * G : n_bd;
+    const int64_t blocks = (threads + 127) / 128;
+    if (blocks > int64_t(0x7fffffff)) return SSM_ERR_SIZE;
+    const dim3 grid = dim3(unsigned(blocks)), block = dim3(128);
+    if (!vec) {
+        ssm_step_kernel<T><<<grid, block, 0, stream>>>(q);
+    } else {
+        switch (G) {
+            case 1: ssm_step_vec_kernel<T, 1><<<grid, block, 0, stream>>>(q); break;
+            case 2: ssm_step_vec_kernel<T, 2><<<grid, block, 0, stream>>>(q); break;
+            case 4: ssm_step_vec_kernel<T, 4><<<grid, block, 0, stream>>>(q); break;
+            case 8: ssm_step_vec_kernel<T, 8><<<grid, block, 0, stream>>>(q); break;
+            case 16: ssm_step_vec_kernel<T, 16><<<grid, block, 0, stream>>>(q); break;
+            default: ssm_step_vec_kernel<T, 32><<<grid, block, 0, stream>>>(q); break;
+        }
+    }
+    return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -1718,6 +1875,45 @@ int ssm_scan_fwd_bf16(const uint16_t* u, const uint16_t* delta, const float* A,
                         reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
                         reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
                         reinterpret_cast<bf*>(y), h_last, batch, L, dim, N, stream);
+}
+
+int ssm_scan_fwd_h0(const float* u, const float* delta, const float* A, const float* B,
+                    const float* C, const float* D, const float* z, const float* delta_bias,
+                    const float* h0, int softplus_flag, float* y, float* h_last, int64_t batch,
+                    int64_t L, int64_t dim, int64_t N, cudaStream_t stream) {
+    return scan_fwd<float>(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, h_last, batch,
+                           L, dim, N, stream, false, h0);
+}
+
+int ssm_scan_fwd_bf16_h0(const uint16_t* u, const uint16_t* delta, const float* A,
+                         const uint16_t* B, const uint16_t* C, const float* D,
+                         const uint16_t* z, const float* delta_bias, const float* h0,
+                         int softplus_flag, uint16_t* y, float* h_last, int64_t batch,
+                         int64_t L, int64_t dim, int64_t N, cudaStream_t stream) {
+    using bf = __nv_bfloat16;
+    return scan_fwd<bf>(reinterpret_cast<const bf*>(u), reinterpret_cast<const bf*>(delta), A,
+                        reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
+                        reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
+                        reinterpret_cast<bf*>(y), h_last, batch, L, dim, N, stream, false, h0);
+}
+
+int ssm_scan_step(const float* u, const float* delta, const float* A, const float* B,
+                  const float* C, const float* D, const float* z, const float* delta_bias,
+                  int softplus_flag, float* h, float* y, int64_t batch, int64_t dim, int64_t N,
+                  cudaStream_t stream) {
+    return scan_step<float>(u, delta, A, B, C, D, z, delta_bias, softplus_flag, h, y, batch, dim,
+                            N, stream);
+}
+
+int ssm_scan_step_bf16(const uint16_t* u, const uint16_t* delta, const float* A,
+                       const uint16_t* B, const uint16_t* C, const float* D, const uint16_t* z,
+                       const float* delta_bias, int softplus_flag, float* h, uint16_t* y,
+                       int64_t batch, int64_t dim, int64_t N, cudaStream_t stream) {
+    using bf = __nv_bfloat16;
+    return scan_step<bf>(reinterpret_cast<const bf*>(u), reinterpret_cast<const bf*>(delta), A,
+                         reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
+                         reinterpret_cast<const bf*>(z), delta_bias, softplus_flag, h,
+                         reinterpret_cast<bf*>(y), batch, dim, N, stream);
 }
 
 int ssm_scan_fwd_bf16_noalloc(const uint16_t* u, const uint16_t* delta, const float* A,

@@ -46,6 +46,7 @@ SSM_KNOB_SEGMENTS = 7
 SSM_KNOB_KERNEL = 8
 
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc",
+            "ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0", "ssm_scan_step", "ssm_scan_step_bf16",
             "ssm_scan_last_device_status", "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
 
 _vp = ctypes.c_void_p
@@ -54,6 +55,12 @@ _FWD_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp,
              _i64, _i64, _i64, _i64, _vp]
 for _name in ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc"):
     getattr(_lib, _name).argtypes = _FWD_ARGS
+    getattr(_lib, _name).restype = ctypes.c_int
+for _name in ("ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0"):
+    getattr(_lib, _name).argtypes = _FWD_ARGS[:8] + [_vp] + _FWD_ARGS[8:]
+    getattr(_lib, _name).restype = ctypes.c_int
+for _name in ("ssm_scan_step", "ssm_scan_step_bf16"):
+    getattr(_lib, _name).argtypes = [_vp] * 8 + [ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _vp]
     getattr(_lib, _name).restype = ctypes.c_int
 _lib.ssm_scan_last_device_status.argtypes = [_vp]
 _lib.ssm_scan_last_device_status.restype = ctypes.c_int
@@ -98,6 +105,40 @@ def ssm_scan_fwd_bf16_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus_flag
                                           batch, L, dim, N, stream or None)
 
 
+def ssm_scan_fwd_h0(u, delta, A, B, C, D, z, delta_bias, h0, softplus_flag, y, h_last,
+                    batch, L, dim, N, stream) -> int:
+    """fp32 entry point from an initial state h0; pointer arguments are ints."""
+    return _lib.ssm_scan_fwd_h0(u or None, delta or None, A or None, B or None, C or None,
+                                D or None, z or None, delta_bias or None, h0 or None,
+                                int(softplus_flag), y or None, h_last or None, batch, L, dim, N,
+                                stream or None)
+
+
+def ssm_scan_fwd_bf16_h0(u, delta, A, B, C, D, z, delta_bias, h0, softplus_flag, y, h_last,
+                         batch, L, dim, N, stream) -> int:
+    """bf16 entry point from an initial state h0; pointer arguments are ints."""
+    return _lib.ssm_scan_fwd_bf16_h0(u or None, delta or None, A or None, B or None, C or None,
+                                     D or None, z or None, delta_bias or None, h0 or None,
+                                     int(softplus_flag), y or None, h_last or None, batch, L,
+                                     dim, N, stream or None)
+
+
+def ssm_scan_step(u, delta, A, B, C, D, z, delta_bias, softplus_flag, h, y, batch, dim, N,
+                  stream) -> int:
+    """fp32 one-token recurrent step (h updated in place); pointers are ints."""
+    return _lib.ssm_scan_step(u or None, delta or None, A or None, B or None, C or None,
+                              D or None, z or None, delta_bias or None, int(softplus_flag),
+                              h or None, y or None, batch, dim, N, stream or None)
+
+
+def ssm_scan_step_bf16(u, delta, A, B, C, D, z, delta_bias, softplus_flag, h, y, batch, dim, N,
+                       stream) -> int:
+    """bf16 one-token recurrent step (h updated in place); pointers are ints."""
+    return _lib.ssm_scan_step_bf16(u or None, delta or None, A or None, B or None, C or None,
+                                   D or None, z or None, delta_bias or None, int(softplus_flag),
+                                   h or None, y or None, batch, dim, N, stream or None)
+
+
 def ssm_scan_last_device_status(stream=0) -> int:
     return _lib.ssm_scan_last_device_status(stream or None)
 
@@ -126,27 +167,35 @@ def _ptr(t):
     return 0 if t is None else t.data_ptr()
 
 
-def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
-                       y=None, h_last=None, stream=None, want_h_last=True):
-    """Run the kernel on torch CUDA tensors.
-
-    u, delta, z: (batch, L, dim); B, C: (batch, L, N); A: (dim, N) fp32;
-    D, delta_bias: (dim,) fp32.  u/delta/B/C/z are all fp32 (fp32 entry point)
-    or all bf16 (bf16 entry point).  Returns (y, h_last).  Work is enqueued on
-    ``stream`` (default: torch's current stream) without synchronising.
-    """
+def _check_io(u, delta, B, C, z, A, D, delta_bias):
     import torch
 
-    bf16 = u.dtype == torch.bfloat16
-    if not bf16 and u.dtype != torch.float32:
+    if u.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError(f"u must be float32 or bfloat16, got {u.dtype}")
-    io = (u, delta, B, C) + ((z,) if z is not None else ())
-    for t in io:
+    for t in (u, delta, B, C) + ((z,) if z is not None else ()):
         if t.dtype != u.dtype or not t.is_cuda or not t.is_contiguous():
             raise TypeError("u, delta, B, C, z must share u's dtype and be contiguous CUDA tensors")
     for t in (A, D, delta_bias):
         if t is not None and (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()):
             raise TypeError("A, D, delta_bias must be contiguous float32 CUDA tensors")
+    return u.dtype == torch.bfloat16
+
+
+def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
+                       y=None, h_last=None, stream=None, want_h_last=True, h0=None):
+    """Run the kernel on torch CUDA tensors.
+
+    u, delta, z: (batch, L, dim); B, C: (batch, L, N); A: (dim, N) fp32;
+    D, delta_bias: (dim,) fp32; h0: (batch, dim, N) fp32 initial state (None:
+    zeros).  u/delta/B/C/z are all fp32 (fp32 entry point) or all bf16 (bf16
+    entry point).  Returns (y, h_last).  Work is enqueued on ``stream``
+    (default: torch's current stream) without synchronising.
+    """
+    import torch
+
+    bf16 = _check_io(u, delta, B, C, z, A, D, delta_bias)
+    if h0 is not None and (h0.dtype != torch.float32 or not h0.is_cuda or not h0.is_contiguous()):
+        raise TypeError("h0 must be a contiguous float32 CUDA tensor")
     batch, L, dim = u.shape
     N = A.shape[1]
     if y is None:
@@ -155,10 +204,40 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softp
         h_last = torch.empty((batch, dim, N), dtype=torch.float32, device=u.device)
     if stream is None:
         stream = torch.cuda.current_stream(u.device).cuda_stream
-    fn = ssm_scan_fwd_bf16 if bf16 else ssm_scan_fwd
-    st = fn(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-            _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(h_last),
-            batch, L, dim, N, int(stream))
+    if h0 is None:
+        fn = ssm_scan_fwd_bf16 if bf16 else ssm_scan_fwd
+        st = fn(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(h_last),
+                batch, L, dim, N, int(stream))
+    else:
+        fn = ssm_scan_fwd_bf16_h0 if bf16 else ssm_scan_fwd_h0
+        st = fn(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                _ptr(delta_bias), _ptr(h0), int(bool(softplus)), _ptr(y), _ptr(h_last),
+                batch, L, dim, N, int(stream))
     if st != SSM_OK:
         raise SSMError(st, fn.__name__)
     return y, h_last
+
+
+def selective_scan_step(u, delta, A, B, C, h, D=None, z=None, delta_bias=None, softplus=False,
+                        y=None, stream=None):
+    """One recurrent step on torch CUDA tensors; ``h`` (batch, dim, N) fp32 is
+    updated in place.  u, delta, z: (batch, dim); B, C: (batch, N).  Returns y
+    (batch, dim)."""
+    import torch
+
+    bf16 = _check_io(u, delta, B, C, z, A, D, delta_bias)
+    if h.dtype != torch.float32 or not h.is_cuda or not h.is_contiguous():
+        raise TypeError("h must be a contiguous float32 CUDA tensor")
+    batch, dim = u.shape
+    N = A.shape[1]
+    if y is None:
+        y = torch.empty_like(u)
+    if stream is None:
+        stream = torch.cuda.current_stream(u.device).cuda_stream
+    fn = ssm_scan_step_bf16 if bf16 else ssm_scan_step
+    st = fn(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            int(bool(softplus)), _ptr(h), _ptr(y), batch, dim, N, int(stream))
+    if st != SSM_OK:
+        raise SSMError(st, fn.__name__)
+    return y

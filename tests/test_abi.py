@@ -152,3 +152,43 @@ def test_plan_rejects_bad_arguments():
         ssm.ssm_scan_plan(1, 1, 1, 0, 1)
     with pytest.raises(ssm.SSMError):
         ssm.ssm_scan_plan(1, 1, 1, 16, 7)
+
+
+# ---------------------------------------------------------------- initial state / decode step
+def fwd_h0(fn, **kw):
+    args = dict(u=P, delta=P + 0x100000, A=P + 0x200000, B=P + 0x300000, C=P + 0x400000,
+                D=0, z=0, delta_bias=0, h0=P + 0x500000, softplus_flag=0, y=Q, h_last=Q + 0x100000,
+                batch=2, L=8, dim=16, N=4, stream=0)
+    args.update(kw)
+    return fn(**args)
+
+
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd_h0, ssm.ssm_scan_fwd_bf16_h0])
+def test_h0_checks(fn):
+    assert fwd_h0(fn, h0=Q + 0x100000) == ssmscan.SSM_ERR_ALIAS      # h0 is h_last
+    assert fwd_h0(fn, h0=Q + 0x40) == ssmscan.SSM_ERR_ALIAS          # h0 inside y
+    assert fwd_h0(fn, h0=P + 0x500002) == ssmscan.SSM_ERR_ALIGN
+    assert fwd_h0(fn, u=0) == ssmscan.SSM_ERR_NULL
+    assert fwd_h0(fn, batch=0) == ssmscan.SSM_OK
+
+
+def step(fn, **kw):
+    args = dict(u=P, delta=P + 0x100000, A=P + 0x200000, B=P + 0x300000, C=P + 0x400000,
+                D=0, z=0, delta_bias=0, softplus_flag=1, h=Q, y=Q + 0x100000,
+                batch=2, dim=16, N=4, stream=0)
+    args.update(kw)
+    return fn(**args)
+
+
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_step, ssm.ssm_scan_step_bf16])
+def test_step_checks(fn):
+    for k in ("u", "delta", "A", "B", "C", "h", "y"):
+        assert step(fn, **{k: 0}) == ssmscan.SSM_ERR_NULL, k
+    assert step(fn, batch=-1) == ssmscan.SSM_ERR_SIZE
+    assert step(fn, N=0) == ssmscan.SSM_ERR_SIZE
+    assert step(fn, N=129) == ssmscan.SSM_ERR_UNSUPPORTED_N
+    assert step(fn, h=P + 0x100000) == ssmscan.SSM_ERR_ALIAS          # h is delta
+    assert step(fn, y=Q + 0x10) == ssmscan.SSM_ERR_ALIAS              # y inside h
+    assert step(fn, y=P) == ssmscan.SSM_ERR_ALIAS                     # y is u
+    assert step(fn, h=Q + 2) == ssmscan.SSM_ERR_ALIGN
+    assert step(fn, batch=0) == ssmscan.SSM_OK and step(fn, dim=0) == ssmscan.SSM_OK
