@@ -66,6 +66,8 @@ def _declare(lib):
     lib.ssm_oracle_fwd_h0.restype = ctypes.c_int
     lib.ssm_oracle_fwd_h0.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
                                       dp, dp, i64, i64, i64, i64]
+    lib.ssm_oracle_causal_conv_silu.restype = ctypes.c_int
+    lib.ssm_oracle_causal_conv_silu.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64]
 
 
 def _f64(a):
@@ -130,6 +132,29 @@ def selective_scan_step(h, u, delta, A, B, C, D=None, z=None, delta_bias=None,
                                None if z is None else z[:, None], delta_bias, softplus,
                                lib=lib, h0=h)
     return y[:, 0], hn
+
+
+def causal_conv_silu(x, w, cb=None, lib=None):
+    """u = silu(causal depthwise conv1d(x) + cb) in fp64 (see ssm_oracle.c).
+    x: (batch, L, dim); w: (dim, K); cb: (dim,) or None."""
+    lib = lib or load()
+    x, w, cb = _f64(x), _f64(w), _f64(cb)
+    batch, L, dim = x.shape
+    K = w.shape[1]
+    assert w.shape == (dim, K) and (cb is None or cb.shape == (dim,))
+    u = np.zeros((batch, L, dim), dtype=np.float64)
+    rc = lib.ssm_oracle_causal_conv_silu(_ptr(x), _ptr(w), _ptr(cb), _ptr(u), batch, L, dim, K)
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (rc={rc})")
+    return u
+
+
+def conv_selective_scan_fwd(x, w, cb, delta, A, B, C, D=None, z=None, delta_bias=None,
+                            softplus=False, h0=None):
+    """The scan whose input is u = causal_conv_silu(x, w, cb) (the two steps in
+    order, each as defined above).  Returns (y, h_last)."""
+    u = causal_conv_silu(x, w, cb)
+    return selective_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, h0=h0)
 
 
 def selective_scan_fwd_threads(u, delta, A, B, C, D=None, z=None, delta_bias=None,

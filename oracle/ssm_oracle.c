@@ -146,3 +146,36 @@ int ssm_oracle_fwd(const double *u, const double *delta, const double *A,
     return ssm_oracle_fwd_h0(u, delta, A, B, C, D, z, delta_bias, NULL, softplus_flag, y,
                              h_last, batch, L, dim, N);
 }
+
+/*
+ * Causal depthwise 1-D convolution followed by SiLU: the step before the scan
+ * in the MambaBlock listings ("Mamba와 State Space Model 논문 심층 분석",
+ * youngju.dev, and the SelectiveSSM listing of the "State Space Models (SSM)"
+ * summary page, section 5.1): nn.Conv1d with groups = channels, kernel size
+ * K, padding K - 1 and a bias, trimmed to the first L outputs, then SiLU.
+ * Conv1d is a cross-correlation over the left-padded input, so
+ *
+ *   u[b,t,d] = silu( sum_{k=0..K-1} w[d,k] * x[b, t - (K-1) + k, d] + cb[d] ),
+ *
+ * with x = 0 before t = 0 (the causal padding).
+ *   x, u : (batch, L, dim)    w : (dim, K)    cb : (dim) or NULL (no bias)
+ * Returns 0, or -1 for a NULL pointer or a bad size.
+ */
+int ssm_oracle_causal_conv_silu(const double *x, const double *w, const double *cb, double *u,
+                                int64_t batch, int64_t L, int64_t dim, int64_t K)
+{
+    if (!x || !w || !u || batch < 0 || L < 0 || dim < 0 || K < 1)
+        return -1;
+    for (int64_t b = 0; b < batch; ++b)
+        for (int64_t t = 0; t < L; ++t)
+            for (int64_t d = 0; d < dim; ++d) {
+                double acc = cb ? cb[d] : 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    const int64_t s = t - (K - 1) + k;   /* input step under tap k */
+                    if (s >= 0)
+                        acc += w[d * K + k] * x[(b * L + s) * dim + d];
+                }
+                u[(b * L + t) * dim + d] = silu(acc);
+            }
+    return 0;
+}

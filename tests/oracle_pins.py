@@ -34,6 +34,17 @@ What each pin rests on:
                   generation-time recurrence of the Obsidian "Mamba" note,
                   4.2, carries only the state).
 Pins that pass an initial state call ``scan(..., h0=h0)``.
+
+The causal convolution + SiLU prologue (``conv`` functions with the signature
+``conv(x, w, cb) -> u``) is pinned separately:
+  conv_numpy      each channel against numpy.convolve (full convolution of x
+                  with the kernel, the first L outputs) plus the bias, then
+                  SiLU from its definition z / (1 + e^-z).
+  conv_k1         K = 1 is the pointwise silu(w x + cb).
+  conv_causal     changing x at step s changes no u before s, and changes u
+                  at s .. s + K - 1.
+  conv_impulse    a unit impulse at step s with zero bias gives
+                  u[s + j] = silu(w[K-1-j]) (the taps in reverse order).
 """
 from __future__ import annotations
 
@@ -334,6 +345,71 @@ def pin_chaining(scan, seed=7):
         yk, hk = _call(scan, one, h0=hk)
         worst = max(worst, _rel_err(y[:, t:t + 1], yk))
     return max(worst, _rel_err(h, hk))
+
+
+# ---------------------------------------------------------------- conv prologue
+def _silu(v):
+    return v / (1.0 + np.exp(-v))
+
+
+def pin_conv_numpy(conv, seed=8):
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for K, bias in ((4, True), (3, False), (2, True)):
+        x = rng.standard_normal((2, 19, 5))
+        w = rng.standard_normal((5, K))
+        cb = rng.standard_normal(5) if bias else None
+        u = conv(x, w, cb)
+        ref = np.empty_like(x)
+        for b in range(2):
+            for d in range(5):
+                # Conv1d is a cross-correlation: convolve with the reversed taps
+                full = np.convolve(x[b, :, d], w[d, ::-1])
+                ref[b, :, d] = full[:19] + (cb[d] if bias else 0.0)
+        worst = max(worst, _rel_err(u, _silu(ref)))
+    return worst
+
+
+def pin_conv_k1(conv, seed=9):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((3, 7, 4))
+    w = rng.standard_normal((4, 1))
+    cb = rng.standard_normal(4)
+    return _rel_err(conv(x, w, cb), _silu(x * w[:, 0] + cb))
+
+
+def pin_conv_causal(conv, seed=10):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((1, 16, 3))
+    w = rng.standard_normal((3, 4))
+    cb = rng.standard_normal(3)
+    u0 = conv(x, w, cb)
+    x2 = x.copy()
+    x2[:, 9] += 1.0
+    u1 = conv(x2, w, cb)
+    changed = np.any(u1 != u0, axis=(0, 2))
+    ok = (not np.any(changed[:9])) and bool(np.all(changed[9:13])) and not np.any(changed[13:])
+    return 0.0 if ok else 1.0
+
+
+def pin_conv_impulse(conv):
+    K = 4
+    w = np.array([[0.5, -1.25, 2.0, 0.75]])
+    x = np.zeros((1, 12, 1))
+    x[0, 5, 0] = 1.0
+    u = conv(x, w, np.zeros(1))
+    ref = np.zeros(12)            # silu(0) = 0 away from the impulse
+    for j in range(K):
+        ref[5 + j] = _silu(w[0, K - 1 - j])
+    return _rel_err(u[0, :, 0], ref)
+
+
+CONV_PINS = {
+    "conv_numpy": (pin_conv_numpy, 1e-14),
+    "conv_k1": (pin_conv_k1, 1e-15),
+    "conv_causal": (pin_conv_causal, 0.0),
+    "conv_impulse": (pin_conv_impulse, 1e-15),
+}
 
 
 ALL_PINS = {

@@ -7,7 +7,7 @@ import subprocess
 import pytest
 
 import oracle
-from tests.oracle_pins import ALL_PINS
+from tests.oracle_pins import ALL_PINS, CONV_PINS
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ssm_oracle.c")
 
@@ -68,6 +68,37 @@ def test_pins_catch_mutant(name, tmpdir_mod):
         try:
             err = fn(scan)
         except Exception:           # a crash or a shape error also counts as caught
+            err = float("inf")
+        if not (err <= tol):
+            failures.append(pname)
+    assert failures, f"mutant {name} passed every pin"
+
+
+CONV_MUTANTS = {
+    "conv_not_causal": ("const int64_t s = t - (K - 1) + k;", "const int64_t s = t + k;"),
+    "conv_taps_reversed": ("w[d * K + k]", "w[d * K + (K - 1 - k)]"),
+    "conv_bias_dropped": ("double acc = cb ? cb[d] : 0.0;", "double acc = 0.0;"),
+    "conv_no_silu": ("u[(b * L + t) * dim + d] = silu(acc);", "u[(b * L + t) * dim + d] = acc;"),
+    "conv_off_by_one": ("const int64_t s = t - (K - 1) + k;", "const int64_t s = t - K + k;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CONV_MUTANTS))
+def test_conv_pins_catch_mutant(name, tmpdir_mod):
+    old, new = CONV_MUTANTS[name]
+    src = open(SRC).read()
+    assert old in src, f"mutation anchor for {name} not found"
+    cfile = os.path.join(tmpdir_mod, f"{name}.c")
+    sofile = os.path.join(tmpdir_mod, f"lib{name}.so")
+    with open(cfile, "w") as f:
+        f.write(src.replace(old, new))
+    oracle.build(force=True, src=cfile, out=sofile)
+    lib = oracle.load(sofile)
+    failures = []
+    for pname, (fn, tol) in CONV_PINS.items():
+        try:
+            err = fn(lambda x, w, cb: oracle.causal_conv_silu(x, w, cb, lib=lib))
+        except Exception:
             err = float("inf")
         if not (err <= tol):
             failures.append(pname)

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.oracle_pins import ALL_PINS
+from tests.oracle_pins import ALL_PINS, CONV_PINS
 
 
 @pytest.mark.parametrize("name", sorted(ALL_PINS))
@@ -61,3 +61,10 @@ def test_oracle_decode_step_is_the_scan_at_one_token():
     y, hn = oracle.selective_scan_step(h, p["u"][:, 0], p["delta"][:, 0], p["A"], p["B"][:, 0],
                                        p["C"][:, 0], p["D"], p["z"][:, 0], p["delta_bias"], True)
     assert np.array_equal(y, y_ref[:, 0]) and np.array_equal(hn, h_ref)
+
+
+@pytest.mark.parametrize("name", sorted(CONV_PINS))
+def test_oracle_conv_pin(name):
+    fn, tol = CONV_PINS[name]
+    err = fn(oracle.causal_conv_silu)
+    assert err <= tol, f"{name}: error {err:.3e} > {tol:.1e}"
