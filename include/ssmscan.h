@@ -158,6 +158,36 @@ SSM_API int ssm_scan_fwd_bf16_h0(const uint16_t *u, const uint16_t *delta, const
                     cudaStream_t stream);
 
 /*
+ * The scan with its input produced in the same kernel by the step before it
+ * in the Mamba block: a causal depthwise 1-D convolution of kernel size
+ * conv_k (1 .. 4) with bias, then SiLU (the MambaBlock listing of the
+ * youngju.dev page, and the SelectiveSSM listing, section 5.1, of the "State
+ * Space Models (SSM)" summary page: nn.Conv1d(groups = channels, padding =
+ * conv_k - 1), trimmed to the first L outputs):
+ *
+ *   u[b,t,d] = silu( sum_{k<conv_k} conv_w[d,k] x[b, t-(conv_k-1)+k, d] + conv_b[d] ),
+ *
+ * x = 0 before t = 0; then the scan of ssm_scan_fwd on u (the D skip uses
+ * this u).  x is (batch, L, dim) in place of u; conv_w is (dim, conv_k) fp32;
+ * conv_b is (dim,) fp32 or NULL.  Everything else as ssm_scan_fwd /
+ * ssm_scan_fwd_bf16.  u is never written to memory.  The prologue needs rows
+ * that move by TMA (dim x element size a multiple of 16 bytes, x, delta, z, y
+ * 16-byte aligned); otherwise the call returns SSM_ERR_ALIGN.
+ */
+SSM_API int ssm_conv_scan_fwd(const float *x, const float *conv_w, const float *conv_b,
+                      int conv_k, const float *delta, const float *A,
+                      const float *B, const float *C, const float *D,
+                      const float *z, const float *delta_bias, int softplus_flag,
+                      float *y, float *h_last, int64_t batch, int64_t L, int64_t dim,
+                      int64_t N, cudaStream_t stream);
+SSM_API int ssm_conv_scan_fwd_bf16(const uint16_t *x, const float *conv_w, const float *conv_b,
+                      int conv_k, const uint16_t *delta, const float *A,
+                      const uint16_t *B, const uint16_t *C, const float *D,
+                      const uint16_t *z, const float *delta_bias, int softplus_flag,
+                      uint16_t *y, float *h_last, int64_t batch, int64_t L, int64_t dim,
+                      int64_t N, cudaStream_t stream);
+
+/*
  * One recurrent (decode) step for every channel: the scan at L = 1 from the
  * state h, which is updated in place.
  *   u, delta, z, y : (batch, dim)      B, C : (batch, N)

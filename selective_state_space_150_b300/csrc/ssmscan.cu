@@ -58,6 +58,8 @@ constexpr int kMaxStages = 8;  // deepest TMA ring
 constexpr int kMaxSegments = 64;   // time segments of one call
 constexpr int kMinSegChunks = 8;   // shortest automatic segment, in chunks
 constexpr int kMinSegments = 8;    // fewest automatic segments once a split pays
+constexpr int kMaxConvK = 4;       // longest causal convolution of the prologue
+constexpr int kConvHalo = kMaxConvK - 1;  // rows before a chunk that it reads
 constexpr size_t kMaxSmem = 227 * 1024;  // opt-in shared memory per block on sm_103
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -287,7 +289,11 @@ struct Tile {
     static constexpr uint32_t SWZ_MASK = uint32_t(RS / 16 - 1);
     // Byte offset of byte b of row t in a tile of TC rows.
     __device__ static __forceinline__ uint32_t off(int t, int b, int TC) {
-        const uint32_t o = uint32_t((b / RS) * TC * RS + t * RS + (b % RS));
+        return off_cbs(t, b, uint32_t(TC * RS));
+    }
+    // The same with column blocks cbs bytes apart (a multiple of 1024).
+    __device__ static __forceinline__ uint32_t off_cbs(int t, int b, uint32_t cbs) {
+        const uint32_t o = uint32_t(b / RS) * cbs + uint32_t(t * RS + (b % RS));
         return o ^ (((o >> 7) & SWZ_MASK) << 4);
     }
 };
@@ -325,6 +331,12 @@ struct KParams {
     float* hseg;        // [n_seg-1][batch][dim][N]
     float* sseg;        // [n_seg-1][batch][dim]
     const float* h0;    // [batch][dim][N] or null (zero initial state)
+    // Causal depthwise convolution + SiLU prologue (warp-specialised kernel
+    // only): when conv_k > 0, the tensor at u is the convolution's input x
+    // and the scan input is u = silu(sum_k conv_w[d,k] x[t-(conv_k-1)+k] + conv_b[d]).
+    const float* conv_w;  // [dim][conv_k]
+    const float* conv_b;  // [dim] or null
+    int conv_k;           // 0 (no prologue) or 1 .. kMaxConvK
 };
 
 // Compile-time geometry of one block.
@@ -861,8 +873,12 @@ struct GeoW {
 
 // Shared memory of one warp-specialised block (bytes from a 1024-byte aligned base).
 //   raw ring  stages x { u, delta, z : tile ; B, C : [TC][N] T }   (summary: u, delta, B)
+//             with the convolution prologue the u tile is the x tile, TC +
+//             kConvHalo rows from step t0 - kConvHalo, each column block
+//             padded to a multiple of 1024 bytes
 //   s_B, s_C  2 x [TC][NP] fp32        (summary: no s_C)
 //   s_dd      2 x [TC][DT] float2      (dt, dt*u)
+//   s_u       2 x [TC][DT] fp32        (prologue only: u for the skip term)
 //   s_part    2 x [WS][TC][DT] fp32                        (summary: none)
 //   s_y       2 x tile                                     (summary: none)
 //   barriers  TMA[kMaxStages], EMPTY[kMaxStages], FULL[2], DONE[2], PEMPTY[2],
@@ -870,19 +886,24 @@ struct GeoW {
 template <typename T, int NPT, int WS, int TC, bool SUM>
 struct LayoutW {
     using G = GeoW<T, NPT, WS, TC>;
-    size_t tile_bc, stage, bc, dd, part, off_raw, off_bf, off_cf, off_dd, off_part, off_y,
-        off_bar, total;
-    __host__ __device__ LayoutW(int64_t N, int stages) {
+    size_t tile_bc, cbs_x, tile_x, stage, bc, dd, ub, part, off_raw, off_bf, off_cf, off_dd, off_u,
+        off_part, off_y, off_bar, total;
+    __host__ __device__ LayoutW(int64_t N, int stages, bool conv = false) {
+        using TT = typename G::TileT;
         tile_bc = round1k(size_t(TC) * size_t(N) * G::ES);
-        stage = (SUM ? 2 : 3) * G::TILE + (SUM ? 1 : 2) * tile_bc;
+        cbs_x = conv ? round1k(size_t(TC + kConvHalo) * TT::RS) : size_t(TC) * TT::RS;
+        tile_x = conv ? TT::NB * cbs_x : G::TILE;
+        stage = tile_x + (SUM ? 1 : 2) * G::TILE + (SUM ? 1 : 2) * tile_bc;
         bc = round1k(size_t(TC) * G::NP * 4);
         dd = round1k(size_t(TC) * G::DT * 8);
+        ub = (conv && !SUM) ? round1k(size_t(TC) * G::DT * 4) : 0;
         part = round1k(size_t(WS) * TC * G::DT * 4);
         off_raw = 0;
         off_bf = off_raw + size_t(stages) * stage;
         off_cf = off_bf + 2 * bc;
         off_dd = off_cf + (SUM ? 0 : 2 * bc);
-        off_part = off_dd + 2 * dd;
+        off_u = off_dd + 2 * dd;
+        off_part = off_u + 2 * ub;
         off_y = off_part + (SUM ? 0 : 2 * part);
         off_bar = off_y + (SUM ? 0 : 2 * G::TILE);
         total = off_bar + 256;
@@ -909,7 +930,8 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     __shared__ int s_abort;
     volatile int* const abort_flag = &s_abort;
     unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const LayoutW<T, NPT, WS, TC, SUMMARY> lay(p.N, p.stages);
+    const bool conv = p.conv_k > 0;
+    const LayoutW<T, NPT, WS, TC, SUMMARY> lay(p.N, p.stages, conv);
     const int nst = p.stages;
 
     const int tid = threadIdx.x;
@@ -922,17 +944,22 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
 
     unsigned char* const raw0 = base + lay.off_raw;
     const uint32_t stage_b = uint32_t(lay.stage), tbc = uint32_t(lay.tile_bc);
+    const uint32_t tilex = uint32_t(lay.tile_x), cbsx = uint32_t(lay.cbs_x);
     constexpr uint32_t TILE = uint32_t(G::TILE);
-    constexpr uint32_t NTILE = SUMMARY ? 2 : 3;
+    constexpr uint32_t NDZ = SUMMARY ? 1 : 2;  // delta (, z) tiles after the u / x tile
     auto raw_u = [=](int s) { return raw0 + s * stage_b; };
-    auto raw_dt = [=](int s) { return raw0 + s * stage_b + TILE; };
-    auto raw_z = [=](int s) { return raw0 + s * stage_b + 2 * TILE; };
-    auto raw_B = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + NTILE * TILE); };
-    auto raw_C = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + NTILE * TILE + tbc); };
+    auto raw_dt = [=](int s) { return raw0 + s * stage_b + tilex; };
+    auto raw_z = [=](int s) { return raw0 + s * stage_b + tilex + TILE; };
+    auto raw_B = [=](int s) { return reinterpret_cast<T*>(raw0 + s * stage_b + tilex + NDZ * TILE); };
+    auto raw_C = [=](int s) {
+        return reinterpret_cast<T*>(raw0 + s * stage_b + tilex + NDZ * TILE + tbc);
+    };
     const uint32_t bcb = uint32_t(lay.bc), ddb = uint32_t(lay.dd), ptb = uint32_t(lay.part);
+    const uint32_t ubb = uint32_t(lay.ub);
     auto s_B = [=](int k) { return reinterpret_cast<float*>(base + lay.off_bf + k * bcb); };
     auto s_C = [=](int k) { return reinterpret_cast<float*>(base + lay.off_cf + k * bcb); };
     auto s_dd = [=](int k) { return reinterpret_cast<float2*>(base + lay.off_dd + k * ddb); };
+    auto s_u = [=](int k) { return reinterpret_cast<float2*>(base + lay.off_u + k * ubb); };
     auto s_part = [=](int k) { return reinterpret_cast<float*>(base + lay.off_part + k * ptb); };
     unsigned char* const s_y0 = base + lay.off_y;
     const uint32_t bar0 = smem_u32(base + lay.off_bar);
@@ -1037,8 +1064,10 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     if (warp == G::NSW + G::NPW + G::NQW) {
         // ============================================================ PRODUCER
         if (lane != 0) return;
-        const uint32_t tx_bytes = uint32_t((has_z ? 3 : 2) * TC * G::WB) +
+        const int xrows = conv ? TC + kConvHalo : TC;
+        const uint32_t tx_bytes = uint32_t((xrows + (has_z ? 2 : 1) * TC) * G::WB) +
                                   (p.tma_bc ? uint32_t((summary ? 1 : 2) * TC * N * ES) : 0u);
+        const uint32_t xcbs = conv ? cbsx : uint32_t(TC * RS);
         int s = 0;
         uint32_t use = 0;  // how often stage s was filled before
         int64_t issued = 0;
@@ -1054,7 +1083,10 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
             for (int cb = 0; cb < NB; ++cb) {
                 const int x = int(d0) + cb * (RS / ES);
                 const uint32_t o = uint32_t(cb * TC * RS);
-                tma_load_3d(smem_u32(raw_u(s) + o), &tm_u, x, t0, int(b), bar);
+                // the x tile of the prologue starts kConvHalo steps early (rows
+                // before step 0 read as zeros: the causal padding)
+                tma_load_3d(smem_u32(raw_u(s) + cb * xcbs), &tm_u, x, conv ? t0 - kConvHalo : t0,
+                            int(b), bar);
                 tma_load_3d(smem_u32(raw_dt(s) + o), &tm_dt, x, t0, int(b), bar);
                 if (has_z) tma_load_3d(smem_u32(raw_z(s) + o), &tm_z, x, t0, int(b), bar);
             }
@@ -1085,6 +1117,20 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
             bias2[k] = (p.bias != nullptr && d < dim) ? p.bias[d] : 0.f;
         }
         const float2 b2 = make_float2(bias2[0], bias2[1]);
+        // Prologue taps of the two channels, aligned to the last conv_k rows of
+        // the kMaxConvK-row window ending at the step (missing taps are 0).
+        float cw[2][kMaxConvK], cbias[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int64_t d = d0 + 2 * pp + k;
+            const bool okd = conv && d < dim;
+#pragma unroll
+            for (int j = 0; j < kMaxConvK; ++j) {
+                const int tap = j - (kMaxConvK - p.conv_k);
+                cw[k][j] = (okd && tap >= 0) ? p.conv_w[d * p.conv_k + tap] : 0.f;
+            }
+            cbias[k] = (okd && p.conv_b != nullptr) ? p.conv_b[d] : 0.f;
+        }
         const T* gB = static_cast<const T*>(p.B);
         const T* gC = static_cast<const T*>(p.C);
         const bool bc_vec = p.tma_bc && N == NP && (N % 4) == 0;
@@ -1136,13 +1182,30 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
             const unsigned char* ru = raw_u(s);
             const unsigned char* rdt = raw_dt(s);
             float2* const sdd = s_dd(bf);
+            float2* const su2 = s_u(bf);
 #pragma unroll
             for (int it = 0; it < ITEMS; ++it) {
                 const int t = tq0 + it * TSTEP;
                 const uint32_t o = TT::off(t, 2 * pp * ES, TC);
                 float xr[2], uu[2];
                 ld_k<T, 2>(rdt + o, xr);
-                ld_k<T, 2>(ru + o, uu);
+                if (conv) {
+                    // u = silu(causal conv): rows t .. t + kConvHalo of the x
+                    // tile are steps t - kConvHalo .. t of the chunk
+                    float2 acc = make_float2(cbias[0], cbias[1]);
+#pragma unroll
+                    for (int j = 0; j < kMaxConvK; ++j) {
+                        float xv[2];
+                        ld_k<T, 2>(ru + TT::off_cbs(t + j, 2 * pp * ES, cbsx), xv);
+                        acc = __ffma2_rn(make_float2(cw[0][j], cw[1][j]), make_float2(xv[0], xv[1]), acc);
+                    }
+                    const float2 uv = Act<T>::silu2(acc);
+                    uu[0] = uv.x;
+                    uu[1] = uv.y;
+                    if constexpr (!summary) su2[t * (DT / 2) + pp] = uv;
+                } else {
+                    ld_k<T, 2>(ru + o, uu);
+                }
                 float2 x = __fadd2_rn(make_float2(xr[0], xr[1]), b2);
                 if (p.softplus) x = Act<T>::softplus2(x);
                 const float2 xu = __fmul2_rn(x, make_float2(uu[0], uu[1]));
@@ -1200,7 +1263,13 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
                 for (int sgi = 1; sgi < WS; ++sgi)
                     acc = __fadd2_rn(acc, *reinterpret_cast<const float2*>(part + (sgi * TC + t) * DT + 2 * pp));
                 float uu[2];
-                ld_k<T, 2>(ru + o, uu);
+                if (conv) {
+                    const float2 uv = s_u(bf)[t * (DT / 2) + pp];
+                    uu[0] = uv.x;
+                    uu[1] = uv.y;
+                } else {
+                    ld_k<T, 2>(ru + o, uu);
+                }
                 float2 g = make_float2(1.f, 1.f);
                 if (has_z) {
                     float zz[2];
@@ -1415,9 +1484,9 @@ size_t smem_bytes(int64_t N, int stages, int TC) {
 }
 
 template <typename T, int NPT, int WS, bool SUM = false>
-size_t smem_bytes_w(int64_t N, int stages, int TC) {
-    if (TC == 16) return LayoutW<T, NPT, WS, 16, SUM>(N, stages).total + 1024;
-    return LayoutW<T, NPT, WS, 32, SUM>(N, stages).total + 1024;
+size_t smem_bytes_w(int64_t N, int stages, int TC, bool conv = false) {
+    if (TC == 16) return LayoutW<T, NPT, WS, 16, SUM>(N, stages, conv).total + 1024;
+    return LayoutW<T, NPT, WS, 32, SUM>(N, stages, conv).total + 1024;
 }
 
 #define SSM_FOR_EACH_VARIANT(X)                            \
@@ -1444,9 +1513,9 @@ size_t variant_smem(int npt, int ws, int64_t N, int stages, int TC) {
 }
 
 template <typename T>
-size_t variant_smem_w(int npt, int ws, int64_t N, int stages, int TC) {
+size_t variant_smem_w(int npt, int ws, int64_t N, int stages, int TC, bool conv = false) {
 #define SSM_SMEM_W(NPT_, WS_) \
-    if (npt == NPT_ && ws == WS_) return smem_bytes_w<T, NPT_, WS_>(N, stages, TC);
+    if (npt == NPT_ && ws == WS_) return smem_bytes_w<T, NPT_, WS_>(N, stages, TC, conv);
     SSM_FOR_EACH_VARIANT(SSM_SMEM_W)
 #undef SSM_SMEM_W
     return 0;
@@ -1458,7 +1527,7 @@ constexpr size_t kWsSmemTarget = 60 * 1024;
 template <typename T>
 Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, const void* dt,
                const void* z, const void* y, const void* Bp, const void* Cp,
-               bool allow_tma = true) {
+               bool allow_tma = true, bool conv = false) {
     const size_t es = sizeof(T);
     Plan pl;
     const int64_t channels = batch * dim;
@@ -1498,20 +1567,23 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
     const int ft = g_force_chunk.load();
     const int fs = g_force_stages.load();
     // The warp-specialised kernel wherever its tiles can move by TMA.
-    pl.ws = pl.tma_udz && g_force_kernel.load() != 1 &&
-            variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 16) <= kMaxSmem;
+    // (The convolution prologue exists only in the warp-specialised kernel.)
+    pl.ws = pl.tma_udz && (conv || g_force_kernel.load() != 1) &&
+            variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 16, conv) <= kMaxSmem;
     if (pl.ws) {
         pl.NT = (wc * pl.WS + 5) * 32;  // + 2 prepare, 2 finish and 1 producer warp
-        pl.TC = (ft == 32 && variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 32) <= kMaxSmem) ? 32 : 16;
+        pl.TC = (ft == 32 && variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 32, conv) <= kMaxSmem) ? 32
+                                                                                        : 16;
         // The deepest ring (chunks in flight) within the footprint target.
         pl.stages = 2;
         for (int st : {6, 5, 4, 3})
-            if (variant_smem_w<T>(pl.NPT, pl.WS, N, st, pl.TC) <= kWsSmemTarget) {
+            if (variant_smem_w<T>(pl.NPT, pl.WS, N, st, pl.TC, conv) <= kWsSmemTarget) {
                 pl.stages = st;
                 break;
             }
-        if (fs != 0 && variant_smem_w<T>(pl.NPT, pl.WS, N, fs, pl.TC) <= kMaxSmem) pl.stages = fs;
-        pl.smem = variant_smem_w<T>(pl.NPT, pl.WS, N, pl.stages, pl.TC);
+        if (fs != 0 && variant_smem_w<T>(pl.NPT, pl.WS, N, fs, pl.TC, conv) <= kMaxSmem)
+            pl.stages = fs;
+        pl.smem = variant_smem_w<T>(pl.NPT, pl.WS, N, pl.stages, pl.TC, conv);
     } else {
         // Chunk length: 32 steps unless the grid does not fit in one wave of
         // blocks at that footprint (then 16 steps: half the shared memory).
@@ -1585,7 +1657,7 @@ template <typename T, int NPT, int WS, int TC, bool SUMMARY>
 int launch_one_w(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
     using G = GeoW<T, NPT, WS, TC>;
     auto kern = ssm_scan_ws_kernel<T, NPT, WS, TC, SUMMARY>;
-    const size_t smem = smem_bytes_w<T, NPT, WS, SUMMARY>(kp.N, kp.stages, TC);
+    const size_t smem = smem_bytes_w<T, NPT, WS, SUMMARY>(kp.N, kp.stages, TC, kp.conv_k > 0);
     static std::atomic<size_t> configured[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_LAUNCH;
@@ -1679,13 +1751,16 @@ template <typename T>
 int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C, const float* D,
              const T* z, const float* delta_bias, int softplus_flag, T* y, float* h_last,
              int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream,
-             bool fixed_scratch = false, const float* h0 = nullptr) {
+             bool fixed_scratch = false, const float* h0 = nullptr,
+             const float* conv_w = nullptr, const float* conv_b = nullptr, int conv_k = 0) {
     if (batch < 0 || L < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
     // A pointer may be NULL only when its tensor has no elements.
     if ((batch > 0 && L > 0 && dim > 0) && (!u || !delta || !y)) return SSM_ERR_NULL;
     if ((batch > 0 && L > 0) && (!B || !C)) return SSM_ERR_NULL;
     if (dim > 0 && !A) return SSM_ERR_NULL;
     if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED_N;
+    if (conv_k < 0 || conv_k > kMaxConvK) return SSM_ERR_SIZE;
+    if (conv_k > 0 && dim > 0 && !conv_w) return SSM_ERR_NULL;
     const size_t es = sizeof(T);
     int64_t n_bld, n_bln, n_dn, n_bdn, tmp;
     if (!mul_ok(batch, L, &tmp) || !mul_ok(tmp, dim, &n_bld) || !mul_ok(tmp, N, &n_bln) ||
@@ -1696,13 +1771,15 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
                             (const void*)z, (const void*)y})
         if (ptr && !aligned(ptr, es)) return SSM_ERR_ALIGN;
     for (const void* ptr : {(const void*)A, (const void*)D, (const void*)delta_bias,
-                            (const void*)h_last, (const void*)h0})
+                            (const void*)h_last, (const void*)h0, (const void*)conv_w,
+                            (const void*)conv_b})
         if (ptr && !aligned(ptr, 4)) return SSM_ERR_ALIGN;
     // Outputs must not overlap inputs or each other.
     const int64_t by = n_bld * int64_t(es), bh = n_bdn * 4;
     const struct { const void* p; int64_t n; } ins[] = {
         {u, by}, {delta, by}, {z, z ? by : 0}, {B, n_bln * int64_t(es)}, {C, n_bln * int64_t(es)},
-        {A, n_dn * 4}, {D, D ? dim * 4 : 0}, {delta_bias, delta_bias ? dim * 4 : 0}};
+        {A, n_dn * 4}, {D, D ? dim * 4 : 0}, {delta_bias, delta_bias ? dim * 4 : 0},
+        {conv_w, conv_w ? dim * conv_k * 4 : 0}, {conv_b, conv_b ? dim * 4 : 0}};
     for (const auto& in : ins) {
         if (overlaps(y, by, in.p, in.n)) return SSM_ERR_ALIAS;
         if (overlaps(h_last, bh, in.p, in.n)) return SSM_ERR_ALIAS;
@@ -1712,8 +1789,12 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     if (overlaps(h0, bh, y, by) || overlaps(h0, bh, h_last, bh)) return SSM_ERR_ALIAS;
     if (batch == 0 || dim == 0) return SSM_OK;  // nothing to compute
 
-    Plan pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C);
+    const bool conv = conv_k > 0;
+    Plan pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C, true, conv);
     if (pl.grid * pl.n_seg > int64_t(0x7fffffff)) return SSM_ERR_SIZE;
+    // The prologue runs in the warp-specialised kernel, which needs rows TMA
+    // can describe; with L = 0 there is nothing to convolve.
+    if (conv && L > 0 && !pl.ws) return SSM_ERR_ALIGN;
 
     CUtensorMap tms[6];
     std::memset(tms, 0, sizeof(tms));
@@ -1722,7 +1803,8 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
         const auto ty = Elt<T>::tmap_type;
         const int box = pl.row_span / int(es);
         const auto swz = swizzle_for(pl.row_span);
-        tma_udz = encode3d(&tms[0], ty, es, u, dim, L, batch, box, pl.TC, swz) &&
+        tma_udz = encode3d(&tms[0], ty, es, u, dim, L, batch, box,
+                           pl.TC + (conv ? kConvHalo : 0), swz) &&
                   encode3d(&tms[1], ty, es, delta, dim, L, batch, box, pl.TC, swz) &&
                   encode3d(&tms[2], ty, es, z ? z : u, dim, L, batch, box, pl.TC, swz) &&
                   encode3d(&tms[5], ty, es, y, dim, L, batch, box, pl.TC, swz);
@@ -1733,6 +1815,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
                               CU_TENSOR_MAP_SWIZZLE_NONE);
         if (!tma_udz) tma_bc = false;
         if (!tma_udz) {
+            if (conv) return SSM_ERR_ALIGN;
             // The tensor maps could not be encoded: plan again for plain loads.
             pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C, /*allow_tma=*/false);
             tma_bc = false;
@@ -1767,6 +1850,9 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     kp.hseg = nullptr;
     kp.sseg = nullptr;
     kp.h0 = h0;
+    kp.conv_w = conv_w;
+    kp.conv_b = conv_b;
+    kp.conv_k = conv ? conv_k : 0;
     if (pl.n_seg == 1) return dispatch<T>(pl, pl.grid, tms, kp, stream);
 
     // Segment summaries live in stream-ordered scratch from the device's
@@ -1895,6 +1981,31 @@ int ssm_scan_fwd_bf16_h0(const uint16_t* u, const uint16_t* delta, const float* 
                         reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
                         reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
                         reinterpret_cast<bf*>(y), h_last, batch, L, dim, N, stream, false, h0);
+}
+
+int ssm_conv_scan_fwd(const float* x, const float* conv_w, const float* conv_b, int conv_k,
+                      const float* delta, const float* A, const float* B, const float* C,
+                      const float* D, const float* z, const float* delta_bias, int softplus_flag,
+                      float* y, float* h_last, int64_t batch, int64_t L, int64_t dim, int64_t N,
+                      cudaStream_t stream) {
+    if (conv_k < 1) return SSM_ERR_SIZE;
+    return scan_fwd<float>(x, delta, A, B, C, D, z, delta_bias, softplus_flag, y, h_last, batch,
+                           L, dim, N, stream, false, nullptr, conv_w, conv_b, conv_k);
+}
+
+int ssm_conv_scan_fwd_bf16(const uint16_t* x, const float* conv_w, const float* conv_b,
+                           int conv_k, const uint16_t* delta, const float* A, const uint16_t* B,
+                           const uint16_t* C, const float* D, const uint16_t* z,
+                           const float* delta_bias, int softplus_flag, uint16_t* y,
+                           float* h_last, int64_t batch, int64_t L, int64_t dim, int64_t N,
+                           cudaStream_t stream) {
+    using bf = __nv_bfloat16;
+    if (conv_k < 1) return SSM_ERR_SIZE;
+    return scan_fwd<bf>(reinterpret_cast<const bf*>(x), reinterpret_cast<const bf*>(delta), A,
+                        reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
+                        reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
+                        reinterpret_cast<bf*>(y), h_last, batch, L, dim, N, stream, false,
+                        nullptr, conv_w, conv_b, conv_k);
 }
 
 int ssm_scan_step(const float* u, const float* delta, const float* A, const float* B,

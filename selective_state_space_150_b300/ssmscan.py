@@ -47,6 +47,7 @@ SSM_KNOB_KERNEL = 8
 
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc",
             "ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0", "ssm_scan_step", "ssm_scan_step_bf16",
+            "ssm_conv_scan_fwd", "ssm_conv_scan_fwd_bf16",
             "ssm_scan_last_device_status", "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
 
 _vp = ctypes.c_void_p
@@ -58,6 +59,9 @@ for _name in ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc"):
     getattr(_lib, _name).restype = ctypes.c_int
 for _name in ("ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0"):
     getattr(_lib, _name).argtypes = _FWD_ARGS[:8] + [_vp] + _FWD_ARGS[8:]
+    getattr(_lib, _name).restype = ctypes.c_int
+for _name in ("ssm_conv_scan_fwd", "ssm_conv_scan_fwd_bf16"):
+    getattr(_lib, _name).argtypes = [_vp, _vp, _vp, ctypes.c_int] + _FWD_ARGS[1:]
     getattr(_lib, _name).restype = ctypes.c_int
 for _name in ("ssm_scan_step", "ssm_scan_step_bf16"):
     getattr(_lib, _name).argtypes = [_vp] * 8 + [ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _vp]
@@ -121,6 +125,25 @@ def ssm_scan_fwd_bf16_h0(u, delta, A, B, C, D, z, delta_bias, h0, softplus_flag,
                                      D or None, z or None, delta_bias or None, h0 or None,
                                      int(softplus_flag), y or None, h_last or None, batch, L,
                                      dim, N, stream or None)
+
+
+def ssm_conv_scan_fwd(x, conv_w, conv_b, conv_k, delta, A, B, C, D, z, delta_bias,
+                      softplus_flag, y, h_last, batch, L, dim, N, stream) -> int:
+    """fp32 scan with the causal conv + SiLU prologue; pointers are ints."""
+    return _lib.ssm_conv_scan_fwd(x or None, conv_w or None, conv_b or None, int(conv_k),
+                                  delta or None, A or None, B or None, C or None, D or None,
+                                  z or None, delta_bias or None, int(softplus_flag), y or None,
+                                  h_last or None, batch, L, dim, N, stream or None)
+
+
+def ssm_conv_scan_fwd_bf16(x, conv_w, conv_b, conv_k, delta, A, B, C, D, z, delta_bias,
+                           softplus_flag, y, h_last, batch, L, dim, N, stream) -> int:
+    """bf16 scan with the causal conv + SiLU prologue; pointers are ints."""
+    return _lib.ssm_conv_scan_fwd_bf16(x or None, conv_w or None, conv_b or None, int(conv_k),
+                                       delta or None, A or None, B or None, C or None, D or None,
+                                       z or None, delta_bias or None, int(softplus_flag),
+                                       y or None, h_last or None, batch, L, dim, N,
+                                       stream or None)
 
 
 def ssm_scan_step(u, delta, A, B, C, D, z, delta_bias, softplus_flag, h, y, batch, dim, N,
@@ -214,6 +237,34 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softp
         st = fn(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                 _ptr(delta_bias), _ptr(h0), int(bool(softplus)), _ptr(y), _ptr(h_last),
                 batch, L, dim, N, int(stream))
+    if st != SSM_OK:
+        raise SSMError(st, fn.__name__)
+    return y, h_last
+
+
+def conv_selective_scan_fwd(x, conv_w, conv_b, delta, A, B, C, D=None, z=None, delta_bias=None,
+                            softplus=False, y=None, h_last=None, stream=None):
+    """The scan of u = silu(causal depthwise conv1d(x) + conv_b) on torch CUDA
+    tensors; conv_w: (dim, K) fp32, K <= 4; conv_b: (dim,) fp32 or None.
+    Returns (y, h_last)."""
+    import torch
+
+    bf16 = _check_io(x, delta, B, C, z, A, D, delta_bias)
+    for t in (conv_w, conv_b):
+        if t is not None and (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()):
+            raise TypeError("conv_w, conv_b must be contiguous float32 CUDA tensors")
+    batch, L, dim = x.shape
+    N = A.shape[1]
+    if y is None:
+        y = torch.empty_like(x)
+    if h_last is None:
+        h_last = torch.empty((batch, dim, N), dtype=torch.float32, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    fn = ssm_conv_scan_fwd_bf16 if bf16 else ssm_conv_scan_fwd
+    st = fn(_ptr(x), _ptr(conv_w), _ptr(conv_b), conv_w.shape[1], _ptr(delta), _ptr(A), _ptr(B),
+            _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)), _ptr(y),
+            _ptr(h_last), batch, L, dim, N, int(stream))
     if st != SSM_OK:
         raise SSMError(st, fn.__name__)
     return y, h_last

@@ -192,3 +192,22 @@ def test_step_checks(fn):
     assert step(fn, y=P) == ssmscan.SSM_ERR_ALIAS                     # y is u
     assert step(fn, h=Q + 2) == ssmscan.SSM_ERR_ALIGN
     assert step(fn, batch=0) == ssmscan.SSM_OK and step(fn, dim=0) == ssmscan.SSM_OK
+
+
+# ---------------------------------------------------------------- conv prologue
+def conv_fwd(fn, **kw):
+    args = dict(x=P, conv_w=P + 0x600000, conv_b=0, conv_k=4, delta=P + 0x100000,
+                A=P + 0x200000, B=P + 0x300000, C=P + 0x400000, D=0, z=0, delta_bias=0,
+                softplus_flag=0, y=Q, h_last=0, batch=2, L=8, dim=16, N=4, stream=0)
+    args.update(kw)
+    return fn(**args)
+
+
+@pytest.mark.parametrize("fn", [ssm.ssm_conv_scan_fwd, ssm.ssm_conv_scan_fwd_bf16])
+def test_conv_checks(fn):
+    assert conv_fwd(fn, conv_k=0) == ssmscan.SSM_ERR_SIZE
+    assert conv_fwd(fn, conv_k=5) == ssmscan.SSM_ERR_SIZE
+    assert conv_fwd(fn, conv_w=0) == ssmscan.SSM_ERR_NULL
+    assert conv_fwd(fn, conv_w=P + 0x600002) == ssmscan.SSM_ERR_ALIGN
+    assert conv_fwd(fn, y=P + 0x600000) == ssmscan.SSM_ERR_ALIAS     # y over the taps
+    assert conv_fwd(fn, batch=0) == ssmscan.SSM_OK
