@@ -463,6 +463,125 @@ def run_ours(args, wl, world, rank, local):
     return line
 
 
+def _events_mean_ms(fn, reps, stream):
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for i, (a, b) in enumerate(ev):
+        a.record(stream)
+        fn(i)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def run_op(args, wl):
+    """Secondary operations on one workload's shape, one JSON line each:
+    conv_scan  the scan with the fused causal conv1d + SiLU prologue, timed
+               beside the plain scan on the same inputs;
+    step       the one-token recurrent step over (batch, dim, N) states,
+               timed through a CUDA graph of 100 steps (device time only)."""
+    import torch
+    import selective_state_space_150_b300 as ssm
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    inp = W.make_inputs(wl, seed=0)
+    bf = wl.dtype == "bf16"
+
+    def dev(a):
+        if a is None:
+            return None
+        t = (torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16
+             else torch.from_numpy(a))
+        return t.cuda()
+
+    rng = np.random.default_rng(1)
+    es = 2 if bf else 4
+    hbm_gbs, hbm_src = measured_peaks()
+    if args.op == "conv_scan":
+        sets = [{k: dev(inp[k]) for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}
+                for _ in range(2)]
+        w = torch.from_numpy((0.5 * rng.standard_normal((wl.dim, 4))).astype(np.float32)).cuda()
+        cb = torch.from_numpy((0.1 * rng.standard_normal(wl.dim)).astype(np.float32)).cuda()
+        outs = [(torch.empty_like(s["u"]),
+                 torch.empty((wl.batch, wl.dim, wl.N), dtype=torch.float32, device="cuda"))
+                for s in sets]
+
+        def conv_call(i):
+            s, (y, h) = sets[i & 1], outs[i & 1]
+            ssm.conv_selective_scan_fwd(s["u"], w, cb, s["delta"], s["A"], s["B"], s["C"], s["D"],
+                                        s["z"], s["delta_bias"], wl.softplus, y=y, h_last=h)
+
+        def scan_call(i):
+            s, (y, h) = sets[i & 1], outs[i & 1]
+            ssm.selective_scan_fwd(s["u"], s["delta"], s["A"], s["B"], s["C"], s["D"], s["z"],
+                                   s["delta_bias"], wl.softplus, y=y, h_last=h)
+
+        for i in range(args.warmup):
+            conv_call(i)
+            scan_call(i)
+        torch.cuda.synchronize()
+        ms_conv = _events_mean_ms(conv_call, args.steps, stream)
+        ms_scan = _events_mean_ms(scan_call, args.steps, stream)
+        st = ssm.ssm_scan_last_device_status(stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(ssm.ssm_status_string(st))
+        bytes_launch = algorithmic_bytes(wl) + wl.dim * 5 * 4
+        # a separate conv kernel would read x and write u once more
+        unfused_extra = 2 * es * wl.batch * wl.L * wl.dim
+        return {
+            "op": "conv_scan", "metric": "selective-scan fwd with causal conv1d(k=4)+SiLU "
+            "prologue tokens/s", "value": wl.tokens / (ms_conv * 1e-3), "unit": "tokens/s",
+            "higher_is_better": True, "ms_per_step": ms_conv, "steps": args.steps,
+            "warmup": args.warmup, "plain_scan_ms": ms_scan,
+            "prologue_cost_ms": ms_conv - ms_scan,
+            "unfused_conv_floor_ms": unfused_extra / (hbm_gbs * 1e9) * 1e3,
+            "hbm": {"achieved_gbs": bytes_launch / (ms_conv * 1e-3) / 1e9, "peak_gbs": hbm_gbs,
+                    "frac": bytes_launch / (ms_conv * 1e-3) / 1e9 / hbm_gbs,
+                    "peak_source": hbm_src},
+            "dtype": "f32", "data": "synthetic (seeded; see ssm_workloads.py)",
+            "config": config_of(wl, "inputs rotate over 2 resident copies"), "impl": "ours"}
+    # one-token step over the workload's (batch, dim, N) states
+    tok = {k: (None if inp[k] is None else dev(inp[k][:, 0].copy()) if inp[k].ndim == 3
+               else dev(inp[k])) for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}
+    h = torch.zeros((wl.batch, wl.dim, wl.N), dtype=torch.float32, device="cuda")
+    y = torch.empty_like(tok["u"])
+
+    def step_call():
+        ssm.selective_scan_step(tok["u"], tok["delta"], tok["A"], tok["B"], tok["C"], h,
+                                tok["D"], tok["z"], tok["delta_bias"], wl.softplus, y=y)
+
+    for _ in range(args.warmup):
+        step_call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(100):
+            step_call()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, args.steps // 20)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / (reps * 100)
+    state_bytes = wl.batch * wl.dim * wl.N * 8 + wl.dim * wl.N * 4
+    return {
+        "op": "step", "metric": "one-token recurrent step latency", "value": us, "unit": "us",
+        "higher_is_better": False, "tokens_per_s": wl.batch / (us * 1e-6),
+        "steps_timed": reps * 100,
+        "hbm": {"achieved_gbs": state_bytes / (us * 1e-6) / 1e9, "peak_gbs": hbm_gbs,
+                "frac": state_bytes / (us * 1e-6) / 1e9 / hbm_gbs, "peak_source": hbm_src},
+        "timing": "CUDA graph of 100 steps, device time per step",
+        "dtype": "f32", "data": "synthetic (seeded; see ssm_workloads.py)",
+        "config": {"workload": wl.name, "batch": wl.batch, "dim": wl.dim, "N": wl.N,
+                   "io_dtype": wl.dtype}, "impl": "ours"}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -478,6 +597,8 @@ def main(argv=None):
                     help="wall seconds of oracle work per reference step")
     ap.add_argument("--clock-window", type=float, default=0.5)
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--op", choices=["scan", "conv_scan", "step"], default="scan",
+                    help="scan (the headline); conv_scan / step: secondary lines")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -489,6 +610,11 @@ def main(argv=None):
         for n in names:
             line = run_reference(args, W.WORKLOADS[n])
             print(json.dumps(line), flush=True)
+        return 0
+
+    if args.op != "scan":
+        for n in names:
+            print(json.dumps(run_op(args, W.WORKLOADS[n])), flush=True)
         return 0
 
     world, rank, local = dist_init()

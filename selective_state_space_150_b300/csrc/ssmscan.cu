@@ -1107,9 +1107,11 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
 
     if (warp < G::NSW + G::NPW) {
         // ============================================================= PREPARE
-        constexpr int NPR = G::NPR, ITEMS = G::ITEMS_P, TSTEP = NPR / NPAIR;
+        constexpr int NPR = G::NPR, ITEMS = G::ITEMS_P;
         const int pt = tid - G::NS;  // 0 .. NPR-1
-        const int pp = pt % NPAIR, tq0 = pt / NPAIR;
+        // channel pair pp, steps tq0 .. tq0 + ITEMS - 1 (consecutive, so the
+        // prologue's convolution window slides by one row per step)
+        const int pp = pt % NPAIR, tq0 = (pt / NPAIR) * ITEMS;
         float bias2[2];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -1183,22 +1185,34 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
             const unsigned char* rdt = raw_dt(s);
             float2* const sdd = s_dd(bf);
             float2* const su2 = s_u(bf);
+            // x rows t .. t + kConvHalo of the x tile are steps t - kConvHalo ..
+            // t of the chunk; xw holds the window, oldest first
+            float2 xw[kMaxConvK];
+            if (conv) {
+#pragma unroll
+                for (int j = 0; j < kMaxConvK - 1; ++j) {
+                    float xv[2];
+                    ld_k<T, 2>(ru + TT::off_cbs(tq0 + j, 2 * pp * ES, cbsx), xv);
+                    xw[j + 1] = make_float2(xv[0], xv[1]);
+                }
+            }
 #pragma unroll
             for (int it = 0; it < ITEMS; ++it) {
-                const int t = tq0 + it * TSTEP;
+                const int t = tq0 + it;
                 const uint32_t o = TT::off(t, 2 * pp * ES, TC);
                 float xr[2], uu[2];
                 ld_k<T, 2>(rdt + o, xr);
                 if (conv) {
-                    // u = silu(causal conv): rows t .. t + kConvHalo of the x
-                    // tile are steps t - kConvHalo .. t of the chunk
+                    // u = silu(causal conv) over the window ending at step t
+                    float xv[2];
+                    ld_k<T, 2>(ru + TT::off_cbs(t + kConvHalo, 2 * pp * ES, cbsx), xv);
+#pragma unroll
+                    for (int j = 0; j < kMaxConvK - 1; ++j) xw[j] = xw[j + 1];
+                    xw[kMaxConvK - 1] = make_float2(xv[0], xv[1]);
                     float2 acc = make_float2(cbias[0], cbias[1]);
 #pragma unroll
-                    for (int j = 0; j < kMaxConvK; ++j) {
-                        float xv[2];
-                        ld_k<T, 2>(ru + TT::off_cbs(t + j, 2 * pp * ES, cbsx), xv);
-                        acc = __ffma2_rn(make_float2(cw[0][j], cw[1][j]), make_float2(xv[0], xv[1]), acc);
-                    }
+                    for (int j = 0; j < kMaxConvK; ++j)
+                        acc = __ffma2_rn(make_float2(cw[0][j], cw[1][j]), xw[j], acc);
                     const float2 uv = Act<T>::silu2(acc);
                     uu[0] = uv.x;
                     uu[1] = uv.y;
