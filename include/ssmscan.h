@@ -188,6 +188,39 @@ SSM_API int ssm_conv_scan_fwd_bf16(const uint16_t *x, const float *conv_w, const
                       int64_t N, cudaStream_t stream);
 
 /*
+ * The scan on HOST buffers, for callers whose data lives in host memory: the
+ * inputs are copied to the device, the scan runs, and y and h_last are copied
+ * back, with the copies of one part of the problem overlapping the scan of
+ * another (parts are groups of batch rows; with fewer than 4 rows, pieces of
+ * the sequence chained through the state).  Every array argument (u, delta,
+ * A, B, C, D, z, delta_bias, y, h_last) is a HOST pointer with the layout of
+ * ssm_scan_fwd; page-locked (pinned) memory lets the copies run
+ * asynchronously.  workspace is a DEVICE buffer of at least
+ * ssm_scan_host_workspace_bytes(batch, L, dim, N, dtype) bytes (dtype 0 =
+ * fp32, 1 = bf16), 256-byte aligned, owned by the caller; it must not be in
+ * use by another call.  The call enqueues everything behind the work already
+ * on `stream` and makes `stream` wait for the last copy back: y and h_last
+ * are valid after `stream` synchronises.  The library creates and destroys
+ * three streams and some events per call.  Results match ssm_scan_fwd within
+ * the tolerances above (a part may be planned differently from the whole).
+ * Returns SSM_ERR_SIZE if workspace_bytes is too small.
+ */
+SSM_API int64_t ssm_scan_host_workspace_bytes(int64_t batch, int64_t L, int64_t dim, int64_t N,
+                                              int dtype);
+SSM_API int ssm_scan_fwd_host(const float *u, const float *delta, const float *A,
+                      const float *B, const float *C, const float *D,
+                      const float *z, const float *delta_bias, int softplus_flag,
+                      float *y, float *h_last, int64_t batch, int64_t L, int64_t dim,
+                      int64_t N, void *workspace, int64_t workspace_bytes,
+                      cudaStream_t stream);
+SSM_API int ssm_scan_fwd_bf16_host(const uint16_t *u, const uint16_t *delta, const float *A,
+                      const uint16_t *B, const uint16_t *C, const float *D,
+                      const uint16_t *z, const float *delta_bias, int softplus_flag,
+                      uint16_t *y, float *h_last, int64_t batch, int64_t L, int64_t dim,
+                      int64_t N, void *workspace, int64_t workspace_bytes,
+                      cudaStream_t stream);
+
+/*
  * One recurrent (decode) step for every channel: the scan at L = 1 from the
  * state h, which is updated in place.
  *   u, delta, z, y : (batch, dim)      B, C : (batch, N)

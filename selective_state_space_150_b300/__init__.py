@@ -12,6 +12,9 @@ from .ssmscan import (  # noqa: F401
     ssm_conv_scan_fwd_bf16,
     ssm_scan_fwd,
     ssm_scan_fwd_bf16,
+    ssm_scan_fwd_bf16_host,
+    ssm_scan_fwd_host,
+    ssm_scan_host_workspace_bytes,
     ssm_scan_fwd_bf16_noalloc,
     ssm_scan_fwd_bf16_h0,
     ssm_scan_fwd_h0,

@@ -1953,6 +1953,194 @@ int scan_step(const T* u, const T* delta, const float* A, const T* B, const T* C
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
+// ----------------------------------------------------------- host-buffer calls
+// The scan on host buffers: inputs go up, the scan runs and y, h_last come
+// back, overlapped across parts of the problem on three streams (uploads,
+// compute, downloads) so that copies in both directions and the kernels run
+// at the same time.  Parts are groups of batch rows, or, for fewer than
+// kMinRowParts rows, pieces of the sequence chained through the state (the
+// piece k + 1 starts from piece k's h_last).  Device memory is the caller's
+// workspace: the small per-channel vectors plus kHostSlots slots of one part.
+constexpr int kHostSlots = 2;
+constexpr int kMaxParts = 8;
+constexpr int kMinRowParts = 4;
+
+struct HostSplit {
+    bool by_rows;
+    int parts;
+    int64_t rows;  // batch rows per part (by_rows)
+    int64_t len;   // steps per piece (by time)
+};
+
+HostSplit host_split(int64_t batch, int64_t L) {
+    HostSplit hs{};
+    if (batch >= kMinRowParts) {
+        hs.by_rows = true;
+        hs.parts = int(std::min<int64_t>(batch, kMaxParts));
+        hs.rows = (batch + hs.parts - 1) / hs.parts;
+        hs.parts = int((batch + hs.rows - 1) / hs.rows);
+        hs.len = L;
+    } else {
+        hs.by_rows = false;
+        const int64_t want = std::min<int64_t>(kMaxParts, std::max<int64_t>(1, L / 1024));
+        hs.len = (L + want - 1) / want;
+        hs.len = (hs.len + 31) / 32 * 32;  // whole 32-step chunks
+        if (hs.len < 1) hs.len = 1;
+        hs.parts = int(std::max<int64_t>(1, (L + hs.len - 1) / hs.len));
+        hs.rows = batch;
+    }
+    return hs;
+}
+
+struct HostLayout {
+    size_t dvec, bias, slot0;             // D, delta_bias, first slot (A sits at 0)
+    size_t u, dt, z, b, c, y, h, slot;    // offsets within a slot; slot size
+    size_t total;
+};
+
+HostLayout host_layout(int64_t batch, int64_t L, int64_t dim, int64_t N, size_t es, bool has_z,
+                       bool has_d, bool has_bias) {
+    const HostSplit hs = host_split(batch, L);
+    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+    HostLayout ly{};
+    const size_t rows = size_t(hs.rows), len = size_t(hs.len);
+    ly.dvec = al(size_t(dim * N) * 4);
+    ly.bias = ly.dvec + (has_d ? al(size_t(dim) * 4) : 0);
+    size_t o = ly.bias + (has_bias ? al(size_t(dim) * 4) : 0);
+    // a slot: u, delta, z, B, C, y for one part and its h_last
+    const size_t ud = al(rows * len * size_t(dim) * es), bc = al(rows * len * size_t(N) * es);
+    const size_t hh = al(rows * size_t(dim * N) * 4);
+    ly.u = 0;
+    ly.dt = ud;
+    ly.z = 2 * ud;
+    ly.b = (has_z ? 3 : 2) * ud;
+    ly.c = ly.b + bc;
+    ly.y = ly.c + bc;
+    ly.h = ly.y + ud;
+    ly.slot = ly.h + hh;
+    ly.slot0 = o;
+    ly.total = o + size_t(kHostSlots) * ly.slot;
+    return ly;
+}
+
+template <typename T>
+int scan_fwd_host(const T* u, const T* delta, const float* A, const T* B, const T* C,
+                  const float* D, const T* z, const float* delta_bias, int softplus_flag, T* y,
+                  float* h_last, int64_t batch, int64_t L, int64_t dim, int64_t N, void* ws,
+                  int64_t ws_bytes, cudaStream_t stream) {
+    if (batch < 0 || L < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
+    if (N > SSM_MAX_N) return SSM_ERR_UNSUPPORTED_N;
+    if (batch == 0 || dim == 0) return SSM_OK;
+    if (!u || !delta || !A || !B || !C || !y || !ws) return SSM_ERR_NULL;
+    int64_t tmp;
+    if (!mul_ok(batch, L, &tmp) || !mul_ok(tmp, dim * N, &tmp)) return SSM_ERR_SIZE;
+    const size_t es = sizeof(T);
+    const HostSplit hs = host_split(batch, L);
+    const HostLayout ly = host_layout(batch, L, dim, N, es, z != nullptr, D != nullptr,
+                                      delta_bias != nullptr);
+    if (ws_bytes < int64_t(ly.total)) return SSM_ERR_SIZE;
+    if (!aligned(ws, 256)) return SSM_ERR_ALIGN;
+    unsigned char* const w = static_cast<unsigned char*>(ws);
+    float* const dA = reinterpret_cast<float*>(w);
+    float* const dD = D ? reinterpret_cast<float*>(w + ly.dvec) : nullptr;
+    float* const dBias = delta_bias ? reinterpret_cast<float*>(w + ly.bias) : nullptr;
+    auto slot = [&](int k) { return w + ly.slot0 + size_t(k) * ly.slot; };
+
+    cudaStream_t sh = nullptr, sc = nullptr, sd = nullptr;
+    cudaEvent_t ev[2 + 3 * kMaxParts] = {};
+    int st = SSM_OK;
+    auto chk = [&](cudaError_t e) {
+        if (e != cudaSuccess && st == SSM_OK) st = SSM_ERR_LAUNCH;
+        return st == SSM_OK;
+    };
+    const int nev = 2 + 3 * hs.parts;
+    if (chk(cudaStreamCreateWithFlags(&sh, cudaStreamNonBlocking)) &&
+        chk(cudaStreamCreateWithFlags(&sc, cudaStreamNonBlocking)) &&
+        chk(cudaStreamCreateWithFlags(&sd, cudaStreamNonBlocking)))
+        for (int i = 0; i < nev && st == SSM_OK; ++i)
+            chk(cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming));
+    cudaEvent_t e_start = ev[0], e_end = ev[1];
+    auto e_in = [&](int g) { return ev[2 + g]; };           // part g uploaded
+    auto e_out = [&](int g) { return ev[2 + hs.parts + g]; };  // part g computed
+    auto e_free = [&](int g) { return ev[2 + 2 * hs.parts + g]; };  // part g downloaded
+
+    const cudaMemcpyKind H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
+    if (st == SSM_OK) {
+        chk(cudaEventRecord(e_start, stream));
+        for (cudaStream_t s2 : {sh, sc, sd}) chk(cudaStreamWaitEvent(s2, e_start, 0));
+        chk(cudaMemcpyAsync(dA, A, size_t(dim * N) * 4, H2D, sh));
+        if (dD) chk(cudaMemcpyAsync(dD, D, size_t(dim) * 4, H2D, sh));
+        if (dBias) chk(cudaMemcpyAsync(dBias, delta_bias, size_t(dim) * 4, H2D, sh));
+    }
+    for (int g = 0; g < hs.parts && st == SSM_OK; ++g) {
+        unsigned char* const sl = slot(g % kHostSlots);
+        T* const su = reinterpret_cast<T*>(sl + ly.u);
+        T* const sdt = reinterpret_cast<T*>(sl + ly.dt);
+        T* const szz = z ? reinterpret_cast<T*>(sl + ly.z) : nullptr;
+        T* const sB = reinterpret_cast<T*>(sl + ly.b);
+        T* const sC = reinterpret_cast<T*>(sl + ly.c);
+        T* const sy = reinterpret_cast<T*>(sl + ly.y);
+        float* const shl = reinterpret_cast<float*>(sl + ly.h);
+        // this part: rows r0 .. r0 + nr - 1, steps t0 .. t0 + nl - 1
+        const int64_t r0 = hs.by_rows ? g * hs.rows : 0;
+        const int64_t nr = hs.by_rows ? std::min<int64_t>(hs.rows, batch - r0) : batch;
+        const int64_t t0 = hs.by_rows ? 0 : g * hs.len;
+        const int64_t nl = hs.by_rows ? L : std::min<int64_t>(hs.len, L - t0);
+        // uploads, once the slot's previous part has been downloaded
+        if (g >= kHostSlots) chk(cudaStreamWaitEvent(sh, e_free(g - kHostSlots), 0));
+        for (int64_t r = 0; r < nr && st == SSM_OK; ++r) {
+            const int64_t hrow = r0 + r;
+            const size_t dl = size_t(nl * dim) * es, nn = size_t(nl * N) * es;
+            const size_t ho = size_t((hrow * L + t0) * dim), hb = size_t((hrow * L + t0) * N);
+            const size_t dof = size_t(r * nl * dim), bof = size_t(r * nl * N);
+            chk(cudaMemcpyAsync(su + dof, u + ho, dl, H2D, sh));
+            chk(cudaMemcpyAsync(sdt + dof, delta + ho, dl, H2D, sh));
+            if (z) chk(cudaMemcpyAsync(szz + dof, z + ho, dl, H2D, sh));
+            chk(cudaMemcpyAsync(sB + bof, B + hb, nn, H2D, sh));
+            chk(cudaMemcpyAsync(sC + bof, C + hb, nn, H2D, sh));
+        }
+        chk(cudaEventRecord(e_in(g), sh));
+        // compute; a time piece starts from the previous piece's final state,
+        // which sits in the other slot (written earlier on this stream, and
+        // overwritten only by a later kernel on it)
+        chk(cudaStreamWaitEvent(sc, e_in(g), 0));
+        if (st != SSM_OK) break;
+        const float* h0 =
+            (!hs.by_rows && g > 0)
+                ? reinterpret_cast<const float*>(slot((g - 1) % kHostSlots) + ly.h)
+                : nullptr;
+        const int rc = scan_fwd<T>(su, sdt, dA, sB, sC, dD, szz, dBias, softplus_flag, sy, shl, nr,
+                                   nl, dim, N, sc, false, h0);
+        if (rc != SSM_OK && st == SSM_OK) st = rc;
+        chk(cudaEventRecord(e_out(g), sc));
+        // downloads
+        chk(cudaStreamWaitEvent(sd, e_out(g), 0));
+        for (int64_t r = 0; r < nr && st == SSM_OK; ++r) {
+            const int64_t hrow = r0 + r;
+            chk(cudaMemcpyAsync(y + size_t((hrow * L + t0) * dim), sy + size_t(r * nl * dim),
+                                size_t(nl * dim) * es, D2H, sd));
+        }
+        const bool last_piece = hs.by_rows || g == hs.parts - 1;
+        if (h_last && last_piece)
+            chk(cudaMemcpyAsync(h_last + size_t(r0 * dim * N), shl, size_t(nr * dim * N) * 4, D2H,
+                                sd));
+        chk(cudaEventRecord(e_free(g), sd));
+    }
+    if (e_end != nullptr && sd != nullptr) {
+        // join: the caller's stream continues after the last download (and
+        // after everything on the other two streams)
+        for (cudaStream_t s2 : {sh, sc, sd}) {
+            if (cudaEventRecord(e_end, s2) == cudaSuccess)
+                (void)cudaStreamWaitEvent(stream, e_end, 0);
+        }
+    }
+    for (int i = 0; i < nev; ++i)
+        if (ev[i]) (void)cudaEventDestroy(ev[i]);
+    for (cudaStream_t s2 : {sh, sc, sd})
+        if (s2) (void)cudaStreamDestroy(s2);
+    return st;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -2020,6 +2208,37 @@ int ssm_conv_scan_fwd_bf16(const uint16_t* x, const float* conv_w, const float* 
                         reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
                         reinterpret_cast<bf*>(y), h_last, batch, L, dim, N, stream, false,
                         nullptr, conv_w, conv_b, conv_k);
+}
+
+int64_t ssm_scan_host_workspace_bytes(int64_t batch, int64_t L, int64_t dim, int64_t N,
+                                      int dtype) {
+    if (batch < 0 || L < 0 || dim < 0 || N < 1 || N > SSM_MAX_N || (dtype != 0 && dtype != 1))
+        return -1;
+    const HostLayout ly = host_layout(batch, L, dim, N, dtype == 1 ? 2 : 4, true, true, true);
+    return int64_t(ly.total);
+}
+
+int ssm_scan_fwd_host(const float* u, const float* delta, const float* A, const float* B,
+                      const float* C, const float* D, const float* z, const float* delta_bias,
+                      int softplus_flag, float* y, float* h_last, int64_t batch, int64_t L,
+                      int64_t dim, int64_t N, void* workspace, int64_t workspace_bytes,
+                      cudaStream_t stream) {
+    return scan_fwd_host<float>(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, h_last,
+                                batch, L, dim, N, workspace, workspace_bytes, stream);
+}
+
+int ssm_scan_fwd_bf16_host(const uint16_t* u, const uint16_t* delta, const float* A,
+                           const uint16_t* B, const uint16_t* C, const float* D,
+                           const uint16_t* z, const float* delta_bias, int softplus_flag,
+                           uint16_t* y, float* h_last, int64_t batch, int64_t L, int64_t dim,
+                           int64_t N, void* workspace, int64_t workspace_bytes,
+                           cudaStream_t stream) {
+    using bf = __nv_bfloat16;
+    return scan_fwd_host<bf>(reinterpret_cast<const bf*>(u), reinterpret_cast<const bf*>(delta), A,
+                             reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
+                             reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
+                             reinterpret_cast<bf*>(y), h_last, batch, L, dim, N, workspace,
+                             workspace_bytes, stream);
 }
 
 int ssm_scan_step(const float* u, const float* delta, const float* A, const float* B,

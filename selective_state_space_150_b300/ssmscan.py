@@ -47,7 +47,8 @@ SSM_KNOB_KERNEL = 8
 
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc",
             "ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0", "ssm_scan_step", "ssm_scan_step_bf16",
-            "ssm_conv_scan_fwd", "ssm_conv_scan_fwd_bf16",
+            "ssm_conv_scan_fwd", "ssm_conv_scan_fwd_bf16", "ssm_scan_host_workspace_bytes",
+            "ssm_scan_fwd_host", "ssm_scan_fwd_bf16_host",
             "ssm_scan_last_device_status", "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
 
 _vp = ctypes.c_void_p
@@ -63,6 +64,11 @@ for _name in ("ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0"):
 for _name in ("ssm_conv_scan_fwd", "ssm_conv_scan_fwd_bf16"):
     getattr(_lib, _name).argtypes = [_vp, _vp, _vp, ctypes.c_int] + _FWD_ARGS[1:]
     getattr(_lib, _name).restype = ctypes.c_int
+for _name in ("ssm_scan_fwd_host", "ssm_scan_fwd_bf16_host"):
+    getattr(_lib, _name).argtypes = _FWD_ARGS[:-1] + [_vp, _i64, _vp]
+    getattr(_lib, _name).restype = ctypes.c_int
+_lib.ssm_scan_host_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int]
+_lib.ssm_scan_host_workspace_bytes.restype = _i64
 for _name in ("ssm_scan_step", "ssm_scan_step_bf16"):
     getattr(_lib, _name).argtypes = [_vp] * 8 + [ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _vp]
     getattr(_lib, _name).restype = ctypes.c_int
@@ -143,6 +149,30 @@ def ssm_conv_scan_fwd_bf16(x, conv_w, conv_b, conv_k, delta, A, B, C, D, z, delt
                                        delta or None, A or None, B or None, C or None, D or None,
                                        z or None, delta_bias or None, int(softplus_flag),
                                        y or None, h_last or None, batch, L, dim, N,
+                                       stream or None)
+
+
+def ssm_scan_host_workspace_bytes(batch, L, dim, N, dtype: int) -> int:
+    """Device workspace bytes the host-buffer entry points need (-1: bad size)."""
+    return int(_lib.ssm_scan_host_workspace_bytes(batch, L, dim, N, int(dtype)))
+
+
+def ssm_scan_fwd_host(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, h_last, batch, L,
+                      dim, N, workspace, workspace_bytes, stream) -> int:
+    """fp32 scan on HOST buffers (pointers are ints); workspace is a device pointer."""
+    return _lib.ssm_scan_fwd_host(u or None, delta or None, A or None, B or None, C or None,
+                                  D or None, z or None, delta_bias or None, int(softplus_flag),
+                                  y or None, h_last or None, batch, L, dim, N, workspace or None,
+                                  int(workspace_bytes), stream or None)
+
+
+def ssm_scan_fwd_bf16_host(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, h_last, batch,
+                           L, dim, N, workspace, workspace_bytes, stream) -> int:
+    """bf16 scan on HOST buffers (pointers are ints); workspace is a device pointer."""
+    return _lib.ssm_scan_fwd_bf16_host(u or None, delta or None, A or None, B or None, C or None,
+                                       D or None, z or None, delta_bias or None,
+                                       int(softplus_flag), y or None, h_last or None, batch, L,
+                                       dim, N, workspace or None, int(workspace_bytes),
                                        stream or None)
 
 

@@ -211,3 +211,26 @@ def test_conv_checks(fn):
     assert conv_fwd(fn, conv_w=P + 0x600002) == ssmscan.SSM_ERR_ALIGN
     assert conv_fwd(fn, y=P + 0x600000) == ssmscan.SSM_ERR_ALIAS     # y over the taps
     assert conv_fwd(fn, batch=0) == ssmscan.SSM_OK
+
+
+# ---------------------------------------------------------------- host-buffer calls
+def test_host_workspace_sizes():
+    f = ssm.ssm_scan_host_workspace_bytes
+    small = f(8, 2048, 1536, 16, 1)
+    assert small > 0 and f(8, 2048, 1536, 16, 0) > small          # fp32 slots are larger
+    # two slots of one part (a row group of 1 row here) plus A, D, bias
+    per_row = 4 * 2048 * 1536 * 2 + 2 * 2048 * 16 * 2 + 1536 * 16 * 4
+    assert 2 * per_row <= small <= 2 * per_row + 1536 * 16 * 4 + 8 * 1536 + 64 * 256
+    assert f(1, 131072, 5120, 16, 1) < f(1, 131072, 5120, 16, 1) * 2   # time pieces: finite
+    assert f(-1, 1, 1, 1, 1) == -1 and f(1, 1, 1, 0, 1) == -1 and f(1, 1, 1, 1, 2) == -1
+
+
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd_host, ssm.ssm_scan_fwd_bf16_host])
+def test_host_call_checks(fn):
+    args = dict(u=P, delta=P, A=P, B=P, C=P, D=0, z=0, delta_bias=0, softplus_flag=0, y=Q,
+                h_last=0, batch=2, L=8, dim=16, N=4, workspace=P, workspace_bytes=16, stream=0)
+    assert fn(**{**args, "u": 0}) == ssmscan.SSM_ERR_NULL
+    assert fn(**{**args, "workspace": 0}) == ssmscan.SSM_ERR_NULL
+    assert fn(**args) == ssmscan.SSM_ERR_SIZE                     # workspace too small
+    assert fn(**{**args, "batch": 0}) == ssmscan.SSM_OK
+    assert fn(**{**args, "N": 200}) == ssmscan.SSM_ERR_UNSUPPORTED_N
