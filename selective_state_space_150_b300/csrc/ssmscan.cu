@@ -910,7 +910,7 @@ struct LayoutW {
     }
 };
 
-template <typename T, int NPT, int WS, int TC, bool SUMMARY>
+template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV>
 __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     ssm_scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u,
                        const __grid_constant__ CUtensorMap tm_dt,
@@ -930,7 +930,7 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     __shared__ int s_abort;
     volatile int* const abort_flag = &s_abort;
     unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const bool conv = p.conv_k > 0;
+    constexpr bool conv = CONV;  // the convolution prologue (p.conv_k > 0)
     const LayoutW<T, NPT, WS, TC, SUMMARY> lay(p.N, p.stages, conv);
     const int nst = p.stages;
 
@@ -1188,7 +1188,7 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
             // x rows t .. t + kConvHalo of the x tile are steps t - kConvHalo ..
             // t of the chunk; xw holds the window, oldest first
             float2 xw[kMaxConvK];
-            if (conv) {
+            if constexpr (conv) {
 #pragma unroll
                 for (int j = 0; j < kMaxConvK - 1; ++j) {
                     float xv[2];
@@ -1202,7 +1202,7 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
                 const uint32_t o = TT::off(t, 2 * pp * ES, TC);
                 float xr[2], uu[2];
                 ld_k<T, 2>(rdt + o, xr);
-                if (conv) {
+                if constexpr (conv) {
                     // u = silu(causal conv) over the window ending at step t
                     float xv[2];
                     ld_k<T, 2>(ru + TT::off_cbs(t + kConvHalo, 2 * pp * ES, cbsx), xv);
@@ -1277,7 +1277,7 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
                 for (int sgi = 1; sgi < WS; ++sgi)
                     acc = __fadd2_rn(acc, *reinterpret_cast<const float2*>(part + (sgi * TC + t) * DT + 2 * pp));
                 float uu[2];
-                if (conv) {
+                if constexpr (conv) {
                     const float2 uv = s_u(bf)[t * (DT / 2) + pp];
                     uu[0] = uv.x;
                     uu[1] = uv.y;
@@ -1586,8 +1586,9 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
             variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 16, conv) <= kMaxSmem;
     if (pl.ws) {
         pl.NT = (wc * pl.WS + 5) * 32;  // + 2 prepare, 2 finish and 1 producer warp
-        pl.TC = (ft == 32 && variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 32, conv) <= kMaxSmem) ? 32
-                                                                                        : 16;
+        pl.TC = (!conv && ft == 32 && variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 32) <= kMaxSmem)
+                    ? 32
+                    : 16;
         // The deepest ring (chunks in flight) within the footprint target.
         pl.stages = 2;
         for (int st : {6, 5, 4, 3})
@@ -1667,11 +1668,11 @@ int launch_one(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStre
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
-template <typename T, int NPT, int WS, int TC, bool SUMMARY>
+template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV>
 int launch_one_w(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
     using G = GeoW<T, NPT, WS, TC>;
-    auto kern = ssm_scan_ws_kernel<T, NPT, WS, TC, SUMMARY>;
-    const size_t smem = smem_bytes_w<T, NPT, WS, SUMMARY>(kp.N, kp.stages, TC, kp.conv_k > 0);
+    auto kern = ssm_scan_ws_kernel<T, NPT, WS, TC, SUMMARY, CONV>;
+    const size_t smem = smem_bytes_w<T, NPT, WS, SUMMARY>(kp.N, kp.stages, TC, CONV);
     static std::atomic<size_t> configured[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_LAUNCH;
@@ -1695,14 +1696,24 @@ int launch_one_w(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaSt
 template <typename T>
 int dispatch(const Plan& pl, int64_t grid, const CUtensorMap* tms, const KParams& kp,
              cudaStream_t stream) {
+    if (pl.ws && kp.conv_k > 0) {  // the prologue is built for 16-step chunks
+        if (pl.TC != 16) return SSM_ERR_ARG;
+#define SSM_CASE_WC(NPT_, WS_)                                                        \
+    if (pl.NPT == NPT_ && pl.WS == WS_)                                               \
+        return kp.summary ? launch_one_w<T, NPT_, WS_, 16, true, true>(grid, tms, kp, stream) \
+                          : launch_one_w<T, NPT_, WS_, 16, false, true>(grid, tms, kp, stream);
+        SSM_FOR_EACH_VARIANT(SSM_CASE_WC)
+#undef SSM_CASE_WC
+        return SSM_ERR_UNSUPPORTED_N;
+    }
     if (pl.ws) {
-#define SSM_CASE_W(NPT_, WS_)                                                                  \
-    if (pl.NPT == NPT_ && pl.WS == WS_) {                                                      \
-        if (kp.summary)                                                                        \
-            return pl.TC == 16 ? launch_one_w<T, NPT_, WS_, 16, true>(grid, tms, kp, stream)  \
-                               : launch_one_w<T, NPT_, WS_, 32, true>(grid, tms, kp, stream); \
-        return pl.TC == 16 ? launch_one_w<T, NPT_, WS_, 16, false>(grid, tms, kp, stream)     \
-                           : launch_one_w<T, NPT_, WS_, 32, false>(grid, tms, kp, stream);    \
+#define SSM_CASE_W(NPT_, WS_)                                                                        \
+    if (pl.NPT == NPT_ && pl.WS == WS_) {                                                            \
+        if (kp.summary)                                                                              \
+            return pl.TC == 16 ? launch_one_w<T, NPT_, WS_, 16, true, false>(grid, tms, kp, stream)  \
+                               : launch_one_w<T, NPT_, WS_, 32, true, false>(grid, tms, kp, stream); \
+        return pl.TC == 16 ? launch_one_w<T, NPT_, WS_, 16, false, false>(grid, tms, kp, stream)     \
+                           : launch_one_w<T, NPT_, WS_, 32, false, false>(grid, tms, kp, stream);    \
     }
         SSM_FOR_EACH_VARIANT(SSM_CASE_W)
 #undef SSM_CASE_W
