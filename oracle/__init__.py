@@ -63,6 +63,9 @@ def _declare(lib):
     lib.ssm_oracle_fwd.restype = ctypes.c_int
     lib.ssm_oracle_fwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
                                    dp, dp, i64, i64, i64, i64]
+    lib.ssm_oracle_fwd_ex.restype = ctypes.c_int
+    lib.ssm_oracle_fwd_ex.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
+                                      ctypes.c_int, dp, dp, i64, i64, i64, i64]
     lib.ssm_oracle_fwd_h0.restype = ctypes.c_int
     lib.ssm_oracle_fwd_h0.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, ctypes.c_int,
                                       dp, dp, i64, i64, i64, i64]
@@ -83,12 +86,13 @@ def _ptr(a):
 
 
 def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
-                       softplus=False, lib=None, h0=None):
+                       softplus=False, lib=None, h0=None, zoh=False):
     """Selective-scan forward in fp64.
 
     u, delta, z: (batch, L, dim); A: (dim, N); B, C: (batch, L, N);
     D, delta_bias: (dim,); h0: (batch, dim, N) initial state.  D, z,
-    delta_bias and h0 may be None (h0 None = zero state).
+    delta_bias and h0 may be None (h0 None = zero state).  zoh: exact
+    zero-order-hold discretisation of B instead of dt * B.
     Inputs are converted to float64 exactly (fp32 or decoded bf16 values).
     Returns (y (batch, L, dim) float64, h_last (batch, dim, N) float64).
     """
@@ -108,7 +112,13 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None,
         assert z.shape == (batch, L, dim)
     y = np.zeros((batch, L, dim), dtype=np.float64)
     h = np.zeros((batch, dim, N), dtype=np.float64)
-    if h0 is None:
+    if zoh:
+        if h0 is not None:
+            assert h0.shape == (batch, dim, N)
+        rc = lib.ssm_oracle_fwd_ex(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
+                                   _ptr(D), _ptr(z), _ptr(delta_bias), _ptr(h0),
+                                   int(bool(softplus)), 1, _ptr(y), _ptr(h), batch, L, dim, N)
+    elif h0 is None:
         rc = lib.ssm_oracle_fwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C),
                                 _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)),
                                 _ptr(y), _ptr(h), batch, L, dim, N)

@@ -17,7 +17,10 @@
  *   for t = 0 .. L-1:
  *     dt = delta[b,t,d] + (delta_bias ? delta_bias[d] : 0)
  *     if softplus_flag: dt = softplus(dt) = log(1 + exp(dt))
- *     for n:  h[n] = exp(dt * A[d,n]) * h[n] + dt * B[b,t,n] * u[b,t,d]
+ *     for n:  h[n] = exp(dt * A[d,n]) * h[n] + Bbar * B[b,t,n] * u[b,t,d]
+ *             Bbar = dt                                  (simplified, Euler: the default)
+ *             Bbar = (exp(dt * A[d,n]) - 1) / A[d,n]     (exact zero-order hold; dt when
+ *                                                         A[d,n] = 0, its limit)
  *     y      = sum_n C[b,t,n] * h[n] + (D ? D[d] : 0) * u[b,t,d]
  *     if z:   y = y * z[b,t,d] / (1 + exp(-z[b,t,d]))       (SiLU(z) gate)
  *     out[b,t,d] = y
@@ -37,9 +40,11 @@
  *    gate silu(z) is applied after the skip.
  *  - "상태 공간 모델" (itwiki), section "Mamba의 선택 메커니즘": the discrete
  *    transition is exp(Delta_t A), varying per token through Delta_t.
- *  - The discretisation of B is the simplified (Euler) form Delta * B used by
- *    every code listing on the pages (not the exact zero-order-hold form the
- *    itwiki page prints in its "이산화" section).
+ *  - The discretisation of B is by default the simplified (Euler) form
+ *    Delta * B used by every code listing on the pages.  With zoh_flag it is
+ *    the exact zero-order-hold form the itwiki page prints in its "이산화"
+ *    section, Bbar = (Delta A)^-1 (exp(Delta A) - I) Delta B, which for a
+ *    diagonal A is (exp(Delta A_n) - 1) / A_n * B_n per state.
  *  - Obsidian "Mamba" note, section 4.2: recurrent (generation-time) inference
  *    carries only the hidden state from one token to the next, so a sequence
  *    split in two gives the same outputs when the second part starts from the
@@ -82,10 +87,10 @@ static double silu(double z)
  * Returns 0, or -1 when a required pointer is NULL, a size is negative or
  * the N-entry state cannot be allocated.
  */
-int ssm_oracle_fwd_h0(const double *u, const double *delta, const double *A,
+int ssm_oracle_fwd_ex(const double *u, const double *delta, const double *A,
                       const double *B, const double *C, const double *D,
                       const double *z, const double *delta_bias, const double *h0,
-                      int softplus_flag, double *y, double *h_last,
+                      int softplus_flag, int zoh_flag, double *y, double *h_last,
                       int64_t batch, int64_t L, int64_t dim, int64_t N)
 {
     if (!u || !delta || !A || !B || !C || !y)
@@ -116,7 +121,15 @@ int ssm_oracle_fwd_h0(const double *u, const double *delta, const double *A,
                 double acc = 0.0;
                 for (int64_t n = 0; n < N; ++n) {
                     const double dA  = exp(dt * A[d * N + n]);       /* discretised A */
-                    const double dBu = dt * B[i_bln + n] * x;       /* Euler B times u */
+                    double dBu;
+                    if (zoh_flag) {
+                        const double a = A[d * N + n];
+                        /* (exp(dt a) - 1) / a, and its limit dt at a = 0 */
+                        const double bbar = (a != 0.0) ? expm1(dt * a) / a : dt;
+                        dBu = bbar * B[i_bln + n] * x;               /* ZOH B times u */
+                    } else {
+                        dBu = dt * B[i_bln + n] * x;                 /* Euler B times u */
+                    }
                     h[n] = dA * h[n] + dBu;
                     acc += C[i_bln + n] * h[n];
                 }
@@ -134,6 +147,17 @@ int ssm_oracle_fwd_h0(const double *u, const double *delta, const double *A,
     }
     free(work);
     return 0;
+}
+
+/* Euler discretisation of B, from h0. */
+int ssm_oracle_fwd_h0(const double *u, const double *delta, const double *A,
+                      const double *B, const double *C, const double *D,
+                      const double *z, const double *delta_bias, const double *h0,
+                      int softplus_flag, double *y, double *h_last,
+                      int64_t batch, int64_t L, int64_t dim, int64_t N)
+{
+    return ssm_oracle_fwd_ex(u, delta, A, B, C, D, z, delta_bias, h0, softplus_flag, 0, y,
+                             h_last, batch, L, dim, N);
 }
 
 /* The same with a zero initial state. */

@@ -35,6 +35,17 @@ What each pin rests on:
                   4.2, carries only the state).
 Pins that pass an initial state call ``scan(..., h0=h0)``.
 
+The exact zero-order-hold discretisation (``scan(..., zoh=True)``) is pinned by:
+  zoh_lti         time-invariant inputs: y = u * K with K_k = sum_n C[n]
+                  exp(k dt A[n]) (exp(dt A[n]) - 1) / A[n] B[n] (the itwiki
+                  page's "이산화" Bbar inside its convolution kernel K), direct
+                  and by FFT.
+  zoh_ode         with B_t u_t held constant over each step, ZOH is the exact
+                  solution of h' = A h + B u: scipy's DOP853 integration of the
+                  continuous system, step by step, at rtol 1e-12.
+  zoh_limit       A = 0 gives exactly the Euler result; |A| = 1e-7 agrees
+                  with it to ~dt^2 |A|.
+
 The causal convolution + SiLU prologue (``conv`` functions with the signature
 ``conv(x, w, cb) -> u``) is pinned separately:
   conv_numpy      each channel against numpy.convolve (full convolution of x
@@ -84,10 +95,15 @@ def random_problem(rng, batch, L, dim, N, softplus=True, bias=True, gate=True, s
     return dict(u=u, delta=delta, A=A, B=B, C=C, D=D, z=z, delta_bias=db, softplus=softplus)
 
 
-def _call(scan, p, h0=None):
+def _call(scan, p, h0=None, zoh=False):
     args = (p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"], p["delta_bias"],
             p["softplus"])
-    return scan(*args) if h0 is None else scan(*args, h0=h0)
+    kw = {}
+    if h0 is not None:
+        kw["h0"] = h0
+    if zoh:
+        kw["zoh"] = True
+    return scan(*args, **kw)
 
 
 # ---------------------------------------------------------------- brute force
@@ -345,6 +361,71 @@ def pin_chaining(scan, seed=7):
         yk, hk = _call(scan, one, h0=hk)
         worst = max(worst, _rel_err(y[:, t:t + 1], yk))
     return max(worst, _rel_err(h, hk))
+
+
+# ---------------------------------------------------------------- zero-order hold
+def pin_zoh_lti(scan, seed=12):
+    rng = np.random.default_rng(seed)
+    p, dt, bvec, cvec = _lti_problem(rng, batch=2, L=300, dim=4, N=8)
+    y, _ = _call(scan, p, zoh=True)
+    A = p["A"]
+    k = np.arange(300)
+    worst = 0.0
+    for d in range(4):
+        bbar = np.expm1(dt[d] * A[d]) / A[d] * bvec                     # (N,)
+        K = (np.exp(np.outer(k, dt[d] * A[d])) * cvec * bbar).sum(axis=1)  # (L,)
+        for b in range(2):
+            x = p["u"][b, :, d]
+            direct = np.array([np.dot(K[:t + 1][::-1], x[:t + 1]) for t in range(300)])
+            n = 600
+            fft = np.fft.irfft(np.fft.rfft(x, n) * np.fft.rfft(K, n), n)[:300]
+            worst = max(worst, _rel_err(y[b, :, d], direct), _rel_err(y[b, :, d], fft))
+    return worst
+
+
+def pin_zoh_ode(scan, seed=13):
+    from scipy.integrate import solve_ivp
+    rng = np.random.default_rng(seed)
+    p = random_problem(rng, batch=1, L=6, dim=2, N=3, gate=True, skip=True)
+    h0 = rng.standard_normal((1, 2, 3))
+    y, h = _call(scan, p, h0=h0, zoh=True)
+    dt = p["delta"] + p["delta_bias"][None, None, :]
+    dt = np.logaddexp(0.0, dt)
+    worst = 0.0
+    for d in range(2):
+        a = p["A"][d]
+        state = h0[0, d].copy()
+        for t in range(6):
+            drive = p["B"][0, t] * p["u"][0, t, d]          # held over the step
+            sol = solve_ivp(lambda _s, x: a * x + drive, (0.0, dt[0, t, d]), state,
+                            method="DOP853", rtol=1e-12, atol=1e-14)
+            state = sol.y[:, -1]
+            yt = np.dot(p["C"][0, t], state) + p["D"][d] * p["u"][0, t, d]
+            zz = p["z"][0, t, d]
+            yt *= zz / (1.0 + np.exp(-zz))
+            worst = max(worst, _rel_err(y[0, t, d], yt))
+        worst = max(worst, _rel_err(h[0, d], state))
+    return worst
+
+
+def pin_zoh_limit(scan, seed=14):
+    rng = np.random.default_rng(seed)
+    p = random_problem(rng, batch=2, L=9, dim=3, N=4)
+    p["A"] = np.zeros_like(p["A"])
+    y0, h0 = _call(scan, p)
+    y1, h1 = _call(scan, p, zoh=True)
+    worst = 0.0 if (np.array_equal(y0, y1) and np.array_equal(h0, h1)) else 1.0
+    p["A"] = np.full_like(p["A"], -1e-7)
+    y0, h0 = _call(scan, p)
+    y1, h1 = _call(scan, p, zoh=True)
+    return max(worst, 1e-4 * _rel_err(y1, y0), 1e-4 * _rel_err(h1, h0))
+
+
+ZOH_PINS = {
+    "zoh_lti": (pin_zoh_lti, 1e-9),
+    "zoh_ode": (pin_zoh_ode, 1e-9),
+    "zoh_limit": (pin_zoh_limit, 1e-10),
+}
 
 
 # ---------------------------------------------------------------- conv prologue

@@ -7,7 +7,7 @@ import subprocess
 import pytest
 
 import oracle
-from tests.oracle_pins import ALL_PINS, CONV_PINS
+from tests.oracle_pins import ALL_PINS, CONV_PINS, ZOH_PINS
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ssm_oracle.c")
 
@@ -98,6 +98,36 @@ def test_conv_pins_catch_mutant(name, tmpdir_mod):
     for pname, (fn, tol) in CONV_PINS.items():
         try:
             err = fn(lambda x, w, cb: oracle.causal_conv_silu(x, w, cb, lib=lib))
+        except Exception:
+            err = float("inf")
+        if not (err <= tol):
+            failures.append(pname)
+    assert failures, f"mutant {name} passed every pin"
+
+
+ZOH_MUTANTS = {
+    "zoh_no_division": ("expm1(dt * a) / a : dt", "expm1(dt * a) : dt"),
+    "zoh_is_euler": ("expm1(dt * a) / a : dt", "dt : dt"),
+    "zoh_sign": ("expm1(dt * a) / a : dt", "expm1(-dt * a) / a : dt"),
+    "zoh_exp_not_expm1": ("expm1(dt * a) / a : dt", "exp(dt * a) / a : dt"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ZOH_MUTANTS))
+def test_zoh_pins_catch_mutant(name, tmpdir_mod):
+    old, new = ZOH_MUTANTS[name]
+    src = open(SRC).read()
+    assert old in src, f"mutation anchor for {name} not found"
+    cfile = os.path.join(tmpdir_mod, f"{name}.c")
+    sofile = os.path.join(tmpdir_mod, f"lib{name}.so")
+    with open(cfile, "w") as f:
+        f.write(src.replace(old, new))
+    oracle.build(force=True, src=cfile, out=sofile)
+    lib = oracle.load(sofile)
+    failures = []
+    for pname, (fn, tol) in ZOH_PINS.items():
+        try:
+            err = fn(lambda *a, **kw: oracle.selective_scan_fwd(*a, lib=lib, **kw))
         except Exception:
             err = float("inf")
         if not (err <= tol):

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.oracle_pins import ALL_PINS, CONV_PINS
+from tests.oracle_pins import ALL_PINS, CONV_PINS, ZOH_PINS
 
 
 @pytest.mark.parametrize("name", sorted(ALL_PINS))
@@ -67,4 +67,11 @@ def test_oracle_decode_step_is_the_scan_at_one_token():
 def test_oracle_conv_pin(name):
     fn, tol = CONV_PINS[name]
     err = fn(oracle.causal_conv_silu)
+    assert err <= tol, f"{name}: error {err:.3e} > {tol:.1e}"
+
+
+@pytest.mark.parametrize("name", sorted(ZOH_PINS))
+def test_oracle_zoh_pin(name):
+    fn, tol = ZOH_PINS[name]
+    err = fn(oracle.selective_scan_fwd)
     assert err <= tol, f"{name}: error {err:.3e} > {tol:.1e}"
