@@ -158,6 +158,28 @@ SSM_API int ssm_scan_fwd_bf16_h0(const uint16_t *u, const uint16_t *delta, const
                     cudaStream_t stream);
 
 /*
+ * The scan with the exact zero-order-hold discretisation of B (itwiki "상태
+ * 공간 모델", section "이산화": Bbar = (dt A)^-1 (exp(dt A) - I) dt B), per
+ * state
+ *   h[n] = exp(dt A[d,n]) h[n] + (exp(dt A[d,n]) - 1) / A[d,n] * B[b,t,n] u[b,t,d]
+ * (dt B u where A[d,n] = 0, the limit), instead of the dt B u of the other
+ * entry points.  Arguments as ssm_scan_fwd_h0 (h0 may be NULL).  Runs in the
+ * warp-specialised kernel only: rows TMA cannot describe return SSM_ERR_ALIGN.
+ */
+SSM_API int ssm_scan_fwd_zoh(const float *u, const float *delta, const float *A,
+                    const float *B, const float *C, const float *D,
+                    const float *z, const float *delta_bias, const float *h0,
+                    int softplus_flag, float *y, float *h_last,
+                    int64_t batch, int64_t L, int64_t dim, int64_t N,
+                    cudaStream_t stream);
+SSM_API int ssm_scan_fwd_bf16_zoh(const uint16_t *u, const uint16_t *delta, const float *A,
+                    const uint16_t *B, const uint16_t *C, const float *D,
+                    const uint16_t *z, const float *delta_bias, const float *h0,
+                    int softplus_flag, uint16_t *y, float *h_last,
+                    int64_t batch, int64_t L, int64_t dim, int64_t N,
+                    cudaStream_t stream);
+
+/*
  * The scan with its input produced in the same kernel by the step before it
  * in the Mamba block: a causal depthwise 1-D convolution of kernel size
  * conv_k (1 .. 4) with bias, then SiLU (the MambaBlock listing of the

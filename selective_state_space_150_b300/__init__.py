@@ -17,7 +17,9 @@ from .ssmscan import (  # noqa: F401
     ssm_scan_host_workspace_bytes,
     ssm_scan_fwd_bf16_noalloc,
     ssm_scan_fwd_bf16_h0,
+    ssm_scan_fwd_bf16_zoh,
     ssm_scan_fwd_h0,
+    ssm_scan_fwd_zoh,
     ssm_scan_step,
     ssm_scan_step_bf16,
     ssm_scan_last_device_status,

@@ -337,6 +337,7 @@ struct KParams {
     const float* conv_w;  // [dim][conv_k]
     const float* conv_b;  // [dim] or null
     int conv_k;           // 0 (no prologue) or 1 .. kMaxConvK
+    int zoh;              // 1: exact zero-order-hold B (warp-specialised kernel only)
 };
 
 // Compile-time geometry of one block.
@@ -422,12 +423,68 @@ __device__ __forceinline__ float scan_step(float2 v, const float (&bb)[NPT], con
     }
 }
 
+// The same step with the exact zero-order-hold B (itwiki "상태 공간 모델",
+// section "이산화": Bbar = (dt A)^-1 (exp(dt A) - 1) dt B, per state
+// (e - 1) / A B with e = exp(dt A)).  v = (dt, u); ia = 1 / A (0 where A = 0).
+// For |dt A| < 1/16 the factor is dt (1 + x/2 + x^2/6 + x^3/24 + x^4/120),
+// x = dt A (the dropped terms are below 2e-9 relative), which also gives the
+// limit dt at A = 0; elsewhere (e - 1) / A loses at most ~3e-6 relative.
+__device__ __forceinline__ float2 zoh_factor2(float2 vx, float2 x2, float2 e, float2 ia) {
+    const float2 xa = __fmul2_rn(x2, make_float2(kLn2, kLn2));  // dt A
+    float2 s = __ffma2_rn(xa, make_float2(1.f / 120.f, 1.f / 120.f),
+                          make_float2(1.f / 24.f, 1.f / 24.f));
+    s = __ffma2_rn(s, xa, make_float2(1.f / 6.f, 1.f / 6.f));
+    s = __ffma2_rn(s, xa, make_float2(0.5f, 0.5f));
+    s = __ffma2_rn(s, xa, make_float2(1.f, 1.f));
+    const float2 fs = __fmul2_rn(vx, s);
+    const float2 fl = __fmul2_rn(__fadd2_rn(e, make_float2(-1.f, -1.f)), ia);
+    return make_float2(fabsf(xa.x) < 0.0625f ? fs.x : fl.x, fabsf(xa.y) < 0.0625f ? fs.y : fl.y);
+}
+
+template <int NPT, bool WITH_C>
+__device__ __forceinline__ float scan_step_zoh(float2 v, const float (&bb)[NPT],
+                                               const float (&cc)[NPT], const float (&a2)[NPT],
+                                               const float (&ia)[NPT], float (&h)[NPT]) {
+    const float2 vx = make_float2(v.x, v.x), vy = make_float2(v.y, v.y);
+    if constexpr (NPT == 1) {
+        const float x2 = v.x * a2[0];
+        const float e = ex2_approx(x2);
+        const float2 f = zoh_factor2(vx, make_float2(x2, x2), make_float2(e, e),
+                                     make_float2(ia[0], ia[0]));
+        h[0] = fmaf(e, h[0], (v.y * bb[0]) * f.x);
+        return WITH_C ? cc[0] * h[0] : 0.f;
+    } else {
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < NPT; j += 2) {
+            const float2 x = __fmul2_rn(vx, make_float2(a2[j], a2[j + 1]));
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            const float2 f = zoh_factor2(vx, x, e, make_float2(ia[j], ia[j + 1]));
+            const float2 w = __fmul2_rn(__fmul2_rn(vy, make_float2(bb[j], bb[j + 1])), f);
+            const float2 hh = __ffma2_rn(e, make_float2(h[j], h[j + 1]), w);
+            h[j] = hh.x;
+            h[j + 1] = hh.y;
+            if constexpr (WITH_C) acc = __ffma2_rn(make_float2(cc[j], cc[j + 1]), hh, acc);
+        }
+        return WITH_C ? acc.x + acc.y : 0.f;
+    }
+}
+
+template <int NPT, bool WITH_C, bool ZOH>
+__device__ __forceinline__ float scan_step_any(float2 v, const float (&bb)[NPT],
+                                               const float (&cc)[NPT], const float (&a2)[NPT],
+                                               const float (&ia)[NPT], float (&h)[NPT]) {
+    if constexpr (ZOH) return scan_step_zoh<NPT, WITH_C>(v, bb, cc, a2, ia, h);
+    else return scan_step<NPT, WITH_C>(v, bb, cc, a2, h);
+}
+
 // Summary variant: the same state update without the readout; returns the
 // chunk's sum of dt for this channel (padded steps hold dt = 0).
-template <int NPT, int NP, int DT, int TC>
+template <int NPT, int NP, int DT, int TC, bool ZOH = false>
 __device__ __forceinline__ float scan_chunk_summary(const float2* __restrict__ dd,
                                                    const float* __restrict__ Bs,
-                                                   const float (&a2)[NPT], float (&h)[NPT]) {
+                                                   const float (&a2)[NPT],
+                                                   const float (&ia)[NPT], float (&h)[NPT]) {
     constexpr int SB = scan_block<NPT>() < TC ? scan_block<NPT>() : TC;
     float sdt = 0.f;
 #pragma unroll 1
@@ -439,7 +496,7 @@ __device__ __forceinline__ float scan_chunk_summary(const float2* __restrict__ d
             float bb[NPT];
             ld_states<NPT>(Bs + t * NP, bb);
             sdt += v.x;
-            scan_step<NPT, false>(v, bb, bb, a2, h);
+            scan_step_any<NPT, false, ZOH>(v, bb, bb, a2, ia, h);
         }
     }
     return sdt;
@@ -450,12 +507,12 @@ __device__ __forceinline__ float scan_chunk_summary(const float2* __restrict__ d
 // stay in registers until its steps are done: a shared store between steps
 // would keep the compiler from issuing later steps' loads ahead of it and
 // serialise the steps.
-template <int NPT, int NP, int DT, int TC>
+template <int NPT, int NP, int DT, int TC, bool ZOH = false>
 __device__ __forceinline__ void scan_chunk(const float2* __restrict__ dd,
                                            const float* __restrict__ Bs,
                                            const float* __restrict__ Cs,
                                            float* __restrict__ part, const float (&a2)[NPT],
-                                           float (&h)[NPT]) {
+                                           const float (&ia)[NPT], float (&h)[NPT]) {
     constexpr int SB = scan_block<NPT>() < TC ? scan_block<NPT>() : TC;
     static_assert(TC % SB == 0, "register blocks");
 #pragma unroll 1
@@ -467,7 +524,7 @@ __device__ __forceinline__ void scan_chunk(const float2* __restrict__ dd,
             float bb[NPT], cc[NPT];
             ld_states<NPT>(Bs + t * NP, bb);
             ld_states<NPT>(Cs + t * NP, cc);
-            pv[i] = scan_step<NPT, true>(dd[t * DT], bb, cc, a2, h);
+            pv[i] = scan_step_any<NPT, true, ZOH>(dd[t * DT], bb, cc, a2, ia, h);
         }
 #pragma unroll
         for (int i = 0; i < SB; ++i) part[(t0 + i) * DT] = pv[i];
@@ -727,14 +784,15 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
 
         // ---------------- SCAN: all TC steps (padded ones are no-ops)
         if constexpr (summary) {
-            sdt_seg += double(scan_chunk_summary<NPT, NP, DT, TC>(s_dd + c, s_B + sg * NPT, a2, h));
+            sdt_seg +=
+                double(scan_chunk_summary<NPT, NP, DT, TC>(s_dd + c, s_B + sg * NPT, a2, a2, h));
             __syncthreads();  // the next PREP overwrites s_dd, s_B
             if (++st == nst) { st = 0; ph ^= 1u; }
             if (++sa == nst) sa = 0;
             continue;
         }
         scan_chunk<NPT, NP, DT, TC>(s_dd + c, s_B + sg * NPT, s_C + sg * NPT,
-                                    s_part + sg * TC * DT + c, a2, h);
+                                    s_part + sg * TC * DT + c, a2, a2, h);
         __syncthreads();
 
         // ---------------- POST: y = (sum of the state groups' partials) g + D u g
@@ -910,7 +968,7 @@ struct LayoutW {
     }
 };
 
-template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV>
+template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH>
 __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     ssm_scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u,
                        const __grid_constant__ CUtensorMap tm_dt,
@@ -1003,11 +1061,13 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
         const int c = ct * 32 + lane;
         const int64_t d_scan = d0 + c;
         const bool scan_ok = d_scan < dim;
-        float a2[NPT], h[NPT];
+        float a2[NPT], h[NPT], ia[NPT];
 #pragma unroll
         for (int j = 0; j < NPT; ++j) {
             const int64_t n = int64_t(sg) * NPT + j;
-            a2[j] = (scan_ok && n < N) ? p.A[d_scan * N + n] * kLog2e : 0.f;
+            const float a = (scan_ok && n < N) ? p.A[d_scan * N + n] : 0.f;
+            a2[j] = a * kLog2e;
+            ia[j] = (ZOH && a != 0.f) ? 1.f / a : 0.f;  // the ZOH factor's 1 / A
             h[j] = (p.h0 != nullptr && !summary && scan_ok && n < N)
                        ? p.h0[(b * dim + d_scan) * N + n]
                        : 0.f;
@@ -1032,11 +1092,12 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
                 return;
             }
             if constexpr (summary) {
-                sdt_seg += double(scan_chunk_summary<NPT, NP, DT, TC>(s_dd(bf) + c,
-                                                                      s_B(bf) + sg * NPT, a2, h));
+                sdt_seg += double(scan_chunk_summary<NPT, NP, DT, TC, ZOH>(
+                    s_dd(bf) + c, s_B(bf) + sg * NPT, a2, ia, h));
             } else {
-                scan_chunk<NPT, NP, DT, TC>(s_dd(bf) + c, s_B(bf) + sg * NPT, s_C(bf) + sg * NPT,
-                                            s_part(bf) + sg * TC * DT + c, a2, h);
+                scan_chunk<NPT, NP, DT, TC, ZOH>(s_dd(bf) + c, s_B(bf) + sg * NPT,
+                                                 s_C(bf) + sg * NPT,
+                                                 s_part(bf) + sg * TC * DT + c, a2, ia, h);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_done(bf));
@@ -1222,7 +1283,9 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
                 }
                 float2 x = __fadd2_rn(make_float2(xr[0], xr[1]), b2);
                 if (p.softplus) x = Act<T>::softplus2(x);
-                const float2 xu = __fmul2_rn(x, make_float2(uu[0], uu[1]));
+                // (dt, dt u); with the ZOH B the scan scales u itself: (dt, u)
+                const float2 xu = ZOH ? make_float2(uu[0], uu[1])
+                                      : __fmul2_rn(x, make_float2(uu[0], uu[1]));
                 *reinterpret_cast<float4*>(sdd + t * DT + 2 * pp) =
                     t < tv ? make_float4(x.x, xu.x, x.y, xu.y) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -1541,7 +1604,7 @@ constexpr size_t kWsSmemTarget = 60 * 1024;
 template <typename T>
 Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, const void* dt,
                const void* z, const void* y, const void* Bp, const void* Cp,
-               bool allow_tma = true, bool conv = false) {
+               bool allow_tma = true, bool conv = false, bool need_ws = false) {
     const size_t es = sizeof(T);
     Plan pl;
     const int64_t channels = batch * dim;
@@ -1581,12 +1644,14 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
     const int ft = g_force_chunk.load();
     const int fs = g_force_stages.load();
     // The warp-specialised kernel wherever its tiles can move by TMA.
-    // (The convolution prologue exists only in the warp-specialised kernel.)
-    pl.ws = pl.tma_udz && (conv || g_force_kernel.load() != 1) &&
+    // (The convolution prologue and the ZOH variant exist only in the
+    // warp-specialised kernel, built for 16-step chunks.)
+    if (conv) need_ws = true;
+    pl.ws = pl.tma_udz && (need_ws || g_force_kernel.load() != 1) &&
             variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 16, conv) <= kMaxSmem;
     if (pl.ws) {
         pl.NT = (wc * pl.WS + 5) * 32;  // + 2 prepare, 2 finish and 1 producer warp
-        pl.TC = (!conv && ft == 32 && variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 32) <= kMaxSmem)
+        pl.TC = (!need_ws && ft == 32 && variant_smem_w<T>(pl.NPT, pl.WS, N, 2, 32) <= kMaxSmem)
                     ? 32
                     : 16;
         // The deepest ring (chunks in flight) within the footprint target.
@@ -1668,10 +1733,10 @@ int launch_one(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStre
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
-template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV>
+template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH = false>
 int launch_one_w(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
     using G = GeoW<T, NPT, WS, TC>;
-    auto kern = ssm_scan_ws_kernel<T, NPT, WS, TC, SUMMARY, CONV>;
+    auto kern = ssm_scan_ws_kernel<T, NPT, WS, TC, SUMMARY, CONV, ZOH>;
     const size_t smem = smem_bytes_w<T, NPT, WS, SUMMARY>(kp.N, kp.stages, TC, CONV);
     static std::atomic<size_t> configured[64];
     int dev = 0;
@@ -1696,6 +1761,17 @@ int launch_one_w(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaSt
 template <typename T>
 int dispatch(const Plan& pl, int64_t grid, const CUtensorMap* tms, const KParams& kp,
              cudaStream_t stream) {
+    if (pl.ws && kp.zoh) {  // the ZOH variant is built for 16-step chunks, no prologue
+        if (pl.TC != 16 || kp.conv_k > 0) return SSM_ERR_ARG;
+#define SSM_CASE_WZ(NPT_, WS_)                                                                \
+    if (pl.NPT == NPT_ && pl.WS == WS_)                                                       \
+        return kp.summary                                                                     \
+                   ? launch_one_w<T, NPT_, WS_, 16, true, false, true>(grid, tms, kp, stream) \
+                   : launch_one_w<T, NPT_, WS_, 16, false, false, true>(grid, tms, kp, stream);
+        SSM_FOR_EACH_VARIANT(SSM_CASE_WZ)
+#undef SSM_CASE_WZ
+        return SSM_ERR_UNSUPPORTED_N;
+    }
     if (pl.ws && kp.conv_k > 0) {  // the prologue is built for 16-step chunks
         if (pl.TC != 16) return SSM_ERR_ARG;
 #define SSM_CASE_WC(NPT_, WS_)                                                        \
@@ -1777,7 +1853,8 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
              const T* z, const float* delta_bias, int softplus_flag, T* y, float* h_last,
              int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream,
              bool fixed_scratch = false, const float* h0 = nullptr,
-             const float* conv_w = nullptr, const float* conv_b = nullptr, int conv_k = 0) {
+             const float* conv_w = nullptr, const float* conv_b = nullptr, int conv_k = 0,
+             bool zoh = false) {
     if (batch < 0 || L < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
     // A pointer may be NULL only when its tensor has no elements.
     if ((batch > 0 && L > 0 && dim > 0) && (!u || !delta || !y)) return SSM_ERR_NULL;
@@ -1815,11 +1892,11 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     if (batch == 0 || dim == 0) return SSM_OK;  // nothing to compute
 
     const bool conv = conv_k > 0;
-    Plan pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C, true, conv);
+    // The prologue and the ZOH variant run in the warp-specialised kernel only.
+    Plan pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C, true, conv, zoh);
     if (pl.grid * pl.n_seg > int64_t(0x7fffffff)) return SSM_ERR_SIZE;
-    // The prologue runs in the warp-specialised kernel, which needs rows TMA
-    // can describe; with L = 0 there is nothing to convolve.
-    if (conv && L > 0 && !pl.ws) return SSM_ERR_ALIGN;
+    // That kernel needs rows TMA can describe; with L = 0 there is no step.
+    if ((conv || zoh) && L > 0 && !pl.ws) return SSM_ERR_ALIGN;
 
     CUtensorMap tms[6];
     std::memset(tms, 0, sizeof(tms));
@@ -1840,7 +1917,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
                               CU_TENSOR_MAP_SWIZZLE_NONE);
         if (!tma_udz) tma_bc = false;
         if (!tma_udz) {
-            if (conv) return SSM_ERR_ALIGN;
+            if (conv || zoh) return SSM_ERR_ALIGN;
             // The tensor maps could not be encoded: plan again for plain loads.
             pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C, /*allow_tma=*/false);
             tma_bc = false;
@@ -1878,6 +1955,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     kp.conv_w = conv_w;
     kp.conv_b = conv_b;
     kp.conv_k = conv ? conv_k : 0;
+    kp.zoh = (zoh && pl.ws) ? 1 : 0;
     if (pl.n_seg == 1) return dispatch<T>(pl, pl.grid, tms, kp, stream);
 
     // Segment summaries live in stream-ordered scratch from the device's
@@ -2194,6 +2272,27 @@ int ssm_scan_fwd_bf16_h0(const uint16_t* u, const uint16_t* delta, const float* 
                         reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
                         reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
                         reinterpret_cast<bf*>(y), h_last, batch, L, dim, N, stream, false, h0);
+}
+
+int ssm_scan_fwd_zoh(const float* u, const float* delta, const float* A, const float* B,
+                     const float* C, const float* D, const float* z, const float* delta_bias,
+                     const float* h0, int softplus_flag, float* y, float* h_last, int64_t batch,
+                     int64_t L, int64_t dim, int64_t N, cudaStream_t stream) {
+    return scan_fwd<float>(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, h_last, batch,
+                           L, dim, N, stream, false, h0, nullptr, nullptr, 0, true);
+}
+
+int ssm_scan_fwd_bf16_zoh(const uint16_t* u, const uint16_t* delta, const float* A,
+                          const uint16_t* B, const uint16_t* C, const float* D,
+                          const uint16_t* z, const float* delta_bias, const float* h0,
+                          int softplus_flag, uint16_t* y, float* h_last, int64_t batch,
+                          int64_t L, int64_t dim, int64_t N, cudaStream_t stream) {
+    using bf = __nv_bfloat16;
+    return scan_fwd<bf>(reinterpret_cast<const bf*>(u), reinterpret_cast<const bf*>(delta), A,
+                        reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
+                        reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
+                        reinterpret_cast<bf*>(y), h_last, batch, L, dim, N, stream, false, h0,
+                        nullptr, nullptr, 0, true);
 }
 
 int ssm_conv_scan_fwd(const float* x, const float* conv_w, const float* conv_b, int conv_k,

@@ -46,7 +46,8 @@ SSM_KNOB_SEGMENTS = 7
 SSM_KNOB_KERNEL = 8
 
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc",
-            "ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0", "ssm_scan_step", "ssm_scan_step_bf16",
+            "ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0", "ssm_scan_fwd_zoh", "ssm_scan_fwd_bf16_zoh",
+            "ssm_scan_step", "ssm_scan_step_bf16",
             "ssm_conv_scan_fwd", "ssm_conv_scan_fwd_bf16", "ssm_scan_host_workspace_bytes",
             "ssm_scan_fwd_host", "ssm_scan_fwd_bf16_host",
             "ssm_scan_last_device_status", "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
@@ -58,7 +59,7 @@ _FWD_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp,
 for _name in ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc"):
     getattr(_lib, _name).argtypes = _FWD_ARGS
     getattr(_lib, _name).restype = ctypes.c_int
-for _name in ("ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0"):
+for _name in ("ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0", "ssm_scan_fwd_zoh", "ssm_scan_fwd_bf16_zoh"):
     getattr(_lib, _name).argtypes = _FWD_ARGS[:8] + [_vp] + _FWD_ARGS[8:]
     getattr(_lib, _name).restype = ctypes.c_int
 for _name in ("ssm_conv_scan_fwd", "ssm_conv_scan_fwd_bf16"):
@@ -176,6 +177,24 @@ def ssm_scan_fwd_bf16_host(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y
                                        stream or None)
 
 
+def ssm_scan_fwd_zoh(u, delta, A, B, C, D, z, delta_bias, h0, softplus_flag, y, h_last,
+                     batch, L, dim, N, stream) -> int:
+    """fp32 entry point with the exact zero-order-hold B; pointers are ints."""
+    return _lib.ssm_scan_fwd_zoh(u or None, delta or None, A or None, B or None, C or None,
+                                 D or None, z or None, delta_bias or None, h0 or None,
+                                 int(softplus_flag), y or None, h_last or None, batch, L, dim, N,
+                                 stream or None)
+
+
+def ssm_scan_fwd_bf16_zoh(u, delta, A, B, C, D, z, delta_bias, h0, softplus_flag, y, h_last,
+                          batch, L, dim, N, stream) -> int:
+    """bf16 entry point with the exact zero-order-hold B; pointers are ints."""
+    return _lib.ssm_scan_fwd_bf16_zoh(u or None, delta or None, A or None, B or None, C or None,
+                                      D or None, z or None, delta_bias or None, h0 or None,
+                                      int(softplus_flag), y or None, h_last or None, batch, L,
+                                      dim, N, stream or None)
+
+
 def ssm_scan_step(u, delta, A, B, C, D, z, delta_bias, softplus_flag, h, y, batch, dim, N,
                   stream) -> int:
     """fp32 one-token recurrent step (h updated in place); pointers are ints."""
@@ -235,13 +254,13 @@ def _check_io(u, delta, B, C, z, A, D, delta_bias):
 
 
 def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
-                       y=None, h_last=None, stream=None, want_h_last=True, h0=None):
+                       y=None, h_last=None, stream=None, want_h_last=True, h0=None, zoh=False):
     """Run the kernel on torch CUDA tensors.
 
     u, delta, z: (batch, L, dim); B, C: (batch, L, N); A: (dim, N) fp32;
     D, delta_bias: (dim,) fp32; h0: (batch, dim, N) fp32 initial state (None:
-    zeros).  u/delta/B/C/z are all fp32 (fp32 entry point) or all bf16 (bf16
-    entry point).  Returns (y, h_last).  Work is enqueued on ``stream``
+    zeros); zoh: the exact zero-order-hold B.  u/delta/B/C/z are all fp32
+    (fp32 entry point) or all bf16 (bf16 entry point).  Returns (y, h_last).  Work is enqueued on ``stream``
     (default: torch's current stream) without synchronising.
     """
     import torch
@@ -257,7 +276,12 @@ def selective_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softp
         h_last = torch.empty((batch, dim, N), dtype=torch.float32, device=u.device)
     if stream is None:
         stream = torch.cuda.current_stream(u.device).cuda_stream
-    if h0 is None:
+    if zoh:
+        fn = ssm_scan_fwd_bf16_zoh if bf16 else ssm_scan_fwd_zoh
+        st = fn(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                _ptr(delta_bias), _ptr(h0), int(bool(softplus)), _ptr(y), _ptr(h_last),
+                batch, L, dim, N, int(stream))
+    elif h0 is None:
         fn = ssm_scan_fwd_bf16 if bf16 else ssm_scan_fwd
         st = fn(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                 _ptr(delta_bias), int(bool(softplus)), _ptr(y), _ptr(h_last),

@@ -234,3 +234,10 @@ def test_host_call_checks(fn):
     assert fn(**args) == ssmscan.SSM_ERR_SIZE                     # workspace too small
     assert fn(**{**args, "batch": 0}) == ssmscan.SSM_OK
     assert fn(**{**args, "N": 200}) == ssmscan.SSM_ERR_UNSUPPORTED_N
+
+
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_fwd_zoh, ssm.ssm_scan_fwd_bf16_zoh])
+def test_zoh_checks(fn):
+    assert fwd_h0(fn, u=0) == ssmscan.SSM_ERR_NULL
+    assert fwd_h0(fn, h0=Q + 0x100000) == ssmscan.SSM_ERR_ALIAS
+    assert fwd_h0(fn, h0=0, batch=0) == ssmscan.SSM_OK
