@@ -482,6 +482,8 @@ def run_op(args, wl):
     """Secondary operations on one workload's shape, one JSON line each:
     conv_scan  the scan with the fused causal conv1d + SiLU prologue, timed
                beside the plain scan on the same inputs;
+    zoh_scan   the scan with the exact zero-order-hold B, timed beside the
+               Euler scan on the same inputs;
     step       the one-token recurrent step over (batch, dim, N) states,
                timed through a CUDA graph of 100 steps (device time only)."""
     import torch
@@ -502,6 +504,34 @@ def run_op(args, wl):
     rng = np.random.default_rng(1)
     es = 2 if bf else 4
     hbm_gbs, hbm_src = measured_peaks()
+    if args.op == "zoh_scan":
+        sets = [{k: dev(inp[k]) for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}
+                for _ in range(2)]
+        outs = [(torch.empty_like(s["u"]),
+                 torch.empty((wl.batch, wl.dim, wl.N), dtype=torch.float32, device="cuda"))
+                for s in sets]
+
+        def call(i, zoh):
+            s, (y, h) = sets[i & 1], outs[i & 1]
+            ssm.selective_scan_fwd(s["u"], s["delta"], s["A"], s["B"], s["C"], s["D"], s["z"],
+                                   s["delta_bias"], wl.softplus, y=y, h_last=h, zoh=zoh)
+
+        for i in range(args.warmup):
+            call(i, True)
+            call(i, False)
+        torch.cuda.synchronize()
+        ms_zoh = _events_mean_ms(lambda i: call(i, True), args.steps, stream)
+        ms_scan = _events_mean_ms(lambda i: call(i, False), args.steps, stream)
+        st = ssm.ssm_scan_last_device_status(stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(ssm.ssm_status_string(st))
+        return {
+            "op": "zoh_scan", "metric": "selective-scan fwd with exact zero-order-hold B tokens/s",
+            "value": wl.tokens / (ms_zoh * 1e-3), "unit": "tokens/s", "higher_is_better": True,
+            "ms_per_step": ms_zoh, "steps": args.steps, "warmup": args.warmup,
+            "euler_scan_ms": ms_scan, "zoh_cost_ms": ms_zoh - ms_scan,
+            "dtype": "f32", "data": "synthetic (seeded; see ssm_workloads.py)",
+            "config": config_of(wl, "inputs rotate over 2 resident copies"), "impl": "ours"}
     if args.op == "conv_scan":
         sets = [{k: dev(inp[k]) for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}
                 for _ in range(2)]
@@ -600,8 +630,8 @@ def main(argv=None):
                     help="wall seconds of oracle work per reference step")
     ap.add_argument("--clock-window", type=float, default=0.5)
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--op", choices=["scan", "conv_scan", "step"], default="scan",
-                    help="scan (the headline); conv_scan / step: secondary lines")
+    ap.add_argument("--op", choices=["scan", "conv_scan", "zoh_scan", "step"], default="scan",
+                    help="scan (the headline); conv_scan / zoh_scan / step: secondary lines")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
