@@ -493,6 +493,45 @@ CONV_PINS = {
 }
 
 
+# ---------------------------------------------------------------- backward
+def pin_bwd_loop_forward(seed=15):
+    """The autograd loop's forward equals the C oracle's."""
+    import oracle
+    from oracle.backward import selective_scan_fwd_loop
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for kw in (dict(), dict(softplus=False, bias=False, gate=False, skip=False)):
+        p = random_problem(rng, batch=2, L=7, dim=3, N=4, **kw)
+        y = selective_scan_fwd_loop(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
+                                    p["delta_bias"], p["softplus"])
+        yr, _ = _call(oracle.selective_scan_fwd, p)
+        worst = max(worst, _rel_err(y, yr))
+    return worst
+
+
+def pin_bwd_finite_differences(bwd, seed=16, eps=1e-6):
+    """Every gradient against central differences of the C oracle's forward
+    along a random direction per input: <grad_X, v> = d/de <dout, y(X + e v)>."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for kw in (dict(), dict(softplus=False, bias=True, gate=False, skip=True, a_neg=False)):
+        p = random_problem(rng, batch=2, L=6, dim=3, N=4, **kw)
+        dout = rng.standard_normal(p["u"].shape)
+        grads = bwd(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
+                    p["delta_bias"], p["softplus"], dout)
+        for name, g in grads.items():
+            v = rng.standard_normal(np.shape(p[name]))
+            plus = {**p, name: p[name] + eps * v}
+            minus = {**p, name: p[name] - eps * v}
+            yp, _ = _call(oracle.selective_scan_fwd, plus)
+            ym, _ = _call(oracle.selective_scan_fwd, minus)
+            fd = float(np.sum(dout * (yp - ym)) / (2 * eps))
+            an = float(np.sum(g * v))
+            worst = max(worst, abs(fd - an) / (1.0 + abs(fd)))
+    return worst
+
+
 ALL_PINS = {
     "bruteforce": (pin_bruteforce, 1e-12),
     "lti_direct": (pin_lti_direct, 1e-9),

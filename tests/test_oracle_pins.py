@@ -75,3 +75,26 @@ def test_oracle_zoh_pin(name):
     fn, tol = ZOH_PINS[name]
     err = fn(oracle.selective_scan_fwd)
     assert err <= tol, f"{name}: error {err:.3e} > {tol:.1e}"
+
+
+def test_oracle_backward_loop_forward():
+    from tests.oracle_pins import pin_bwd_loop_forward
+    assert pin_bwd_loop_forward() <= 1e-13
+
+
+def test_oracle_backward_finite_differences():
+    from oracle.backward import selective_scan_bwd
+    from tests.oracle_pins import pin_bwd_finite_differences
+    assert pin_bwd_finite_differences(selective_scan_bwd) <= 1e-7
+
+
+def test_oracle_backward_catches_a_wrong_gradient():
+    """The finite-difference pin rejects a gradient with one term wrong."""
+    from oracle.backward import selective_scan_bwd
+    from tests.oracle_pins import pin_bwd_finite_differences
+
+    def broken(*a):
+        g = selective_scan_bwd(*a)
+        g["B"] = g["B"] * 1.01
+        return g
+    assert pin_bwd_finite_differences(broken) > 1e-5
