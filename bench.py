@@ -484,6 +484,8 @@ def run_op(args, wl):
                beside the plain scan on the same inputs;
     zoh_scan   the scan with the exact zero-order-hold B, timed beside the
                Euler scan on the same inputs;
+    bwd        the backward pass on the workload's values in fp32, timed
+               beside the fp32 forward;
     step       the one-token recurrent step over (batch, dim, N) states,
                timed through a CUDA graph of 100 steps (device time only)."""
     import torch
@@ -504,6 +506,36 @@ def run_op(args, wl):
     rng = np.random.default_rng(1)
     es = 2 if bf else 4
     hbm_gbs, hbm_src = measured_peaks()
+    if args.op == "bwd":
+        # the backward pass works on fp32 inputs: the workload's values, widened
+        f32 = {k: (None if inp[k] is None else torch.from_numpy(
+                   np.ascontiguousarray(W.decode(inp[k]) if inp[k].dtype == np.uint16
+                                        else inp[k]).astype(np.float32)).cuda())
+               for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}
+        dy = torch.randn((wl.batch, wl.L, wl.dim), device="cuda",
+                         generator=torch.Generator(device="cuda").manual_seed(0))
+
+        def bwd_call(i):
+            ssm.selective_scan_bwd(f32["u"], f32["delta"], f32["A"], f32["B"], f32["C"], dy,
+                                   f32["D"], f32["z"], f32["delta_bias"], wl.softplus)
+
+        def fwd_call(i):
+            ssm.selective_scan_fwd(f32["u"], f32["delta"], f32["A"], f32["B"], f32["C"], f32["D"],
+                                   f32["z"], f32["delta_bias"], wl.softplus)
+
+        for i in range(args.warmup):
+            bwd_call(i)
+            fwd_call(i)
+        torch.cuda.synchronize()
+        ms_bwd = _events_mean_ms(bwd_call, args.steps, stream)
+        ms_fwd = _events_mean_ms(fwd_call, args.steps, stream)
+        return {
+            "op": "bwd", "metric": "selective-scan backward (recomputation) tokens/s",
+            "value": wl.tokens / (ms_bwd * 1e-3), "unit": "tokens/s", "higher_is_better": True,
+            "ms_per_step": ms_bwd, "steps": args.steps, "warmup": args.warmup,
+            "fp32_forward_ms": ms_fwd, "dtype": "f32",
+            "data": "synthetic (seeded; see ssm_workloads.py), values widened to fp32",
+            "config": config_of(wl, "one resident copy"), "impl": "ours"}
     if args.op == "zoh_scan":
         sets = [{k: dev(inp[k]) for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}
                 for _ in range(2)]
@@ -630,8 +662,9 @@ def main(argv=None):
                     help="wall seconds of oracle work per reference step")
     ap.add_argument("--clock-window", type=float, default=0.5)
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--op", choices=["scan", "conv_scan", "zoh_scan", "step"], default="scan",
-                    help="scan (the headline); conv_scan / zoh_scan / step: secondary lines")
+    ap.add_argument("--op", choices=["scan", "conv_scan", "zoh_scan", "step", "bwd"],
+                    default="scan",
+                    help="scan (the headline); conv_scan / zoh_scan / step / bwd: secondary lines")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

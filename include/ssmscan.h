@@ -269,6 +269,28 @@ SSM_API int ssm_scan_step_bf16(const uint16_t *u, const uint16_t *delta, const f
                   cudaStream_t stream);
 
 /*
+ * Backward pass: gradients of y of ssm_scan_fwd (fp32, Euler B, zero initial
+ * state) with respect to every input, given dy = dL/dy (batch, L, dim):
+ *   du, ddelta, dz : (batch, L, dim)     dB, dC : (batch, L, N)
+ *   dA : (dim, N)     dD, ddelta_bias : (dim,)
+ * ddelta is the gradient with respect to the raw delta (before bias and
+ * softplus).  dz, dD, ddelta_bias are written when z, D, delta_bias are given
+ * (they may be NULL otherwise).  The state is recomputed rather than stored
+ * (doyouknow.kr Mamba guide, section 3-3): the call keeps the state at every
+ * 16th step and per-block partial sums in stream-ordered scratch
+ * (cudaMallocAsync / cudaFreeAsync on `stream`, about batch * L * dim * N / 4
+ * plus 2 * batch * L * N * ceil(dim / 32) fp32 words).  Partials are folded in
+ * a fixed order, so results are deterministic.  N <= 16 (otherwise
+ * SSM_ERR_UNSUPPORTED_N).  Outputs must not overlap inputs or each other.
+ */
+SSM_API int ssm_scan_bwd(const float *u, const float *delta, const float *A,
+                 const float *B, const float *C, const float *D,
+                 const float *z, const float *delta_bias, int softplus_flag,
+                 const float *dy, float *du, float *ddelta, float *dA, float *dB,
+                 float *dC, float *dD, float *dz, float *ddelta_bias,
+                 int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream);
+
+/*
  * No-allocation variant of ssm_scan_fwd_bf16 (an engineering addition: the
  * pages describe nothing like it).  Same arguments, same kernels, same
  * results bit for bit; the only difference is where the time-segment

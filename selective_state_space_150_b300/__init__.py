@@ -6,10 +6,12 @@ The computation lives in the CUDA library ``libssmscan.so`` (C ABI declared in
 from .ssmscan import (  # noqa: F401
     SSMError,
     conv_selective_scan_fwd,
+    selective_scan_bwd,
     selective_scan_fwd,
     selective_scan_step,
     ssm_conv_scan_fwd,
     ssm_conv_scan_fwd_bf16,
+    ssm_scan_bwd,
     ssm_scan_fwd,
     ssm_scan_fwd_bf16,
     ssm_scan_fwd_bf16_host,

@@ -1480,6 +1480,214 @@ __global__ void __launch_bounds__(128) ssm_step_kernel(const StepIn<T> q) {
     q.y[i] = E::from_f(step_y(q, i, d, uu, acc));
 }
 
+// ============================================================ backward pass
+// Gradients of the scan (fp32 inputs, Euler B, zero initial state) with
+// respect to u, delta, A, B, C, D, z and delta_bias, given the gradient of y.
+// The state is recomputed instead of stored (doyouknow.kr Mamba guide,
+// section 3-3, "recomputation"): a forward pass keeps only the state at the
+// start of every kBwdTC-step chunk; the reverse pass recomputes each chunk's
+// states into shared memory and runs the adjoint recurrence backwards,
+//   lam_t = dyc_t C_t + exp(dt_{t+1} A) lam_{t+1},   dyc_t = dy_t silu(z_t),
+// from which every input's gradient follows step by step.  One warp holds
+// 32 channels of one batch row, lane = channel, all N <= 16 states per lane.
+// Gradients of the shared B and C (sums over channels) leave each warp as
+// one partial per channel tile, and dA, D, delta_bias as one partial per
+// batch row; a second kernel folds the partials in a fixed order.
+constexpr int kBwdTC = 16;
+constexpr int kBwdMaxN = 16;
+
+struct BwdParams {
+    const float* u;
+    const float* delta;
+    const float* A;
+    const float* B;
+    const float* C;
+    const float* D;
+    const float* z;
+    const float* bias;
+    const float* dy;
+    float* du;
+    float* ddelta;
+    float* dz;
+    float* ckpt;   // [batch][nchunks][dim][N]
+    float* pB;     // [ntile][batch][L][N]
+    float* pC;     // [ntile][batch][L][N]
+    float* pA;     // [batch][dim][N]
+    float* pD;     // [batch][dim]
+    float* pbias;  // [batch][dim]
+    int64_t batch, L, dim, N, ntile, nchunks;
+    int softplus;
+};
+
+// Sum of v[j] (j < NPT) over the 32 lanes, NPT values at once: each round
+// halves the values a lane keeps and swaps the other half with the partner
+// lane (NPT - 1 + log2(32 / NPT) shuffles instead of 5 NPT).  Afterwards the
+// lane holds the total for index nb, and lanes that differ only in their
+// low log2(32 / NPT) bits hold the same total.
+template <int NPT, int M, int O>
+__device__ __forceinline__ void reduce_rounds(float (&v)[NPT], int lane, int& nb) {
+    if constexpr (O >= 1) {
+        if constexpr (M > 1) {
+            constexpr int HM = M / 2;
+            const bool up = (lane & O) != 0;
+#pragma unroll
+            for (int j = 0; j < HM; ++j) {
+                const float send = up ? v[j] : v[j + HM];
+                const float keep = up ? v[j + HM] : v[j];
+                v[j] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+            }
+            if (up) nb += HM;
+            reduce_rounds<NPT, HM, O / 2>(v, lane, nb);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
+            reduce_rounds<NPT, 1, O / 2>(v, lane, nb);
+        }
+    }
+}
+
+template <int NPT>
+__global__ void __launch_bounds__(32) ssm_bwd_kernel(const BwdParams q) {
+    extern __shared__ float hs[];  // [kBwdTC][NPT][32]: states after each step of a chunk
+    const int lane = threadIdx.x;
+    const int64_t tile = blockIdx.x % q.ntile;
+    const int64_t b = blockIdx.x / q.ntile;
+    const int64_t d = tile * 32 + lane;
+    const bool ok = d < q.dim;
+    const int64_t N = q.N, L = q.L, dim = q.dim;
+    float aA[NPT], a2[NPT];
+#pragma unroll
+    for (int n = 0; n < NPT; ++n) {
+        aA[n] = (ok && n < N) ? q.A[d * N + n] : 0.f;
+        a2[n] = aA[n] * kLog2e;
+    }
+    const float Dd = (ok && q.D != nullptr) ? q.D[d] : 0.f;
+    const float bias = (ok && q.bias != nullptr) ? q.bias[d] : 0.f;
+    auto at = [&](int64_t t) { return (b * L + t) * dim + d; };
+    auto dt_of = [&](float raw) { return q.softplus ? Act<float>::softplus(raw) : raw; };
+    // one forward step of this lane's states (the forward kernels' arithmetic)
+    auto step = [&](int64_t t, float (&h)[NPT]) {
+        const float dt = dt_of((ok ? q.delta[at(t)] : 0.f) + bias);
+        const float du_ = dt * (ok ? q.u[at(t)] : 0.f);
+        const float* Bt = q.B + (b * L + t) * N;
+#pragma unroll
+        for (int n = 0; n < NPT; ++n)
+            h[n] = fmaf(ex2_approx(dt * a2[n]), h[n], du_ * (n < N ? Bt[n] : 0.f));
+    };
+
+    // ---- forward: the state at the start of every chunk
+    float h[NPT];
+#pragma unroll
+    for (int n = 0; n < NPT; ++n) h[n] = 0.f;
+    for (int64_t c = 0; c < q.nchunks; ++c) {
+        if (ok) {
+#pragma unroll
+            for (int n = 0; n < NPT; ++n)
+                if (n < N) q.ckpt[((b * q.nchunks + c) * dim + d) * N + n] = h[n];
+        }
+        const int64_t t1 = (c + 1) * kBwdTC < L ? (c + 1) * kBwdTC : L;
+        for (int64_t t = c * kBwdTC; t < t1; ++t) step(t, h);
+    }
+
+    // ---- reverse
+    float carry[NPT], gA[NPT];  // carry = exp(dt_{t+1} A) lam_{t+1}
+#pragma unroll
+    for (int n = 0; n < NPT; ++n) carry[n] = gA[n] = 0.f;
+    float gD = 0.f, gbias = 0.f;
+    for (int64_t c = q.nchunks - 1; c >= 0; --c) {
+        const int64_t t0 = c * kBwdTC;
+        const int tv = int(L - t0 < kBwdTC ? L - t0 : int64_t(kBwdTC));
+        float hstart[NPT];
+#pragma unroll
+        for (int n = 0; n < NPT; ++n) {
+            hstart[n] = (ok && n < N) ? q.ckpt[((b * q.nchunks + c) * dim + d) * N + n] : 0.f;
+            h[n] = hstart[n];
+        }
+        for (int i = 0; i < tv; ++i) {
+            step(t0 + i, h);
+#pragma unroll
+            for (int n = 0; n < NPT; ++n) hs[(i * NPT + n) * 32 + lane] = h[n];
+        }
+        __syncwarp();
+        for (int i = tv - 1; i >= 0; --i) {
+            const int64_t t = t0 + i;
+            const float raw = (ok ? q.delta[at(t)] : 0.f) + bias;
+            const float dt = dt_of(raw);
+            const float x = ok ? q.u[at(t)] : 0.f;
+            const float dyo = ok ? q.dy[at(t)] : 0.f;
+            const float* Bt = q.B + (b * L + t) * N;
+            const float* Ct = q.C + (b * L + t) * N;
+            float hcur[NPT], hprev[NPT], bb[NPT], cc[NPT];
+#pragma unroll
+            for (int n = 0; n < NPT; ++n) {
+                hcur[n] = hs[(i * NPT + n) * 32 + lane];
+                hprev[n] = i > 0 ? hs[((i - 1) * NPT + n) * 32 + lane] : hstart[n];
+                bb[n] = n < N ? Bt[n] : 0.f;
+                cc[n] = n < N ? Ct[n] : 0.f;
+            }
+            float yc = Dd * x;
+#pragma unroll
+            for (int n = 0; n < NPT; ++n) yc = fmaf(cc[n], hcur[n], yc);
+            float g = 1.f, gz = 0.f;
+            if (q.z != nullptr) {
+                const float zz = ok ? q.z[at(t)] : 0.f;
+                const float sg = 1.f / (1.f + expf(-zz));
+                g = zz * sg;
+                gz = dyo * yc * sg * (1.f + zz * (1.f - sg));  // d silu / dz
+            }
+            const float dyc = dyo * g;
+            float gdt = 0.f, gu = dyc * Dd, vB[NPT], vC[NPT];
+#pragma unroll
+            for (int n = 0; n < NPT; ++n) {
+                const float lam = fmaf(dyc, cc[n], carry[n]);
+                const float e = ex2_approx(dt * a2[n]);
+                const float eh = e * hprev[n];
+                gdt = fmaf(lam, fmaf(aA[n], eh, bb[n] * x), gdt);
+                gA[n] = fmaf(lam * dt, eh, gA[n]);
+                gu = fmaf(lam * dt, bb[n], gu);
+                vB[n] = lam * dt * x;
+                vC[n] = dyc * hcur[n];
+                carry[n] = e * lam;
+            }
+            const float gdelta = q.softplus ? gdt / (1.f + expf(-raw)) : gdt;  // softplus' = sigmoid
+            if (ok) {
+                q.du[at(t)] = gu;
+                q.ddelta[at(t)] = gdelta;
+                if (q.dz != nullptr) q.dz[at(t)] = gz;
+            }
+            gD = fmaf(dyc, x, gD);
+            gbias += gdelta;
+            // partial dB, dC of this channel tile
+            int nbB = 0, nbC = 0;
+            reduce_rounds<NPT, NPT, 16>(vB, lane, nbB);
+            reduce_rounds<NPT, NPT, 16>(vC, lane, nbC);
+            if ((lane & (32 / NPT - 1)) == 0 && nbB < N) {
+                const int64_t o = ((tile * q.batch + b) * L + t) * N;
+                q.pB[o + nbB] = vB[0];
+                q.pC[o + nbC] = vC[0];
+            }
+        }
+        __syncwarp();
+    }
+    if (ok) {
+#pragma unroll
+        for (int n = 0; n < NPT; ++n)
+            if (n < N) q.pA[(b * dim + d) * N + n] = gA[n];
+        q.pD[b * dim + d] = gD;
+        q.pbias[b * dim + d] = gbias;
+    }
+}
+
+// out[i] = sum_k in[k * count + i], k = 0 .. parts-1 in order.
+__global__ void __launch_bounds__(256)
+    ssm_fold_kernel(const float* __restrict__ in, float* __restrict__ out, int64_t parts,
+                    int64_t count) {
+    const int64_t i = int64_t(blockIdx.x) * 256 + threadIdx.x;
+    if (i >= count) return;
+    float acc = 0.f;
+    for (int64_t k = 0; k < parts; ++k) acc += in[k * count + i];
+    out[i] = acc;
+}
+
 // ------------------------------------------------------------------ host side
 std::atomic<int64_t> g_wait_ns{2000000000LL};
 std::atomic<int> g_force_timeout{0};
@@ -2230,6 +2438,102 @@ int scan_fwd_host(const T* u, const T* delta, const float* A, const T* B, const 
     return st;
 }
 
+// Backward: checks, scratch, the two kernels.
+int scan_bwd(const float* u, const float* delta, const float* A, const float* B, const float* C,
+             const float* D, const float* z, const float* delta_bias, int softplus_flag,
+             const float* dy, float* du, float* ddelta, float* dA, float* dB, float* dC,
+             float* dD, float* dz, float* ddelta_bias, int64_t batch, int64_t L, int64_t dim,
+             int64_t N, cudaStream_t stream) {
+    if (batch < 0 || L < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
+    if (N > kBwdMaxN) return SSM_ERR_UNSUPPORTED_N;
+    int64_t n_bld, n_bln, n_dn, n_bdn, tmp;
+    if (!mul_ok(batch, L, &tmp) || !mul_ok(tmp, dim, &n_bld) || !mul_ok(tmp, N, &n_bln) ||
+        !mul_ok(dim, N, &n_dn) || !mul_ok(batch, dim, &tmp) || !mul_ok(tmp, N, &n_bdn))
+        return SSM_ERR_SIZE;
+    const bool any = batch > 0 && L > 0 && dim > 0;
+    if (any && (!u || !delta || !dy || !du || !ddelta || !B || !C || !dB || !dC))
+        return SSM_ERR_NULL;
+    if (dim > 0 && (!A || !dA)) return SSM_ERR_NULL;
+    if ((D && !dD) || (z && !dz) || (delta_bias && !ddelta_bias)) return SSM_ERR_NULL;
+    for (const void* ptr : {(const void*)u, (const void*)delta, (const void*)A, (const void*)B,
+                            (const void*)C, (const void*)D, (const void*)z,
+                            (const void*)delta_bias, (const void*)dy, (const void*)du,
+                            (const void*)ddelta, (const void*)dA, (const void*)dB,
+                            (const void*)dC, (const void*)dD, (const void*)dz,
+                            (const void*)ddelta_bias})
+        if (ptr && !aligned(ptr, 4)) return SSM_ERR_ALIGN;
+    const int64_t by = n_bld * 4, bn = n_bln * 4;
+    const struct { const void* p; int64_t n; } ins[] = {
+        {u, by}, {delta, by}, {z, z ? by : 0}, {dy, by}, {B, bn}, {C, bn}, {A, n_dn * 4},
+        {D, D ? dim * 4 : 0}, {delta_bias, delta_bias ? dim * 4 : 0}};
+    const struct { const void* p; int64_t n; } outs[] = {
+        {du, by}, {ddelta, by}, {dz, dz ? by : 0}, {dB, bn}, {dC, bn}, {dA, n_dn * 4},
+        {dD, dD ? dim * 4 : 0}, {ddelta_bias, ddelta_bias ? dim * 4 : 0}};
+    for (const auto& o : outs) {
+        for (const auto& in : ins)
+            if (overlaps(o.p, o.n, in.p, in.n)) return SSM_ERR_ALIAS;
+        for (const auto& o2 : outs)
+            if (&o2 != &o && overlaps(o.p, o.n, o2.p, o2.n)) return SSM_ERR_ALIAS;
+    }
+    if (batch == 0 || dim == 0) return SSM_OK;
+    const int64_t ntile = (dim + 31) / 32;
+    const int64_t nchunks = (L + kBwdTC - 1) / kBwdTC;
+    if (batch * ntile > int64_t(0x7fffffff)) return SSM_ERR_SIZE;
+    if (L == 0) {  // no step: every gradient is zero
+        for (const auto& o : outs)
+            if (o.p && o.n > 0 &&
+                cudaMemsetAsync(const_cast<void*>(o.p), 0, size_t(o.n), stream) != cudaSuccess)
+                return SSM_ERR_LAUNCH;
+        return SSM_OK;
+    }
+    const size_t n_ck = size_t(batch * nchunks) * size_t(n_dn);
+    const size_t n_p = size_t(ntile) * size_t(n_bln);
+    const size_t n_total = n_ck + 2 * n_p + size_t(n_bdn) + 2 * size_t(batch * dim);
+    void* scratch = nullptr;
+    if (cudaMallocAsync(&scratch, n_total * 4, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SSM_ERR_NOMEM;
+    }
+    float* f = static_cast<float*>(scratch);
+    BwdParams q;
+    q.u = u; q.delta = delta; q.A = A; q.B = B; q.C = C; q.D = D; q.z = z; q.bias = delta_bias;
+    q.dy = dy; q.du = du; q.ddelta = ddelta; q.dz = dz;
+    q.ckpt = f;
+    q.pB = f + n_ck;
+    q.pC = q.pB + n_p;
+    q.pA = q.pC + n_p;
+    q.pD = q.pA + n_bdn;
+    q.pbias = q.pD + batch * dim;
+    q.batch = batch; q.L = L; q.dim = dim; q.N = N; q.ntile = ntile; q.nchunks = nchunks;
+    q.softplus = softplus_flag ? 1 : 0;
+    // every (tile, b, t, n < N) entry of the partial dB / dC is written by
+    // exactly one lane
+    const int npt = supported_npt(N);
+    const size_t smem = size_t(kBwdTC) * size_t(npt) * 32 * 4;
+    const dim3 grid = dim3(unsigned(batch * ntile)), block = dim3(32);
+    switch (npt) {
+        case 1: ssm_bwd_kernel<1><<<grid, block, smem, stream>>>(q); break;
+        case 2: ssm_bwd_kernel<2><<<grid, block, smem, stream>>>(q); break;
+        case 4: ssm_bwd_kernel<4><<<grid, block, smem, stream>>>(q); break;
+        case 8: ssm_bwd_kernel<8><<<grid, block, smem, stream>>>(q); break;
+        default: ssm_bwd_kernel<16><<<grid, block, smem, stream>>>(q); break;
+    }
+    int st = cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    auto fold = [&](const float* in, float* out, int64_t parts, int64_t count) {
+        if (st != SSM_OK || out == nullptr || count == 0) return;
+        ssm_fold_kernel<<<dim3(unsigned((count + 255) / 256)), dim3(256), 0, stream>>>(
+            in, out, parts, count);
+        if (cudaGetLastError() != cudaSuccess) st = SSM_ERR_LAUNCH;
+    };
+    fold(q.pB, dB, ntile, n_bln);
+    fold(q.pC, dC, ntile, n_bln);
+    fold(q.pA, dA, batch, n_dn);
+    fold(q.pD, D ? dD : nullptr, batch, dim);
+    fold(q.pbias, delta_bias ? ddelta_bias : nullptr, batch, dim);
+    if (cudaFreeAsync(scratch, stream) != cudaSuccess && st == SSM_OK) st = SSM_ERR_LAUNCH;
+    return st;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -2349,6 +2653,15 @@ int ssm_scan_fwd_bf16_host(const uint16_t* u, const uint16_t* delta, const float
                              reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
                              reinterpret_cast<bf*>(y), h_last, batch, L, dim, N, workspace,
                              workspace_bytes, stream);
+}
+
+int ssm_scan_bwd(const float* u, const float* delta, const float* A, const float* B,
+                 const float* C, const float* D, const float* z, const float* delta_bias,
+                 int softplus_flag, const float* dy, float* du, float* ddelta, float* dA,
+                 float* dB, float* dC, float* dD, float* dz, float* ddelta_bias, int64_t batch,
+                 int64_t L, int64_t dim, int64_t N, cudaStream_t stream) {
+    return scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, ddelta, dA, dB,
+                    dC, dD, dz, ddelta_bias, batch, L, dim, N, stream);
 }
 
 int ssm_scan_step(const float* u, const float* delta, const float* A, const float* B,

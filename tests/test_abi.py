@@ -241,3 +241,26 @@ def test_zoh_checks(fn):
     assert fwd_h0(fn, u=0) == ssmscan.SSM_ERR_NULL
     assert fwd_h0(fn, h0=Q + 0x100000) == ssmscan.SSM_ERR_ALIAS
     assert fwd_h0(fn, h0=0, batch=0) == ssmscan.SSM_OK
+
+
+# ---------------------------------------------------------------- backward
+def bwd(**kw):
+    args = dict(u=P, delta=P + 0x100000, A=P + 0x200000, B=P + 0x300000, C=P + 0x400000, D=0,
+                z=0, delta_bias=0, softplus_flag=0, dy=P + 0x500000, du=Q, ddelta=Q + 0x100000,
+                dA=Q + 0x200000, dB=Q + 0x300000, dC=Q + 0x400000, dD=0, dz=0, ddelta_bias=0,
+                batch=2, L=8, dim=16, N=4, stream=0)
+    args.update(kw)
+    return ssm.ssm_scan_bwd(**args)
+
+
+def test_backward_checks():
+    for k in ("u", "delta", "dy", "du", "ddelta", "A", "dA", "B", "C", "dB", "dC"):
+        assert bwd(**{k: 0}) == ssmscan.SSM_ERR_NULL, k
+    assert bwd(D=P + 0x600000) == ssmscan.SSM_ERR_NULL            # D given, dD missing
+    assert bwd(z=P + 0x600000) == ssmscan.SSM_ERR_NULL            # z given, dz missing
+    assert bwd(N=17) == ssmscan.SSM_ERR_UNSUPPORTED_N
+    assert bwd(L=-1) == ssmscan.SSM_ERR_SIZE
+    assert bwd(du=P) == ssmscan.SSM_ERR_ALIAS                     # du is u
+    assert bwd(dB=Q + 0x40) == ssmscan.SSM_ERR_ALIAS              # dB inside du
+    assert bwd(du=Q + 2) == ssmscan.SSM_ERR_ALIGN
+    assert bwd(batch=0) == ssmscan.SSM_OK
