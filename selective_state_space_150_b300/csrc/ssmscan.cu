@@ -1545,10 +1545,39 @@ __device__ __forceinline__ void reduce_rounds(float (&v)[NPT], int lane, int& nb
     }
 }
 
-template <int NPT>
-__global__ void __launch_bounds__(32) ssm_bwd_kernel(const BwdParams q) {
-    extern __shared__ float hs[];  // [kBwdTC][NPT][32]: states after each step of a chunk
-    const int lane = threadIdx.x;
+// Block = WS warps over the same 32 channels (lane = channel); warp sg holds
+// states sg*4 .. sg*4 + 3.  Each chunk's inputs are first staged in shared
+// memory by the whole block (coalesced, all loads in flight at once); the
+// per-step work then reads only shared memory.  The per-(step, channel)
+// gradients need sums over all states: each warp leaves its share in shared
+// memory and, after every chunk, the block adds the WS shares in a fixed
+// order.
+constexpr int kBwdNPT = 4;
+
+template <int WS>
+struct BwdSmem {
+    static constexpr int NP = WS * kBwdNPT, T = kBwdTC;
+    // floats, in this order
+    static constexpr int hs = 0;                          // [WS][T][4][32] states after each step
+    static constexpr int part = hs + WS * T * 4 * 32;     // [WS][T][3][32] per-warp shares
+    static constexpr int red = part + WS * T * 3 * 32;    // [WS][2][32]
+    static constexpr int raw = red + WS * 2 * 32;         // [T][32] delta + bias
+    static constexpr int dt = raw + T * 32;               // [T][32]
+    static constexpr int x = dt + T * 32;                 // [T][32] u
+    static constexpr int dy = x + T * 32;                 // [T][32]
+    static constexpr int zz = dy + T * 32;                // [T][32]
+    static constexpr int Bs = zz + T * 32;                // [T][NP]
+    static constexpr int Cs = Bs + T * NP;                // [T][NP]
+    static constexpr int total = Cs + T * NP;
+};
+
+template <int WS>
+__global__ void __launch_bounds__(WS * 32) ssm_bwd_kernel(const BwdParams q) {
+    constexpr int NPT = kBwdNPT, NT = WS * 32;
+    using SM = BwdSmem<WS>;
+    constexpr int NP = SM::NP;
+    extern __shared__ float sm[];
+    const int tid = threadIdx.x, lane = tid & 31, sg = tid >> 5;
     const int64_t tile = blockIdx.x % q.ntile;
     const int64_t b = blockIdx.x / q.ntile;
     const int64_t d = tile * 32 + lane;
@@ -1556,124 +1585,193 @@ __global__ void __launch_bounds__(32) ssm_bwd_kernel(const BwdParams q) {
     const int64_t N = q.N, L = q.L, dim = q.dim;
     float aA[NPT], a2[NPT];
 #pragma unroll
-    for (int n = 0; n < NPT; ++n) {
-        aA[n] = (ok && n < N) ? q.A[d * N + n] : 0.f;
-        a2[n] = aA[n] * kLog2e;
+    for (int j = 0; j < NPT; ++j) {
+        const int64_t n = int64_t(sg) * NPT + j;
+        aA[j] = (ok && n < N) ? q.A[d * N + n] : 0.f;
+        a2[j] = aA[j] * kLog2e;
     }
     const float Dd = (ok && q.D != nullptr) ? q.D[d] : 0.f;
     const float bias = (ok && q.bias != nullptr) ? q.bias[d] : 0.f;
-    auto at = [&](int64_t t) { return (b * L + t) * dim + d; };
-    auto dt_of = [&](float raw) { return q.softplus ? Act<float>::softplus(raw) : raw; };
-    // one forward step of this lane's states (the forward kernels' arithmetic)
-    auto step = [&](int64_t t, float (&h)[NPT]) {
-        const float dt = dt_of((ok ? q.delta[at(t)] : 0.f) + bias);
-        const float du_ = dt * (ok ? q.u[at(t)] : 0.f);
-        const float* Bt = q.B + (b * L + t) * N;
+    float* const s_raw = sm + SM::raw;
+    float* const s_dt = sm + SM::dt;
+    float* const s_x = sm + SM::x;
+    float* const s_dy = sm + SM::dy;
+    float* const s_z = sm + SM::zz;
+    float* const s_B = sm + SM::Bs;
+    float* const s_C = sm + SM::Cs;
+
+    // Stage steps t0 .. t0 + tv - 1 (zeros past tv or past dim).  rev: also
+    // dy, z and C for the reverse pass.
+    auto stage = [&](int64_t t0, int tv, bool rev) {
+        for (int i = sg; i < kBwdTC; i += WS) {
+            const bool in = ok && i < tv;
+            const int64_t o = (b * L + t0 + i) * dim + d;
+            const float r = (in ? q.delta[o] : 0.f) + (in ? bias : 0.f);
+            s_raw[i * 32 + lane] = r;
+            s_dt[i * 32 + lane] = in ? (q.softplus ? Act<float>::softplus(r) : r) : 0.f;
+            s_x[i * 32 + lane] = in ? q.u[o] : 0.f;
+            if (rev) {
+                s_dy[i * 32 + lane] = in ? q.dy[o] : 0.f;
+                s_z[i * 32 + lane] = (in && q.z != nullptr) ? q.z[o] : 0.f;
+            }
+        }
+        for (int k = tid; k < kBwdTC * NP; k += NT) {
+            const int i = k / NP, n = k % NP;
+            const bool in = i < tv && n < N;
+            const int64_t o = (b * L + t0 + i) * N + n;
+            s_B[k] = in ? q.B[o] : 0.f;
+            if (rev) s_C[k] = in ? q.C[o] : 0.f;
+        }
+    };
+    // one forward step of this warp's states from the staged chunk
+    auto step = [&](int i, float (&h)[NPT]) {
+        const float dt = s_dt[i * 32 + lane];
+        const float du_ = dt * s_x[i * 32 + lane];
+        const float* const bb = s_B + i * NP + sg * NPT;
 #pragma unroll
-        for (int n = 0; n < NPT; ++n)
-            h[n] = fmaf(ex2_approx(dt * a2[n]), h[n], du_ * (n < N ? Bt[n] : 0.f));
+        for (int j = 0; j < NPT; ++j) h[j] = fmaf(ex2_approx(dt * a2[j]), h[j], du_ * bb[j]);
+    };
+    auto ck = [&](int64_t c, int j) {
+        return ((b * q.nchunks + c) * dim + d) * N + int64_t(sg) * NPT + j;
     };
 
     // ---- forward: the state at the start of every chunk
     float h[NPT];
 #pragma unroll
-    for (int n = 0; n < NPT; ++n) h[n] = 0.f;
+    for (int j = 0; j < NPT; ++j) h[j] = 0.f;
     for (int64_t c = 0; c < q.nchunks; ++c) {
+        const int64_t t0 = c * kBwdTC;
+        const int tv = int(L - t0 < kBwdTC ? L - t0 : int64_t(kBwdTC));
         if (ok) {
 #pragma unroll
-            for (int n = 0; n < NPT; ++n)
-                if (n < N) q.ckpt[((b * q.nchunks + c) * dim + d) * N + n] = h[n];
+            for (int j = 0; j < NPT; ++j)
+                if (int64_t(sg) * NPT + j < N) q.ckpt[ck(c, j)] = h[j];
         }
-        const int64_t t1 = (c + 1) * kBwdTC < L ? (c + 1) * kBwdTC : L;
-        for (int64_t t = c * kBwdTC; t < t1; ++t) step(t, h);
+        stage(t0, tv, false);
+        __syncthreads();
+        for (int i = 0; i < tv; ++i) step(i, h);
+        __syncthreads();
     }
 
     // ---- reverse
     float carry[NPT], gA[NPT];  // carry = exp(dt_{t+1} A) lam_{t+1}
 #pragma unroll
-    for (int n = 0; n < NPT; ++n) carry[n] = gA[n] = 0.f;
+    for (int j = 0; j < NPT; ++j) carry[j] = gA[j] = 0.f;
     float gD = 0.f, gbias = 0.f;
+    float* const myh = sm + SM::hs + sg * kBwdTC * NPT * 32;
+    float* const part = sm + SM::part;
     for (int64_t c = q.nchunks - 1; c >= 0; --c) {
         const int64_t t0 = c * kBwdTC;
         const int tv = int(L - t0 < kBwdTC ? L - t0 : int64_t(kBwdTC));
         float hstart[NPT];
 #pragma unroll
-        for (int n = 0; n < NPT; ++n) {
-            hstart[n] = (ok && n < N) ? q.ckpt[((b * q.nchunks + c) * dim + d) * N + n] : 0.f;
-            h[n] = hstart[n];
+        for (int j = 0; j < NPT; ++j) {
+            hstart[j] = (ok && int64_t(sg) * NPT + j < N) ? q.ckpt[ck(c, j)] : 0.f;
+            h[j] = hstart[j];
         }
+        stage(t0, tv, true);
+        __syncthreads();
         for (int i = 0; i < tv; ++i) {
-            step(t0 + i, h);
+            step(i, h);
 #pragma unroll
-            for (int n = 0; n < NPT; ++n) hs[(i * NPT + n) * 32 + lane] = h[n];
+            for (int j = 0; j < NPT; ++j) myh[(i * NPT + j) * 32 + lane] = h[j];
         }
         __syncwarp();
         for (int i = tv - 1; i >= 0; --i) {
-            const int64_t t = t0 + i;
-            const float raw = (ok ? q.delta[at(t)] : 0.f) + bias;
-            const float dt = dt_of(raw);
-            const float x = ok ? q.u[at(t)] : 0.f;
-            const float dyo = ok ? q.dy[at(t)] : 0.f;
-            const float* Bt = q.B + (b * L + t) * N;
-            const float* Ct = q.C + (b * L + t) * N;
-            float hcur[NPT], hprev[NPT], bb[NPT], cc[NPT];
+            const float dt = s_dt[i * 32 + lane];
+            const float x = s_x[i * 32 + lane];
+            const float zz = s_z[i * 32 + lane];
+            const float g = q.z != nullptr ? zz / (1.f + expf(-zz)) : 1.f;
+            const float dyc = s_dy[i * 32 + lane] * g;
+            const float* const bb = s_B + i * NP + sg * NPT;
+            const float* const cc = s_C + i * NP + sg * NPT;
+            float vB[NPT], vC[NPT];
+            float yc = 0.f, gdt = 0.f, gu = 0.f;
 #pragma unroll
-            for (int n = 0; n < NPT; ++n) {
-                hcur[n] = hs[(i * NPT + n) * 32 + lane];
-                hprev[n] = i > 0 ? hs[((i - 1) * NPT + n) * 32 + lane] : hstart[n];
-                bb[n] = n < N ? Bt[n] : 0.f;
-                cc[n] = n < N ? Ct[n] : 0.f;
+            for (int j = 0; j < NPT; ++j) {
+                const float hcur = myh[(i * NPT + j) * 32 + lane];
+                const float hprev = i > 0 ? myh[((i - 1) * NPT + j) * 32 + lane] : hstart[j];
+                yc = fmaf(cc[j], hcur, yc);
+                const float lam = fmaf(dyc, cc[j], carry[j]);
+                const float e = ex2_approx(dt * a2[j]);
+                const float eh = e * hprev;
+                gdt = fmaf(lam, fmaf(aA[j], eh, bb[j] * x), gdt);
+                gA[j] = fmaf(lam * dt, eh, gA[j]);
+                gu = fmaf(lam * dt, bb[j], gu);
+                vB[j] = lam * dt * x;
+                vC[j] = dyc * hcur;
+                carry[j] = e * lam;
             }
-            float yc = Dd * x;
-#pragma unroll
-            for (int n = 0; n < NPT; ++n) yc = fmaf(cc[n], hcur[n], yc);
-            float g = 1.f, gz = 0.f;
-            if (q.z != nullptr) {
-                const float zz = ok ? q.z[at(t)] : 0.f;
-                const float sg = 1.f / (1.f + expf(-zz));
-                g = zz * sg;
-                gz = dyo * yc * sg * (1.f + zz * (1.f - sg));  // d silu / dz
-            }
-            const float dyc = dyo * g;
-            float gdt = 0.f, gu = dyc * Dd, vB[NPT], vC[NPT];
-#pragma unroll
-            for (int n = 0; n < NPT; ++n) {
-                const float lam = fmaf(dyc, cc[n], carry[n]);
-                const float e = ex2_approx(dt * a2[n]);
-                const float eh = e * hprev[n];
-                gdt = fmaf(lam, fmaf(aA[n], eh, bb[n] * x), gdt);
-                gA[n] = fmaf(lam * dt, eh, gA[n]);
-                gu = fmaf(lam * dt, bb[n], gu);
-                vB[n] = lam * dt * x;
-                vC[n] = dyc * hcur[n];
-                carry[n] = e * lam;
-            }
-            const float gdelta = q.softplus ? gdt / (1.f + expf(-raw)) : gdt;  // softplus' = sigmoid
-            if (ok) {
-                q.du[at(t)] = gu;
-                q.ddelta[at(t)] = gdelta;
-                if (q.dz != nullptr) q.dz[at(t)] = gz;
-            }
-            gD = fmaf(dyc, x, gD);
-            gbias += gdelta;
-            // partial dB, dC of this channel tile
+            float* const pp = part + ((sg * kBwdTC + i) * 3) * 32 + lane;
+            pp[0] = yc;
+            pp[32] = gdt;
+            pp[64] = gu;
             int nbB = 0, nbC = 0;
             reduce_rounds<NPT, NPT, 16>(vB, lane, nbB);
             reduce_rounds<NPT, NPT, 16>(vC, lane, nbC);
-            if ((lane & (32 / NPT - 1)) == 0 && nbB < N) {
-                const int64_t o = ((tile * q.batch + b) * L + t) * N;
-                q.pB[o + nbB] = vB[0];
-                q.pC[o + nbC] = vC[0];
+            const int64_t n = int64_t(sg) * NPT + nbB;
+            if ((lane & (32 / NPT - 1)) == 0 && n < N) {
+                const int64_t o = ((tile * q.batch + b) * L + t0 + i) * N;
+                q.pB[o + n] = vB[0];
+                q.pC[o + int64_t(sg) * NPT + nbC] = vC[0];
             }
         }
-        __syncwarp();
+        __syncthreads();
+        // the chunk's per-(step, channel) gradients: warp sg takes steps sg, sg + WS, ...
+        for (int i = sg; i < tv; i += WS) {
+            float yc = 0.f, gdt = 0.f, gu = 0.f;
+#pragma unroll
+            for (int w = 0; w < WS; ++w) {
+                const float* const pp = part + ((w * kBwdTC + i) * 3) * 32 + lane;
+                yc += pp[0];
+                gdt += pp[32];
+                gu += pp[64];
+            }
+            const float raw = s_raw[i * 32 + lane];
+            const float x = s_x[i * 32 + lane];
+            const float dyo = s_dy[i * 32 + lane];
+            float g = 1.f, gz = 0.f;
+            yc = fmaf(Dd, x, yc);
+            if (q.z != nullptr) {
+                const float zz = s_z[i * 32 + lane];
+                const float sgm = 1.f / (1.f + expf(-zz));
+                g = zz * sgm;
+                gz = dyo * yc * sgm * (1.f + zz * (1.f - sgm));  // d silu / dz
+            }
+            const float dyc = dyo * g;
+            gu = fmaf(dyc, Dd, gu);
+            const float gdelta = q.softplus ? gdt / (1.f + expf(-raw)) : gdt;  // softplus' = sigmoid
+            if (ok) {
+                const int64_t o = (b * L + t0 + i) * dim + d;
+                q.du[o] = gu;
+                q.ddelta[o] = gdelta;
+                if (q.dz != nullptr) q.dz[o] = gz;
+            }
+            gD = fmaf(dyc, x, gD);
+            gbias += gdelta;
+        }
+        __syncthreads();
     }
     if (ok) {
 #pragma unroll
-        for (int n = 0; n < NPT; ++n)
-            if (n < N) q.pA[(b * dim + d) * N + n] = gA[n];
-        q.pD[b * dim + d] = gD;
-        q.pbias[b * dim + d] = gbias;
+        for (int j = 0; j < NPT; ++j) {
+            const int64_t n = int64_t(sg) * NPT + j;
+            if (n < N) q.pA[(b * dim + d) * N + n] = gA[j];
+        }
+    }
+    float* const red = sm + SM::red;
+    red[(sg * 2) * 32 + lane] = gD;
+    red[(sg * 2 + 1) * 32 + lane] = gbias;
+    __syncthreads();
+    if (sg == 0 && ok) {
+        float sD = 0.f, sb = 0.f;
+#pragma unroll
+        for (int w = 0; w < WS; ++w) {
+            sD += red[(w * 2) * 32 + lane];
+            sb += red[(w * 2 + 1) * 32 + lane];
+        }
+        q.pD[b * dim + d] = sD;
+        q.pbias[b * dim + d] = sb;
     }
 }
 
@@ -2508,15 +2606,34 @@ int scan_bwd(const float* u, const float* delta, const float* A, const float* B,
     q.softplus = softplus_flag ? 1 : 0;
     // every (tile, b, t, n < N) entry of the partial dB / dC is written by
     // exactly one lane
-    const int npt = supported_npt(N);
-    const size_t smem = size_t(kBwdTC) * size_t(npt) * 32 * 4;
-    const dim3 grid = dim3(unsigned(batch * ntile)), block = dim3(32);
-    switch (npt) {
-        case 1: ssm_bwd_kernel<1><<<grid, block, smem, stream>>>(q); break;
-        case 2: ssm_bwd_kernel<2><<<grid, block, smem, stream>>>(q); break;
-        case 4: ssm_bwd_kernel<4><<<grid, block, smem, stream>>>(q); break;
-        case 8: ssm_bwd_kernel<8><<<grid, block, smem, stream>>>(q); break;
-        default: ssm_bwd_kernel<16><<<grid, block, smem, stream>>>(q); break;
+    const int ws = N <= 4 ? 1 : (N <= 8 ? 2 : 4);  // warps of kBwdNPT states per 32 channels
+    const size_t smem = size_t(ws == 1 ? BwdSmem<1>::total
+                                       : (ws == 2 ? BwdSmem<2>::total : BwdSmem<4>::total)) * 4;
+    const dim3 grid = dim3(unsigned(batch * ntile)), block = dim3(unsigned(32 * ws));
+    auto launch = [&](auto kern) {
+        // dynamic shared memory above 48 KB needs the opt-in (per device)
+        static std::atomic<size_t> configured[64];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return false;
+        if (configured[dev & 63].load() < smem) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     int(smem)) != cudaSuccess)
+                return false;
+            configured[dev & 63].store(smem);
+        }
+        kern<<<grid, block, smem, stream>>>(q);
+        return true;
+    };
+    bool launched;
+    switch (ws) {
+        case 1: launched = launch(ssm_bwd_kernel<1>); break;
+        case 2: launched = launch(ssm_bwd_kernel<2>); break;
+        default: launched = launch(ssm_bwd_kernel<4>); break;
+    }
+    if (!launched) {
+        (void)cudaGetLastError();
+        (void)cudaFreeAsync(scratch, stream);
+        return SSM_ERR_LAUNCH;
     }
     int st = cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
     auto fold = [&](const float* in, float* out, int64_t parts, int64_t count) {
