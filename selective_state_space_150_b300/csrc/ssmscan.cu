@@ -860,16 +860,18 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
 //   producer (1 warp)   TMA loads of chunk k into ring stage k % stages, once
 //                       the prepare warps released that stage (EMPTY)
 //   prepare  (2 warps)  dt, dt*u and widened B, C of chunk k into buffer
-//                       k & 1 (FULL), once chunk k-2 is finished (PEMPTY)
+//                       k % kBufs (FULL), once chunk k - kBufs is finished
+//                       (PEMPTY)
 //   scan     (NSW)      the recurrence of chunk k (lane = channel, warp =
 //                       channel tile x state group), partials into s_part
-//                       buffer k & 1 (DONE)
+//                       buffer k % kBufs (DONE)
 //   finish   (2 warps)  y of chunk k from the partials and the chunk's u, z
 //                       in the ring (gate and skip), into an output tile
-//                       stored by TMA; then buffer k & 1 is free (PEMPTY)
+//                       stored by TMA; then buffer k % kBufs is free (PEMPTY)
 // A ring stage is refilled once the prepare and the finish warps are done
 // with it (EMPTY).
-// Every stage may run up to two chunks ahead of the next.  Each wait is
+// Every role may run up to kBufs chunks ahead of the next, which absorbs the
+// roles' uneven timing from chunk to chunk.  Each wait is
 // bounded and also gives up once another warp has raised the block's abort
 // flag; the only named barriers are among the finish warps, which all run
 // the same trip count and vote on aborting.
@@ -907,6 +909,8 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
     return r != 0;
 }
 
+constexpr int kBufs = 3;  // buffers between the prepare, scan and finish roles
+
 template <typename T, int NPT, int WS, int TC>
 struct GeoW {
     static constexpr int ES = int(sizeof(T));
@@ -934,13 +938,13 @@ struct GeoW {
 //             with the convolution prologue the u tile is the x tile, TC +
 //             kConvHalo rows from step t0 - kConvHalo, each column block
 //             padded to a multiple of 1024 bytes
-//   s_B, s_C  2 x [TC][NP] fp32        (summary: no s_C)
-//   s_dd      2 x [TC][DT] float2      (dt, dt*u)
-//   s_u       2 x [TC][DT] fp32        (prologue only: u for the skip term)
-//   s_part    2 x [WS][TC][DT] fp32                        (summary: none)
-//   s_y       2 x tile                                     (summary: none)
-//   barriers  TMA[kMaxStages], EMPTY[kMaxStages], FULL[2], DONE[2], PEMPTY[2],
-//             and one that nothing completes
+//   s_B, s_C  kBufs x [TC][NP] fp32        (summary: no s_C)
+//   s_dd      kBufs x [TC][DT] float2      (dt, dt*u)
+//   s_u       kBufs x [TC][DT] fp32        (prologue only: u for the skip term)
+//   s_part    kBufs x [WS][TC][DT] fp32                        (summary: none)
+//   s_y       2 x tile                                         (summary: none)
+//   barriers  TMA[kMaxStages], EMPTY[kMaxStages], FULL[kBufs], DONE[kBufs],
+//             PEMPTY[kBufs], and one that nothing completes
 template <typename T, int NPT, int WS, int TC, bool SUM>
 struct LayoutW {
     using G = GeoW<T, NPT, WS, TC>;
@@ -958,11 +962,11 @@ struct LayoutW {
         part = round1k(size_t(WS) * TC * G::DT * 4);
         off_raw = 0;
         off_bf = off_raw + size_t(stages) * stage;
-        off_cf = off_bf + 2 * bc;
-        off_dd = off_cf + (SUM ? 0 : 2 * bc);
-        off_u = off_dd + 2 * dd;
-        off_part = off_u + 2 * ub;
-        off_y = off_part + (SUM ? 0 : 2 * part);
+        off_cf = off_bf + kBufs * bc;
+        off_dd = off_cf + (SUM ? 0 : kBufs * bc);
+        off_u = off_dd + kBufs * dd;
+        off_part = off_u + kBufs * ub;
+        off_y = off_part + (SUM ? 0 : kBufs * part);
         off_bar = off_y + (SUM ? 0 : 2 * G::TILE);
         total = off_bar + 256;
     }
@@ -1024,9 +1028,10 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     auto bar_tma = [=](int s) { return bar0 + 8 * s; };
     auto bar_empty = [=](int s) { return bar0 + 8 * (kMaxStages + s); };
     auto bar_full = [=](int k) { return bar0 + 8 * (2 * kMaxStages + k); };
-    auto bar_done = [=](int k) { return bar0 + 8 * (2 * kMaxStages + 2 + k); };
-    auto bar_pempty = [=](int k) { return bar0 + 8 * (2 * kMaxStages + 4 + k); };
-    const uint32_t bar_never = bar0 + 8 * (2 * kMaxStages + 6);
+    auto bar_done = [=](int k) { return bar0 + 8 * (2 * kMaxStages + kBufs + k); };
+    auto bar_pempty = [=](int k) { return bar0 + 8 * (2 * kMaxStages + 2 * kBufs + k); };
+    const uint32_t bar_never = bar0 + 8 * (2 * kMaxStages + 3 * kBufs);
+    static_assert(8 * (2 * kMaxStages + 3 * kBufs + 1) <= 256, "barrier area");
 
     const bool has_z = p.z != nullptr && !summary;
     const int64_t nchunks = (L + TC - 1) / TC;
@@ -1039,7 +1044,7 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
             mbar_init(bar_tma(s), 1);
             mbar_init(bar_empty(s), G::NPW + G::NQW);
         }
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < kBufs; ++k) {
             mbar_init(bar_full(k), G::NPW);
             mbar_init(bar_done(k), G::NSW);
             mbar_init(bar_pempty(k), G::NQW);
@@ -1085,9 +1090,10 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
         }
         double sdt_seg = 0.0;
         (void)sdt_seg;
+        int bf = 0;        // buffer of chunk k: k % kBufs
+        uint32_t par = 0;  // parity of its use: (k / kBufs) & 1
         for (int64_t k = 0; k < nloc; ++k) {
-            const int bf = int(k & 1);
-            if (!mbar_wait_or_abort(bar_full(bf), uint32_t(k >> 1) & 1u, p.wait_ns, abort_flag)) {
+            if (!mbar_wait_or_abort(bar_full(bf), par, p.wait_ns, abort_flag)) {
                 give_up();
                 return;
             }
@@ -1101,6 +1107,7 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_done(bf));
+            if (++bf == kBufs) { bf = 0; par ^= 1u; }
         }
         if constexpr (summary) {
             if (scan_ok) {
@@ -1199,17 +1206,16 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
         const bool bc_vec = p.tma_bc && N == NP && (N % 4) == 0;
         int s = 0;
         uint32_t ph = 0;
+        int bf = 0;        // buffer of chunk k: k % kBufs
+        uint32_t par = 0;  // parity of its use: (k / kBufs) & 1
         for (int64_t k = 0; k < nloc; ++k) {
-            const int bf = int(k & 1);
             const int64_t t0 = (c_begin + k) * TC;
             const int tv = int(L - t0 < TC ? L - t0 : int64_t(TC));
             bool ok = true;
             if (p.force_timeout && k == 0) ok = mbar_wait_bounded(bar_never, 0, p.wait_ns);
             if (ok) ok = mbar_wait_or_abort(bar_tma(s), ph, p.wait_ns, abort_flag);
-            // buffer bf is free once chunk k-2 is finished
-            if (ok && k >= 2)
-                ok = mbar_wait_or_abort(bar_pempty(bf), uint32_t((k >> 1) - 1) & 1u, p.wait_ns,
-                                        abort_flag);
+            // buffer bf is free once chunk k - kBufs is finished
+            if (ok && k >= kBufs) ok = mbar_wait_or_abort(bar_pempty(bf), par ^ 1u, p.wait_ns, abort_flag);
             if (!ok) {
                 give_up();
                 return;
@@ -1295,6 +1301,7 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
                 mbar_arrive(bar_empty(s));  // this warp is done with ring stage s
             }
             if (++s == nst) { s = 0; ph ^= 1u; }
+            if (++bf == kBufs) { bf = 0; par ^= 1u; }
         }
         return;
     }
@@ -1314,20 +1321,21 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     bool failed = false;
     int s = 0;  // ring stage of chunk k, and its TMA phase
     uint32_t ph = 0;
+    int bf = 0;        // buffer of chunk k: k % kBufs
+    uint32_t par = 0;  // parity of its use: (k / kBufs) & 1
     for (int64_t k = 0; k < nloc; ++k) {
-        const int bf = int(k & 1);
-        if (!mbar_wait_or_abort(bar_done(bf), uint32_t(k >> 1) & 1u, p.wait_ns, abort_flag))
+        if (!mbar_wait_or_abort(bar_done(bf), par, p.wait_ns, abort_flag))
             failed = true;
         // the chunk's u and z (complete: the prepare warps waited for them, and
         // the stage is not refilled before this warp releases it)
         if (!summary && !failed && !mbar_wait_or_abort(bar_tma(s), ph, p.wait_ns, abort_flag))
             failed = true;
-        if (!summary && leader) bulk_wait_read_le1();  // output tile bf is free again
+        if (!summary && leader) bulk_wait_read_le1();  // output tile k & 1 is free again
         if (named_sync_or(kBarFinishA, NQ, failed || *abort_flag)) break;
         if constexpr (!summary) {
             // y = (sum of the state groups' partials) g + D u g, g = silu(z) or 1
             const int64_t t0 = (c_begin + k) * TC;
-            unsigned char* yt = s_y0 + bf * TILE;
+            unsigned char* yt = s_y0 + int(k & 1) * TILE;  // output tiles alternate
             const float* part = s_part(bf);
             const unsigned char* ru = raw_u(s);
             const unsigned char* rz = raw_z(s);
@@ -1369,10 +1377,11 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
         }
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(bar_pempty(bf));  // buffers bf may take chunk k + 2
+            mbar_arrive(bar_pempty(bf));  // buffers bf may take chunk k + kBufs
             mbar_arrive(bar_empty(s));    // this warp is done with ring stage s
         }
         if (++s == nst) { s = 0; ph ^= 1u; }
+        if (++bf == kBufs) { bf = 0; par ^= 1u; }
     }
     // A failure in the last iteration has not been voted on yet.
     if (named_sync_or(kBarFinishA, NQ, failed) && leader) give_up();
@@ -1905,7 +1914,7 @@ size_t variant_smem_w(int npt, int ws, int64_t N, int stages, int TC, bool conv 
 }
 
 // Shared memory per warp-specialised block that still lets three blocks share an SM.
-constexpr size_t kWsSmemTarget = 60 * 1024;
+constexpr size_t kWsSmemTarget = 72 * 1024;
 
 template <typename T>
 Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, const void* dt,
