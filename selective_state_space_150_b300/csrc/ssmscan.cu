@@ -871,10 +871,9 @@ __global__ void __launch_bounds__(Geo<T, NPT, WS, TC>::NT)
 // A ring stage is refilled once the prepare and the finish warps are done
 // with it (EMPTY).
 // Every role may run up to kBufs chunks ahead of the next, which absorbs the
-// roles' uneven timing from chunk to chunk.  Each wait is
-// bounded and also gives up once another warp has raised the block's abort
-// flag; the only named barriers are among the finish warps, which all run
-// the same trip count and vote on aborting.
+// roles' uneven timing from chunk to chunk.  Each wait is bounded and also
+// gives up once another warp has raised the block's abort flag.  No two
+// warps share a named barrier.
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -888,25 +887,6 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
         if (*abort) return false;
         if (global_ns() - start > limit_ns) return false;
     }
-}
-
-// Barrier `id` over `n` threads of the block.
-__device__ __forceinline__ void named_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Barrier `id` over `n` threads that also returns the OR of `v` over them.
-__device__ __forceinline__ bool named_sync_or(int id, int n, bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(uint32_t(v)), "r"(id), "r"(n)
-        : "memory");
-    return r != 0;
 }
 
 constexpr int kBufs = 3;  // buffers between the prepare, scan and finish roles
@@ -986,7 +966,6 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     constexpr int DT = G::DT, NP = G::NP, ES = G::ES;
     constexpr int RS = TT::RS, NB = TT::NB, NPAIR = G::NPAIR;
     constexpr bool summary = SUMMARY;
-    constexpr int kBarFinishA = 1, kBarFinishB = 2;  // named barriers (finish warps only)
 
     extern __shared__ unsigned char smem_raw[];
     __shared__ int s_abort;
@@ -1307,10 +1286,16 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     }
 
     // ================================================================= FINISH
-    constexpr int NQ = G::NQ, ITEMS = G::ITEMS_Q, TSTEP = NQ / NPAIR;
+    // Each finish warp owns part of every output tile and stores it itself:
+    // half of the tile's rows (steps) when a block has fewer than 64 channel
+    // pairs, otherwise half of its column blocks.  The two warps share no
+    // barrier; a warp that sees a failure or the block's abort flag stops.
+    constexpr int NQ = G::NQ, ITEMS = G::ITEMS_Q;
+    constexpr bool ROWS = NPAIR < NQ;
     const int qt = tid - G::NS - G::NPR;  // 0 .. NQ-1
-    const bool leader = qt == 0;
-    const int pp = qt % NPAIR, tq0 = qt / NPAIR;
+    const int qw = qt >> 5;               // finish warp
+    const int pp = qt % NPAIR;
+    const int tq0 = (qt / NPAIR) * ITEMS;  // steps tq0 .. tq0 + ITEMS - 1
     float dsk2[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -1324,15 +1309,18 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     int bf = 0;        // buffer of chunk k: k % kBufs
     uint32_t par = 0;  // parity of its use: (k / kBufs) & 1
     for (int64_t k = 0; k < nloc; ++k) {
-        if (!mbar_wait_or_abort(bar_done(bf), par, p.wait_ns, abort_flag))
-            failed = true;
+        if (!mbar_wait_or_abort(bar_done(bf), par, p.wait_ns, abort_flag)) failed = true;
         // the chunk's u and z (complete: the prepare warps waited for them, and
         // the stage is not refilled before this warp releases it)
         if (!summary && !failed && !mbar_wait_or_abort(bar_tma(s), ph, p.wait_ns, abort_flag))
             failed = true;
-        if (!summary && leader) bulk_wait_read_le1();  // output tile k & 1 is free again
-        if (named_sync_or(kBarFinishA, NQ, failed || *abort_flag)) break;
+        if (__any_sync(0xffffffffu, failed || *abort_flag)) {
+            failed = true;
+            break;
+        }
         if constexpr (!summary) {
+            if (lane == 0) bulk_wait_read_le1();  // this warp's part of tile k & 1 is free
+            __syncwarp();
             // y = (sum of the state groups' partials) g + D u g, g = silu(z) or 1
             const int64_t t0 = (c_begin + k) * TC;
             unsigned char* yt = s_y0 + int(k & 1) * TILE;  // output tiles alternate
@@ -1341,7 +1329,7 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
             const unsigned char* rz = raw_z(s);
 #pragma unroll
             for (int it = 0; it < ITEMS; ++it) {
-                const int t = tq0 + it * TSTEP;
+                const int t = tq0 + it;
                 const uint32_t o = TT::off(t, 2 * pp * ES, TC);
                 float2 acc = *reinterpret_cast<const float2*>(part + t * DT + 2 * pp);
 #pragma unroll
@@ -1366,12 +1354,20 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
                 st_k<T, 2>(yt + o, yv);
             }
             fence_proxy_async_smem();
-            named_sync(kBarFinishB, NQ);
-            if (leader) {
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (ROWS) {  // rows qw*TC/2 .. of every column block
+                    constexpr int HR = TC / 2;
 #pragma unroll
-                for (int cb = 0; cb < NB; ++cb)
-                    tma_store_3d(&tm_y, int(d0) + cb * (RS / ES), int(t0), int(b),
-                                 smem_u32(yt + cb * TC * RS));
+                    for (int cb = 0; cb < NB; ++cb)
+                        tma_store_3d(&tm_y, int(d0) + cb * (RS / ES), int(t0) + qw * HR, int(b),
+                                     smem_u32(yt + cb * TC * RS + qw * HR * RS));
+                } else {  // column blocks qw*NB/2 .., all rows
+#pragma unroll
+                    for (int cb = qw * (NB / 2); cb < (qw + 1) * (NB / 2); ++cb)
+                        tma_store_3d(&tm_y, int(d0) + cb * (RS / ES), int(t0), int(b),
+                                     smem_u32(yt + cb * TC * RS));
+                }
                 bulk_commit();
             }
         }
@@ -1383,9 +1379,10 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
         if (++s == nst) { s = 0; ph ^= 1u; }
         if (++bf == kBufs) { bf = 0; par ^= 1u; }
     }
-    // A failure in the last iteration has not been voted on yet.
-    if (named_sync_or(kBarFinishA, NQ, failed) && leader) give_up();
-    if (leader) bulk_wait_all();
+    if (lane == 0) {
+        if (failed) give_up();
+        bulk_wait_all();
+    }
 }
 
 // ============================================================ one recurrent step
@@ -2224,7 +2221,11 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
                            pl.TC + (conv ? kConvHalo : 0), swz) &&
                   encode3d(&tms[1], ty, es, delta, dim, L, batch, box, pl.TC, swz) &&
                   encode3d(&tms[2], ty, es, z ? z : u, dim, L, batch, box, pl.TC, swz) &&
-                  encode3d(&tms[5], ty, es, y, dim, L, batch, box, pl.TC, swz);
+                  // the warp-specialised kernel's two finish warps each store
+                  // half of a tile's rows when a block has fewer than 128
+                  // channels (half of its column blocks otherwise)
+                  encode3d(&tms[5], ty, es, y, dim, L, batch, box,
+                           (pl.ws && pl.DT < 128) ? pl.TC / 2 : pl.TC, swz);
         if (tma_udz && tma_bc)
             tma_bc = encode3d(&tms[3], ty, es, B, N, L, batch, int(N), pl.TC,
                               CU_TENSOR_MAP_SWIZZLE_NONE) &&
