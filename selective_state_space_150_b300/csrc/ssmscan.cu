@@ -899,6 +899,11 @@ struct GeoW {
     static constexpr int NPW = 2, NQW = 2;           // prepare warps, finish warps
     static constexpr int NS = NSW * 32, NPR = NPW * 32, NQ = NQW * 32;
     static constexpr int NT = NS + NPR + NQ + 32;    // + the producer warp
+    // Blocks per SM the register allocation must allow (0: the compiler's
+    // choice).  Three 288-thread blocks share an SM when each thread keeps to
+    // 72 registers, which lanes of up to four states fit; the scan then has the
+    // registers to keep more steps' loads in flight.
+    static constexpr int MINB = (NT <= 288 && NPT <= 4) ? 3 : 0;
     static constexpr int DT = WC * 32;               // channels per block
     static constexpr int NP = NPT * WS;              // padded states per channel
     static constexpr int WB = DT * ES;               // tile row bytes
@@ -952,14 +957,13 @@ struct LayoutW {
     }
 };
 
+// The block's work; the tensor maps are the kernel's own __grid_constant__
+// parameters, passed by reference so that TMA sees their parameter addresses.
 template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH>
-__global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
-    ssm_scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u,
-                       const __grid_constant__ CUtensorMap tm_dt,
-                       const __grid_constant__ CUtensorMap tm_z,
-                       const __grid_constant__ CUtensorMap tm_B,
-                       const __grid_constant__ CUtensorMap tm_C,
-                       const __grid_constant__ CUtensorMap tm_y, const KParams p) {
+__device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensorMap& tm_dt,
+                                         const CUtensorMap& tm_z, const CUtensorMap& tm_B,
+                                         const CUtensorMap& tm_C, const CUtensorMap& tm_y,
+                                         const KParams& p) {
     using E = Elt<T>;
     using G = GeoW<T, NPT, WS, TC>;
     using TT = typename G::TileT;
@@ -1385,6 +1389,27 @@ __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     }
 }
 
+// Two entry kernels around the same block: one that holds the compiler to
+// the registers of GeoW::MINB blocks per SM, and one that leaves the choice to
+// it (a minimum of one block would let it take so many registers that fewer
+// blocks fit than without the bound).
+#define SSM_WS_PARAMS                                                                        \
+    const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dt,     \
+        const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B, \
+        const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y, \
+        const KParams p
+template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH>
+__global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT, GeoW<T, NPT, WS, TC>::MINB)
+    ssm_scan_ws_kernel(SSM_WS_PARAMS) {
+    ws_block<T, NPT, WS, TC, SUMMARY, CONV, ZOH>(tm_u, tm_dt, tm_z, tm_B, tm_C, tm_y, p);
+}
+template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH>
+__global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
+    ssm_scan_ws_kernel_free(SSM_WS_PARAMS) {
+    ws_block<T, NPT, WS, TC, SUMMARY, CONV, ZOH>(tm_u, tm_dt, tm_z, tm_B, tm_C, tm_y, p);
+}
+#undef SSM_WS_PARAMS
+
 // ============================================================ one recurrent step
 // The scan at L = 1 for every (b, d) channel, from state h (updated in place):
 // the generation-time recurrence, which carries only the state from one token
@@ -1655,7 +1680,14 @@ __global__ void __launch_bounds__(WS * 32) ssm_bwd_kernel(const BwdParams q) {
         }
         stage(t0, tv, false);
         __syncthreads();
-        for (int i = 0; i < tv; ++i) step(i, h);
+        // a whole chunk unrolled: later steps' loads and exponentials issue
+        // while earlier steps' state updates wait on each other
+        if (tv == kBwdTC) {
+#pragma unroll
+            for (int i = 0; i < kBwdTC; ++i) step(i, h);
+        } else {
+            for (int i = 0; i < tv; ++i) step(i, h);
+        }
         __syncthreads();
     }
 
@@ -1677,13 +1709,22 @@ __global__ void __launch_bounds__(WS * 32) ssm_bwd_kernel(const BwdParams q) {
         }
         stage(t0, tv, true);
         __syncthreads();
-        for (int i = 0; i < tv; ++i) {
+        auto fwd_keep = [&](int i) {
             step(i, h);
 #pragma unroll
             for (int j = 0; j < NPT; ++j) myh[(i * NPT + j) * 32 + lane] = h[j];
+        };
+        if (tv == kBwdTC) {
+#pragma unroll
+            for (int i = 0; i < kBwdTC; ++i) fwd_keep(i);
+        } else {
+            for (int i = 0; i < tv; ++i) fwd_keep(i);
         }
         __syncwarp();
-        for (int i = tv - 1; i >= 0; --i) {
+        // One reverse step.  Only carry links consecutive steps; the shuffle
+        // reductions of dB and dC hang off it, so with the chunk unrolled
+        // several steps' reductions are in flight at once.
+        auto rev_step = [&](int i) {
             const float dt = s_dt[i * 32 + lane];
             const float x = s_x[i * 32 + lane];
             const float zz = s_z[i * 32 + lane];
@@ -1721,6 +1762,12 @@ __global__ void __launch_bounds__(WS * 32) ssm_bwd_kernel(const BwdParams q) {
                 q.pB[o + n] = vB[0];
                 q.pC[o + int64_t(sg) * NPT + nbC] = vC[0];
             }
+        };
+        if (tv == kBwdTC) {
+#pragma unroll
+            for (int i = kBwdTC - 1; i >= 0; --i) rev_step(i);
+        } else {
+            for (int i = tv - 1; i >= 0; --i) rev_step(i);
         }
         __syncthreads();
         // the chunk's per-(step, channel) gradients: warp sg takes steps sg, sg + WS, ...
@@ -2048,7 +2095,10 @@ int launch_one(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStre
 template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH = false>
 int launch_one_w(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
     using G = GeoW<T, NPT, WS, TC>;
-    auto kern = ssm_scan_ws_kernel<T, NPT, WS, TC, SUMMARY, CONV, ZOH>;
+    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                 KParams);
+    if constexpr (G::MINB > 0) kern = ssm_scan_ws_kernel<T, NPT, WS, TC, SUMMARY, CONV, ZOH>;
+    else kern = ssm_scan_ws_kernel_free<T, NPT, WS, TC, SUMMARY, CONV, ZOH>;
     const size_t smem = smem_bytes_w<T, NPT, WS, SUMMARY>(kp.N, kp.stages, TC, CONV);
     static std::atomic<size_t> configured[64];
     int dev = 0;
