@@ -1577,12 +1577,13 @@ __device__ __forceinline__ void reduce_rounds(float (&v)[NPT], int lane, int& nb
 }
 
 // Block = WS warps over the same 32 channels (lane = channel); warp sg holds
-// states sg*4 .. sg*4 + 3.  Each chunk's inputs are first staged in shared
-// memory by the whole block (coalesced, all loads in flight at once); the
-// per-step work then reads only shared memory.  The per-(step, channel)
-// gradients need sums over all states: each warp leaves its share in shared
-// memory and, after every chunk, the block adds the WS shares in a fixed
-// order.
+// states sg*4 .. sg*4 + 3.  Each chunk's inputs are loaded into registers one
+// chunk ahead and staged in shared memory by the whole block; the per-step
+// work then reads only shared memory.  The per-(step, channel) gradients need
+// sums over all states: each warp leaves its share in shared memory and,
+// after every chunk, the block adds the WS shares in a fixed order.  The
+// register bound keeps three blocks per SM (the shared-memory footprint
+// allows three).
 constexpr int kBwdNPT = 4;
 
 template <int WS>
@@ -1597,13 +1598,14 @@ struct BwdSmem {
     static constexpr int x = dt + T * 32;                 // [T][32] u
     static constexpr int dy = x + T * 32;                 // [T][32]
     static constexpr int zz = dy + T * 32;                // [T][32]
-    static constexpr int Bs = zz + T * 32;                // [T][NP]
+    static constexpr int dyc = zz + T * 32;               // [T][32] dy silu(z)
+    static constexpr int Bs = dyc + T * 32;               // [T][NP]
     static constexpr int Cs = Bs + T * NP;                // [T][NP]
     static constexpr int total = Cs + T * NP;
 };
 
 template <int WS>
-__global__ void __launch_bounds__(WS * 32) ssm_bwd_kernel(const BwdParams q) {
+__global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) {
     constexpr int NPT = kBwdNPT, NT = WS * 32;
     using SM = BwdSmem<WS>;
     constexpr int NP = SM::NP;
@@ -1628,30 +1630,76 @@ __global__ void __launch_bounds__(WS * 32) ssm_bwd_kernel(const BwdParams q) {
     float* const s_x = sm + SM::x;
     float* const s_dy = sm + SM::dy;
     float* const s_z = sm + SM::zz;
+    float* const s_dyc = sm + SM::dyc;
     float* const s_B = sm + SM::Bs;
     float* const s_C = sm + SM::Cs;
 
-    // Stage steps t0 .. t0 + tv - 1 (zeros past tv or past dim).  rev: also
-    // dy, z and C for the reverse pass.
-    auto stage = [&](int64_t t0, int tv, bool rev) {
-        for (int i = sg; i < kBwdTC; i += WS) {
+    // A chunk's inputs for steps t0 .. t0 + tv - 1 are fetched into registers
+    // (zeros past tv or past dim; rev: also dy, z, C and the chunk's starting
+    // state) one chunk ahead, so that their global loads are in flight while
+    // the block works on the chunk before, and staged in shared memory once
+    // that chunk is done.  Warp sg takes rows sg, sg + WS, ...
+    constexpr int RW = kBwdTC / WS, QB = kBwdTC * NP / NT;
+    static_assert(kBwdTC % WS == 0 && (kBwdTC * NP) % NT == 0, "staging split");
+    struct Fetched {
+        float raw[RW], x[RW], dy[RW], z[RW], bv[QB], cv[QB], h0[NPT];
+    };
+    auto ck = [&](int64_t c, int j) {
+        return ((b * q.nchunks + c) * dim + d) * N + int64_t(sg) * NPT + j;
+    };
+    auto chunk_len = [&](int64_t c) {
+        const int64_t t0 = c * kBwdTC;
+        return int(L - t0 < kBwdTC ? L - t0 : int64_t(kBwdTC));
+    };
+    auto fetch = [&](int64_t c, bool rev, Fetched& f) {
+        const int64_t t0 = c * kBwdTC;
+        const int tv = chunk_len(c);
+#pragma unroll
+        for (int k = 0; k < RW; ++k) {
+            const int i = sg + k * WS;
             const bool in = ok && i < tv;
             const int64_t o = (b * L + t0 + i) * dim + d;
-            const float r = (in ? q.delta[o] : 0.f) + (in ? bias : 0.f);
-            s_raw[i * 32 + lane] = r;
-            s_dt[i * 32 + lane] = in ? (q.softplus ? Act<float>::softplus(r) : r) : 0.f;
-            s_x[i * 32 + lane] = in ? q.u[o] : 0.f;
-            if (rev) {
-                s_dy[i * 32 + lane] = in ? q.dy[o] : 0.f;
-                s_z[i * 32 + lane] = (in && q.z != nullptr) ? q.z[o] : 0.f;
-            }
+            f.raw[k] = in ? q.delta[o] : 0.f;
+            f.x[k] = in ? q.u[o] : 0.f;
+            f.dy[k] = (rev && in) ? q.dy[o] : 0.f;
+            f.z[k] = (rev && in && q.z != nullptr) ? q.z[o] : 0.f;
         }
-        for (int k = tid; k < kBwdTC * NP; k += NT) {
-            const int i = k / NP, n = k % NP;
+#pragma unroll
+        for (int k = 0; k < QB; ++k) {
+            const int e = tid + k * NT;
+            const int i = e / NP, n = e % NP;
             const bool in = i < tv && n < N;
             const int64_t o = (b * L + t0 + i) * N + n;
-            s_B[k] = in ? q.B[o] : 0.f;
-            if (rev) s_C[k] = in ? q.C[o] : 0.f;
+            f.bv[k] = in ? q.B[o] : 0.f;
+            f.cv[k] = (rev && in) ? q.C[o] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < NPT; ++j)
+            f.h0[j] = (rev && ok && int64_t(sg) * NPT + j < N) ? q.ckpt[ck(c, j)] : 0.f;
+    };
+    auto stage = [&](const Fetched& f, int tv, bool rev) {
+#pragma unroll
+        for (int k = 0; k < RW; ++k) {
+            const int i = sg + k * WS;
+            const bool in = ok && i < tv;
+            const float r = f.raw[k] + (in ? bias : 0.f);
+            s_raw[i * 32 + lane] = r;
+            s_dt[i * 32 + lane] = in ? (q.softplus ? Act<float>::softplus(r) : r) : 0.f;
+            s_x[i * 32 + lane] = f.x[k];
+            if (rev) {
+                s_dy[i * 32 + lane] = f.dy[k];
+                s_z[i * 32 + lane] = f.z[k];
+                // the gated output gradient, once per (step, channel) rather
+                // than once per state group
+                const float g = q.z != nullptr ? f.z[k] / (1.f + expf(-f.z[k])) : 1.f;
+                s_dyc[i * 32 + lane] = f.dy[k] * g;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < QB; ++k) {
+            const int e = tid + k * NT;
+            s_B[e] = f.bv[k];
+            if (rev) s_C[e] = f.cv[k];
         }
     };
     // one forward step of this warp's states from the staged chunk
@@ -1662,24 +1710,26 @@ __global__ void __launch_bounds__(WS * 32) ssm_bwd_kernel(const BwdParams q) {
 #pragma unroll
         for (int j = 0; j < NPT; ++j) h[j] = fmaf(ex2_approx(dt * a2[j]), h[j], du_ * bb[j]);
     };
-    auto ck = [&](int64_t c, int j) {
-        return ((b * q.nchunks + c) * dim + d) * N + int64_t(sg) * NPT + j;
-    };
 
     // ---- forward: the state at the start of every chunk
     float h[NPT];
 #pragma unroll
     for (int j = 0; j < NPT; ++j) h[j] = 0.f;
+    Fetched f;
+    if (q.nchunks > 0) fetch(0, false, f);
     for (int64_t c = 0; c < q.nchunks; ++c) {
-        const int64_t t0 = c * kBwdTC;
-        const int tv = int(L - t0 < kBwdTC ? L - t0 : int64_t(kBwdTC));
+        const int tv = chunk_len(c);
         if (ok) {
 #pragma unroll
             for (int j = 0; j < NPT; ++j)
                 if (int64_t(sg) * NPT + j < N) q.ckpt[ck(c, j)] = h[j];
         }
-        stage(t0, tv, false);
+        stage(f, tv, false);
         __syncthreads();
+        // the next chunk, or the last one again with the reverse pass's inputs
+        // (its checkpoint was just written by this thread)
+        if (c + 1 < q.nchunks) fetch(c + 1, false, f);
+        else fetch(c, true, f);
         // a whole chunk unrolled: later steps' loads and exponentials issue
         // while earlier steps' state updates wait on each other
         if (tv == kBwdTC) {
@@ -1700,44 +1750,32 @@ __global__ void __launch_bounds__(WS * 32) ssm_bwd_kernel(const BwdParams q) {
     float* const part = sm + SM::part;
     for (int64_t c = q.nchunks - 1; c >= 0; --c) {
         const int64_t t0 = c * kBwdTC;
-        const int tv = int(L - t0 < kBwdTC ? L - t0 : int64_t(kBwdTC));
+        const int tv = chunk_len(c);
         float hstart[NPT];
 #pragma unroll
         for (int j = 0; j < NPT; ++j) {
-            hstart[j] = (ok && int64_t(sg) * NPT + j < N) ? q.ckpt[ck(c, j)] : 0.f;
+            hstart[j] = f.h0[j];
             h[j] = hstart[j];
         }
-        stage(t0, tv, true);
+        stage(f, tv, true);
         __syncthreads();
-        auto fwd_keep = [&](int i) {
-            step(i, h);
-#pragma unroll
-            for (int j = 0; j < NPT; ++j) myh[(i * NPT + j) * 32 + lane] = h[j];
-        };
-        if (tv == kBwdTC) {
-#pragma unroll
-            for (int i = 0; i < kBwdTC; ++i) fwd_keep(i);
-        } else {
-            for (int i = 0; i < tv; ++i) fwd_keep(i);
-        }
-        __syncwarp();
-        // One reverse step.  Only carry links consecutive steps; the shuffle
-        // reductions of dB and dC hang off it, so with the chunk unrolled
-        // several steps' reductions are in flight at once.
-        auto rev_step = [&](int i) {
+        if (c > 0) fetch(c - 1, true, f);
+        // One reverse step from the states after step i and before it.  Only
+        // carry links consecutive steps; the shuffle reductions of dB and dC
+        // hang off it, so with the chunk unrolled several steps' reductions
+        // are in flight at once.
+        auto rev_step = [&](int i, const float (&hc)[NPT], const float (&hp)[NPT]) {
             const float dt = s_dt[i * 32 + lane];
             const float x = s_x[i * 32 + lane];
-            const float zz = s_z[i * 32 + lane];
-            const float g = q.z != nullptr ? zz / (1.f + expf(-zz)) : 1.f;
-            const float dyc = s_dy[i * 32 + lane] * g;
+            const float dyc = s_dyc[i * 32 + lane];
             const float* const bb = s_B + i * NP + sg * NPT;
             const float* const cc = s_C + i * NP + sg * NPT;
             float vB[NPT], vC[NPT];
             float yc = 0.f, gdt = 0.f, gu = 0.f;
 #pragma unroll
             for (int j = 0; j < NPT; ++j) {
-                const float hcur = myh[(i * NPT + j) * 32 + lane];
-                const float hprev = i > 0 ? myh[((i - 1) * NPT + j) * 32 + lane] : hstart[j];
+                const float hcur = hc[j];
+                const float hprev = hp[j];
                 yc = fmaf(cc[j], hcur, yc);
                 const float lam = fmaf(dyc, cc[j], carry[j]);
                 const float e = ex2_approx(dt * a2[j]);
@@ -1763,11 +1801,37 @@ __global__ void __launch_bounds__(WS * 32) ssm_bwd_kernel(const BwdParams q) {
                 q.pC[o + int64_t(sg) * NPT + nbC] = vC[0];
             }
         };
+        auto fwd_keep = [&](int i) {
+            step(i, h);
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) myh[(i * NPT + j) * 32 + lane] = h[j];
+        };
+        // the state after step i comes from the step before in registers;
+        // only the state before it is read back
+        auto rev_from = [&](int i, float (&hc)[NPT]) {
+            float hp[NPT];
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) hp[j] = i > 0 ? myh[((i - 1) * NPT + j) * 32 + lane] : hstart[j];
+            rev_step(i, hc, hp);
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) hc[j] = hp[j];
+        };
         if (tv == kBwdTC) {
 #pragma unroll
-            for (int i = kBwdTC - 1; i >= 0; --i) rev_step(i);
+            for (int i = 0; i < kBwdTC; ++i) fwd_keep(i);
+            __syncwarp();
+            float hc[NPT];
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) hc[j] = h[j];
+#pragma unroll
+            for (int i = kBwdTC - 1; i >= 0; --i) rev_from(i, hc);
         } else {
-            for (int i = tv - 1; i >= 0; --i) rev_step(i);
+            for (int i = 0; i < tv; ++i) fwd_keep(i);
+            __syncwarp();
+            float hc[NPT];
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) hc[j] = h[j];
+            for (int i = tv - 1; i >= 0; --i) rev_from(i, hc);
         }
         __syncthreads();
         // the chunk's per-(step, channel) gradients: warp sg takes steps sg, sg + WS, ...
