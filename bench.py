@@ -334,16 +334,7 @@ def run_ours(args, wl, world, rank, local):
     torch.cuda.synchronize(dev)
 
     # pipe peaks for the compute roofline (measured on this GPU, this run)
-    peaks = None
-    try:
-        import ctypes
-        lib = ctypes.CDLL(os.path.join(ROOT, "selective_state_space_150_b300", "libpipepeaks.so"))
-        out = (ctypes.c_double * 4)()
-        if lib.ssm_pipe_peaks(out, ctypes.c_void_p(sptr)) == 0:
-            peaks = {"ex2_per_s": out[0], "fma_lane_ops_per_s": out[1],
-                     "fma2_lane_ops_per_s": out[2], "sms": int(out[3])}
-    except Exception as e:  # measurement support missing: report without it
-        peaks = {"error": str(e)}
+    peaks = pipe_peaks(sptr)
 
     K = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -466,6 +457,35 @@ def run_ours(args, wl, world, rank, local):
     return line
 
 
+def pipe_peaks(stream_ptr):
+    """MUFU ex2 and FP32 lane-op rates of this GPU, measured now by the
+    libpipepeaks microbenchmarks on the given stream."""
+    try:
+        import ctypes
+        lib = ctypes.CDLL(os.path.join(ROOT, "selective_state_space_150_b300", "libpipepeaks.so"))
+        out = (ctypes.c_double * 4)()
+        if lib.ssm_pipe_peaks(out, ctypes.c_void_p(stream_ptr)) == 0:
+            return {"ex2_per_s": out[0], "fma_lane_ops_per_s": out[1],
+                    "fma2_lane_ops_per_s": out[2], "sms": int(out[3])}
+        return {"error": "ssm_pipe_peaks failed"}
+    except Exception as e:  # measurement support missing: report without it
+        return {"error": str(e)}
+
+
+def bwd_accounting(wl: W.Workload, es: int = 4):
+    """(bytes, MUFU ops) of one backward call whose tensors are es bytes per
+    element.  Bytes: u, delta, z, dy, B, C read once, du, ddelta, dz, dB, dC
+    written once, plus A, D, bias and their fp32 gradients.  MUFU ops: the recomputation evaluates exp(dt A) three
+    times per (b, t, d, n) -- the checkpoint pass, the chunk's recomputed
+    states and the adjoint step -- and per (b, t, d) a softplus (ex2, lg2) in
+    each pass and the gate's exponential in the reverse pass."""
+    bld, bln = wl.batch * wl.L * wl.dim, wl.batch * wl.L * wl.N
+    gate = 1 if wl.gate else 0
+    nbytes = es * bld * (2 * (2 + gate) + 1) + es * bln * 4 + 8 * wl.dim * (wl.N + 2)
+    mufu = 3 * bld * wl.N + bld * ((4 if wl.softplus else 0) + gate)
+    return nbytes, mufu
+
+
 def _events_mean_ms(fn, reps, stream):
     import torch
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -519,22 +539,45 @@ def run_op(args, wl):
             ssm.selective_scan_bwd(f32["u"], f32["delta"], f32["A"], f32["B"], f32["C"], dy,
                                    f32["D"], f32["z"], f32["delta_bias"], wl.softplus)
 
+        # and on the workload's own storage (bf16 tensors through the bf16 entry)
+        io = {k: dev(inp[k]) for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}
+        dy_io = dy.to(torch.bfloat16) if bf else dy
+
+        def bwd_io_call(i):
+            ssm.selective_scan_bwd(io["u"], io["delta"], io["A"], io["B"], io["C"], dy_io,
+                                   io["D"], io["z"], io["delta_bias"], wl.softplus)
+
         def fwd_call(i):
             ssm.selective_scan_fwd(f32["u"], f32["delta"], f32["A"], f32["B"], f32["C"], f32["D"],
                                    f32["z"], f32["delta_bias"], wl.softplus)
 
         for i in range(args.warmup):
             bwd_call(i)
+            bwd_io_call(i)
             fwd_call(i)
         torch.cuda.synchronize()
-        ms_bwd = _events_mean_ms(bwd_call, args.steps, stream)
+        ms_f32 = _events_mean_ms(bwd_call, args.steps, stream)
+        ms_io = _events_mean_ms(bwd_io_call, args.steps, stream)
         ms_fwd = _events_mean_ms(fwd_call, args.steps, stream)
+        ms_bwd = ms_io
+        peaks = pipe_peaks(stream.cuda_stream)
+        nbytes, mufu = bwd_accounting(wl, es)
+        roof = {"bound": "alu", "pipe": "mufu_ex2", "unit": "Gop/s",
+                "achieved": mufu / (ms_bwd * 1e-3) / 1e9, "mufu_ops_per_launch": mufu,
+                "algorithmic_bytes_per_launch": nbytes, "traffic": None,
+                "hbm_frac": nbytes / (ms_bwd * 1e-3) / 1e9 / hbm_gbs}
+        if "ex2_per_s" in peaks:
+            roof["peak"] = peaks["ex2_per_s"] / 1e9
+            roof["frac"] = roof["achieved"] / roof["peak"]
+            roof["peak_source"] = "measured on this GPU by libpipepeaks, same run"
         return {
             "op": "bwd", "metric": "selective-scan backward (recomputation) tokens/s",
             "value": wl.tokens / (ms_bwd * 1e-3), "unit": "tokens/s", "higher_is_better": True,
             "ms_per_step": ms_bwd, "steps": args.steps, "warmup": args.warmup,
-            "fp32_forward_ms": ms_fwd, "dtype": "f32",
-            "data": "synthetic (seeded; see ssm_workloads.py), values widened to fp32",
+            "io_dtype": wl.dtype, "fp32_io_ms": ms_f32, "fp32_forward_ms": ms_fwd,
+            "roofline": roof, "dtype": "f32",
+            "data": "synthetic (seeded; see ssm_workloads.py); fp32_io_ms: the same values "
+                    "widened to fp32",
             "config": config_of(wl, "one resident copy"), "impl": "ours"}
     if args.op == "zoh_scan":
         sets = [{k: dev(inp[k]) for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}

@@ -291,6 +291,22 @@ SSM_API int ssm_scan_bwd(const float *u, const float *delta, const float *A,
                  int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream);
 
 /*
+ * The same backward pass for the bf16 forward: u, delta, B, C, z, dy and the
+ * gradients du, ddelta, dB, dC, dz are bf16 (bit patterns, 2-byte aligned);
+ * A, D, delta_bias and dA, dD, ddelta_bias are fp32.  Inputs are widened to
+ * fp32 exactly, every sum runs in fp32 (the checkpointed states, the adjoint
+ * and the partials of the shared-parameter gradients), and each bf16
+ * gradient is rounded once, to nearest even, when it is written.  Scratch,
+ * limits, determinism and errors as for ssm_scan_bwd.
+ */
+SSM_API int ssm_scan_bwd_bf16(const uint16_t *u, const uint16_t *delta, const float *A,
+                 const uint16_t *B, const uint16_t *C, const float *D,
+                 const uint16_t *z, const float *delta_bias, int softplus_flag,
+                 const uint16_t *dy, uint16_t *du, uint16_t *ddelta, float *dA,
+                 uint16_t *dB, uint16_t *dC, float *dD, uint16_t *dz, float *ddelta_bias,
+                 int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream);
+
+/*
  * No-allocation variant of ssm_scan_fwd_bf16 (an engineering addition: the
  * pages describe nothing like it).  Same arguments, same kernels, same
  * results bit for bit; the only difference is where the time-segment

@@ -12,6 +12,7 @@ from .ssmscan import (  # noqa: F401
     ssm_conv_scan_fwd,
     ssm_conv_scan_fwd_bf16,
     ssm_scan_bwd,
+    ssm_scan_bwd_bf16,
     ssm_scan_fwd,
     ssm_scan_fwd_bf16,
     ssm_scan_fwd_bf16_host,

@@ -1512,8 +1512,9 @@ __global__ void __launch_bounds__(128) ssm_step_kernel(const StepIn<T> q) {
 }
 
 // ============================================================ backward pass
-// Gradients of the scan (fp32 inputs, Euler B, zero initial state) with
-// respect to u, delta, A, B, C, D, z and delta_bias, given the gradient of y.
+// Gradients of the scan (Euler B, zero initial state; fp32 or bf16 tensors,
+// fp32 arithmetic) with respect to u, delta, A, B, C, D, z and delta_bias,
+// given the gradient of y.
 // The state is recomputed instead of stored (doyouknow.kr Mamba guide,
 // section 3-3, "recomputation"): a forward pass keeps only the state at the
 // start of every kBwdTC-step chunk; the reverse pass recomputes each chunk's
@@ -1527,19 +1528,21 @@ __global__ void __launch_bounds__(128) ssm_step_kernel(const StepIn<T> q) {
 constexpr int kBwdTC = 16;
 constexpr int kBwdMaxN = 16;
 
+// u, delta, B, C, z, dy and du, ddelta, dz hold the kernel's element type
+// (fp32 or bf16); everything else is fp32.
 struct BwdParams {
-    const float* u;
-    const float* delta;
+    const void* u;
+    const void* delta;
     const float* A;
-    const float* B;
-    const float* C;
+    const void* B;
+    const void* C;
     const float* D;
-    const float* z;
+    const void* z;
     const float* bias;
-    const float* dy;
-    float* du;
-    float* ddelta;
-    float* dz;
+    const void* dy;
+    void* du;
+    void* ddelta;
+    void* dz;
     float* ckpt;   // [batch][nchunks][dim][N]
     float* pB;     // [ntile][batch][L][N]
     float* pC;     // [ntile][batch][L][N]
@@ -1604,9 +1607,16 @@ struct BwdSmem {
     static constexpr int total = Cs + T * NP;
 };
 
-template <int WS>
+template <typename T, int WS>
 __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) {
+    using E = Elt<T>;
     constexpr int NPT = kBwdNPT, NT = WS * 32;
+    const T* const g_u = static_cast<const T*>(q.u);
+    const T* const g_delta = static_cast<const T*>(q.delta);
+    const T* const g_B = static_cast<const T*>(q.B);
+    const T* const g_C = static_cast<const T*>(q.C);
+    const T* const g_z = static_cast<const T*>(q.z);
+    const T* const g_dy = static_cast<const T*>(q.dy);
     using SM = BwdSmem<WS>;
     constexpr int NP = SM::NP;
     extern __shared__ float sm[];
@@ -1659,10 +1669,10 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
             const int i = sg + k * WS;
             const bool in = ok && i < tv;
             const int64_t o = (b * L + t0 + i) * dim + d;
-            f.raw[k] = in ? q.delta[o] : 0.f;
-            f.x[k] = in ? q.u[o] : 0.f;
-            f.dy[k] = (rev && in) ? q.dy[o] : 0.f;
-            f.z[k] = (rev && in && q.z != nullptr) ? q.z[o] : 0.f;
+            f.raw[k] = in ? E::to_f(g_delta[o]) : 0.f;
+            f.x[k] = in ? E::to_f(g_u[o]) : 0.f;
+            f.dy[k] = (rev && in) ? E::to_f(g_dy[o]) : 0.f;
+            f.z[k] = (rev && in && q.z != nullptr) ? E::to_f(g_z[o]) : 0.f;
         }
 #pragma unroll
         for (int k = 0; k < QB; ++k) {
@@ -1670,8 +1680,8 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
             const int i = e / NP, n = e % NP;
             const bool in = i < tv && n < N;
             const int64_t o = (b * L + t0 + i) * N + n;
-            f.bv[k] = in ? q.B[o] : 0.f;
-            f.cv[k] = (rev && in) ? q.C[o] : 0.f;
+            f.bv[k] = in ? E::to_f(g_B[o]) : 0.f;
+            f.cv[k] = (rev && in) ? E::to_f(g_C[o]) : 0.f;
         }
 #pragma unroll
         for (int j = 0; j < NPT; ++j)
@@ -1860,9 +1870,9 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
             const float gdelta = q.softplus ? gdt / (1.f + expf(-raw)) : gdt;  // softplus' = sigmoid
             if (ok) {
                 const int64_t o = (b * L + t0 + i) * dim + d;
-                q.du[o] = gu;
-                q.ddelta[o] = gdelta;
-                if (q.dz != nullptr) q.dz[o] = gz;
+                static_cast<T*>(q.du)[o] = E::from_f(gu);
+                static_cast<T*>(q.ddelta)[o] = E::from_f(gdelta);
+                if (q.dz != nullptr) static_cast<T*>(q.dz)[o] = E::from_f(gz);
             }
             gD = fmaf(dyc, x, gD);
             gbias += gdelta;
@@ -1892,15 +1902,17 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
     }
 }
 
-// out[i] = sum_k in[k * count + i], k = 0 .. parts-1 in order.
+// out[i] = sum_k in[k * count + i], k = 0 .. parts-1 in order, in fp32,
+// rounded once to the output type.
+template <typename O>
 __global__ void __launch_bounds__(256)
-    ssm_fold_kernel(const float* __restrict__ in, float* __restrict__ out, int64_t parts,
+    ssm_fold_kernel(const float* __restrict__ in, O* __restrict__ out, int64_t parts,
                     int64_t count) {
     const int64_t i = int64_t(blockIdx.x) * 256 + threadIdx.x;
     if (i >= count) return;
     float acc = 0.f;
     for (int64_t k = 0; k < parts; ++k) acc += in[k * count + i];
-    out[i] = acc;
+    out[i] = Elt<O>::from_f(acc);
 }
 
 // ------------------------------------------------------------------ host side
@@ -2661,10 +2673,11 @@ int scan_fwd_host(const T* u, const T* delta, const float* A, const T* B, const 
 }
 
 // Backward: checks, scratch, the two kernels.
-int scan_bwd(const float* u, const float* delta, const float* A, const float* B, const float* C,
-             const float* D, const float* z, const float* delta_bias, int softplus_flag,
-             const float* dy, float* du, float* ddelta, float* dA, float* dB, float* dC,
-             float* dD, float* dz, float* ddelta_bias, int64_t batch, int64_t L, int64_t dim,
+template <typename T>
+int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
+             const float* D, const T* z, const float* delta_bias, int softplus_flag,
+             const T* dy, T* du, T* ddelta, float* dA, T* dB, T* dC,
+             float* dD, T* dz, float* ddelta_bias, int64_t batch, int64_t L, int64_t dim,
              int64_t N, cudaStream_t stream) {
     if (batch < 0 || L < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > kBwdMaxN) return SSM_ERR_UNSUPPORTED_N;
@@ -2677,14 +2690,16 @@ int scan_bwd(const float* u, const float* delta, const float* A, const float* B,
         return SSM_ERR_NULL;
     if (dim > 0 && (!A || !dA)) return SSM_ERR_NULL;
     if ((D && !dD) || (z && !dz) || (delta_bias && !ddelta_bias)) return SSM_ERR_NULL;
-    for (const void* ptr : {(const void*)u, (const void*)delta, (const void*)A, (const void*)B,
-                            (const void*)C, (const void*)D, (const void*)z,
-                            (const void*)delta_bias, (const void*)dy, (const void*)du,
-                            (const void*)ddelta, (const void*)dA, (const void*)dB,
-                            (const void*)dC, (const void*)dD, (const void*)dz,
-                            (const void*)ddelta_bias})
+    const size_t es = sizeof(T);
+    for (const void* ptr : {(const void*)u, (const void*)delta, (const void*)B, (const void*)C,
+                            (const void*)z, (const void*)dy, (const void*)du,
+                            (const void*)ddelta, (const void*)dB, (const void*)dC,
+                            (const void*)dz})
+        if (ptr && !aligned(ptr, es)) return SSM_ERR_ALIGN;
+    for (const void* ptr : {(const void*)A, (const void*)D, (const void*)delta_bias,
+                            (const void*)dA, (const void*)dD, (const void*)ddelta_bias})
         if (ptr && !aligned(ptr, 4)) return SSM_ERR_ALIGN;
-    const int64_t by = n_bld * 4, bn = n_bln * 4;
+    const int64_t by = n_bld * int64_t(es), bn = n_bln * int64_t(es);
     const struct { const void* p; int64_t n; } ins[] = {
         {u, by}, {delta, by}, {z, z ? by : 0}, {dy, by}, {B, bn}, {C, bn}, {A, n_dn * 4},
         {D, D ? dim * 4 : 0}, {delta_bias, delta_bias ? dim * 4 : 0}};
@@ -2750,9 +2765,9 @@ int scan_bwd(const float* u, const float* delta, const float* A, const float* B,
     };
     bool launched;
     switch (ws) {
-        case 1: launched = launch(ssm_bwd_kernel<1>); break;
-        case 2: launched = launch(ssm_bwd_kernel<2>); break;
-        default: launched = launch(ssm_bwd_kernel<4>); break;
+        case 1: launched = launch(ssm_bwd_kernel<T, 1>); break;
+        case 2: launched = launch(ssm_bwd_kernel<T, 2>); break;
+        default: launched = launch(ssm_bwd_kernel<T, 4>); break;
     }
     if (!launched) {
         (void)cudaGetLastError();
@@ -2760,7 +2775,7 @@ int scan_bwd(const float* u, const float* delta, const float* A, const float* B,
         return SSM_ERR_LAUNCH;
     }
     int st = cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
-    auto fold = [&](const float* in, float* out, int64_t parts, int64_t count) {
+    auto fold = [&](const float* in, auto* out, int64_t parts, int64_t count) {
         if (st != SSM_OK || out == nullptr || count == 0) return;
         ssm_fold_kernel<<<dim3(unsigned((count + 255) / 256)), dim3(256), 0, stream>>>(
             in, out, parts, count);
@@ -2769,8 +2784,8 @@ int scan_bwd(const float* u, const float* delta, const float* A, const float* B,
     fold(q.pB, dB, ntile, n_bln);
     fold(q.pC, dC, ntile, n_bln);
     fold(q.pA, dA, batch, n_dn);
-    fold(q.pD, D ? dD : nullptr, batch, dim);
-    fold(q.pbias, delta_bias ? ddelta_bias : nullptr, batch, dim);
+    fold(q.pD, D ? dD : static_cast<float*>(nullptr), batch, dim);
+    fold(q.pbias, delta_bias ? ddelta_bias : static_cast<float*>(nullptr), batch, dim);
     if (cudaFreeAsync(scratch, stream) != cudaSuccess && st == SSM_OK) st = SSM_ERR_LAUNCH;
     return st;
 }
@@ -2901,8 +2916,24 @@ int ssm_scan_bwd(const float* u, const float* delta, const float* A, const float
                  int softplus_flag, const float* dy, float* du, float* ddelta, float* dA,
                  float* dB, float* dC, float* dD, float* dz, float* ddelta_bias, int64_t batch,
                  int64_t L, int64_t dim, int64_t N, cudaStream_t stream) {
-    return scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, ddelta, dA, dB,
-                    dC, dD, dz, ddelta_bias, batch, L, dim, N, stream);
+    return scan_bwd<float>(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, ddelta,
+                           dA, dB, dC, dD, dz, ddelta_bias, batch, L, dim, N, stream);
+}
+
+int ssm_scan_bwd_bf16(const uint16_t* u, const uint16_t* delta, const float* A,
+                      const uint16_t* B, const uint16_t* C, const float* D, const uint16_t* z,
+                      const float* delta_bias, int softplus_flag, const uint16_t* dy,
+                      uint16_t* du, uint16_t* ddelta, float* dA, uint16_t* dB, uint16_t* dC,
+                      float* dD, uint16_t* dz, float* ddelta_bias, int64_t batch, int64_t L,
+                      int64_t dim, int64_t N, cudaStream_t stream) {
+    using bf = __nv_bfloat16;
+    return scan_bwd<bf>(reinterpret_cast<const bf*>(u), reinterpret_cast<const bf*>(delta), A,
+                        reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
+                        reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
+                        reinterpret_cast<const bf*>(dy), reinterpret_cast<bf*>(du),
+                        reinterpret_cast<bf*>(ddelta), dA, reinterpret_cast<bf*>(dB),
+                        reinterpret_cast<bf*>(dC), dD, reinterpret_cast<bf*>(dz), ddelta_bias,
+                        batch, L, dim, N, stream);
 }
 
 int ssm_scan_step(const float* u, const float* delta, const float* A, const float* B,

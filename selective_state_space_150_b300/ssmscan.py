@@ -49,7 +49,7 @@ EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc",
             "ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0", "ssm_scan_fwd_zoh", "ssm_scan_fwd_bf16_zoh",
             "ssm_scan_step", "ssm_scan_step_bf16",
             "ssm_conv_scan_fwd", "ssm_conv_scan_fwd_bf16", "ssm_scan_host_workspace_bytes",
-            "ssm_scan_fwd_host", "ssm_scan_fwd_bf16_host", "ssm_scan_bwd",
+            "ssm_scan_fwd_host", "ssm_scan_fwd_bf16_host", "ssm_scan_bwd", "ssm_scan_bwd_bf16",
             "ssm_scan_last_device_status", "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
 
 _vp = ctypes.c_void_p
@@ -70,8 +70,9 @@ for _name in ("ssm_scan_fwd_host", "ssm_scan_fwd_bf16_host"):
     getattr(_lib, _name).restype = ctypes.c_int
 _lib.ssm_scan_host_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_int]
 _lib.ssm_scan_host_workspace_bytes.restype = _i64
-_lib.ssm_scan_bwd.argtypes = [_vp] * 8 + [ctypes.c_int] + [_vp] * 9 + [_i64] * 4 + [_vp]
-_lib.ssm_scan_bwd.restype = ctypes.c_int
+for _name in ("ssm_scan_bwd", "ssm_scan_bwd_bf16"):
+    getattr(_lib, _name).argtypes = [_vp] * 8 + [ctypes.c_int] + [_vp] * 9 + [_i64] * 4 + [_vp]
+    getattr(_lib, _name).restype = ctypes.c_int
 for _name in ("ssm_scan_step", "ssm_scan_step_bf16"):
     getattr(_lib, _name).argtypes = [_vp] * 8 + [ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _vp]
     getattr(_lib, _name).restype = ctypes.c_int
@@ -204,6 +205,17 @@ def ssm_scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, dde
     return _lib.ssm_scan_bwd(p(u), p(delta), p(A), p(B), p(C), p(D), p(z), p(delta_bias),
                              int(softplus_flag), p(dy), p(du), p(ddelta), p(dA), p(dB), p(dC),
                              p(dD), p(dz), p(ddelta_bias), batch, L, dim, N, p(stream))
+
+
+def ssm_scan_bwd_bf16(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, ddelta, dA,
+                      dB, dC, dD, dz, ddelta_bias, batch, L, dim, N, stream) -> int:
+    """bf16 backward pass (bf16 u/delta/B/C/z/dy and du/ddelta/dB/dC/dz, fp32
+    A/D/bias and their gradients); pointer arguments are ints (0 for NULL)."""
+    p = lambda v: v or None  # noqa: E731
+    return _lib.ssm_scan_bwd_bf16(p(u), p(delta), p(A), p(B), p(C), p(D), p(z), p(delta_bias),
+                                  int(softplus_flag), p(dy), p(du), p(ddelta), p(dA), p(dB),
+                                  p(dC), p(dD), p(dz), p(ddelta_bias), batch, L, dim, N,
+                                  p(stream))
 
 
 def ssm_scan_step(u, delta, A, B, C, D, z, delta_bias, softplus_flag, h, y, batch, dim, N,
@@ -361,14 +373,20 @@ def selective_scan_step(u, delta, A, B, C, h, D=None, z=None, delta_bias=None, s
 
 def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=False,
                        stream=None):
-    """Gradients of selective_scan_fwd's y (fp32 torch CUDA tensors) given dy.
-    Returns a dict with du, ddelta, dA, dB, dC and dD, dz, ddelta_bias where
-    D, z, delta_bias are given."""
+    """Gradients of selective_scan_fwd's y given dy, for contiguous CUDA
+    tensors that are all fp32, or bf16 u/delta/B/C/z/dy with fp32 A/D/
+    delta_bias.  Returns a dict with du, ddelta, dA, dB, dC and dD, dz,
+    ddelta_bias where D, z, delta_bias are given; each gradient has the dtype
+    of its input."""
     import torch
 
-    for t in (u, delta, A, B, C, dy, D, z, delta_bias):
-        if t is not None and (t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous()):
-            raise TypeError("the backward pass takes contiguous float32 CUDA tensors")
+    bf = u.dtype == torch.bfloat16
+    io = torch.bfloat16 if bf else torch.float32
+    for t, want in ((u, io), (delta, io), (B, io), (C, io), (z, io), (dy, io),
+                    (A, torch.float32), (D, torch.float32), (delta_bias, torch.float32)):
+        if t is not None and (t.dtype != want or not t.is_cuda or not t.is_contiguous()):
+            raise TypeError("the backward pass takes contiguous CUDA tensors: all fp32, or bf16 "
+                            "u/delta/B/C/z/dy with fp32 A/D/delta_bias")
     batch, L, dim = u.shape
     N = A.shape[1]
     g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(delta), "dA": torch.empty_like(A),
@@ -381,11 +399,12 @@ def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, s
         g["ddelta_bias"] = torch.empty_like(delta_bias)
     if stream is None:
         stream = torch.cuda.current_stream(u.device).cuda_stream
-    st = ssm_scan_bwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                      _ptr(delta_bias), int(bool(softplus)), _ptr(dy), _ptr(g["du"]),
-                      _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
-                      _ptr(g.get("dD")), _ptr(g.get("dz")), _ptr(g.get("ddelta_bias")),
-                      batch, L, dim, N, int(stream))
+    fn = ssm_scan_bwd_bf16 if bf else ssm_scan_bwd
+    st = fn(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+            _ptr(delta_bias), int(bool(softplus)), _ptr(dy), _ptr(g["du"]),
+            _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
+            _ptr(g.get("dD")), _ptr(g.get("dz")), _ptr(g.get("ddelta_bias")),
+            batch, L, dim, N, int(stream))
     if st != SSM_OK:
-        raise SSMError(st, "ssm_scan_bwd")
+        raise SSMError(st, fn.__name__)
     return g

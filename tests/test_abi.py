@@ -244,23 +244,25 @@ def test_zoh_checks(fn):
 
 
 # ---------------------------------------------------------------- backward
-def bwd(**kw):
+def bwd(fn=ssm.ssm_scan_bwd, **kw):
     args = dict(u=P, delta=P + 0x100000, A=P + 0x200000, B=P + 0x300000, C=P + 0x400000, D=0,
                 z=0, delta_bias=0, softplus_flag=0, dy=P + 0x500000, du=Q, ddelta=Q + 0x100000,
                 dA=Q + 0x200000, dB=Q + 0x300000, dC=Q + 0x400000, dD=0, dz=0, ddelta_bias=0,
                 batch=2, L=8, dim=16, N=4, stream=0)
     args.update(kw)
-    return ssm.ssm_scan_bwd(**args)
+    return fn(**args)
 
 
-def test_backward_checks():
+@pytest.mark.parametrize("fn,es", [(ssm.ssm_scan_bwd, 4), (ssm.ssm_scan_bwd_bf16, 2)])
+def test_backward_checks(fn, es):
     for k in ("u", "delta", "dy", "du", "ddelta", "A", "dA", "B", "C", "dB", "dC"):
-        assert bwd(**{k: 0}) == ssmscan.SSM_ERR_NULL, k
-    assert bwd(D=P + 0x600000) == ssmscan.SSM_ERR_NULL            # D given, dD missing
-    assert bwd(z=P + 0x600000) == ssmscan.SSM_ERR_NULL            # z given, dz missing
-    assert bwd(N=17) == ssmscan.SSM_ERR_UNSUPPORTED_N
-    assert bwd(L=-1) == ssmscan.SSM_ERR_SIZE
-    assert bwd(du=P) == ssmscan.SSM_ERR_ALIAS                     # du is u
-    assert bwd(dB=Q + 0x40) == ssmscan.SSM_ERR_ALIAS              # dB inside du
-    assert bwd(du=Q + 2) == ssmscan.SSM_ERR_ALIGN
-    assert bwd(batch=0) == ssmscan.SSM_OK
+        assert bwd(fn, **{k: 0}) == ssmscan.SSM_ERR_NULL, k
+    assert bwd(fn, D=P + 0x600000) == ssmscan.SSM_ERR_NULL        # D given, dD missing
+    assert bwd(fn, z=P + 0x600000) == ssmscan.SSM_ERR_NULL        # z given, dz missing
+    assert bwd(fn, N=17) == ssmscan.SSM_ERR_UNSUPPORTED_N
+    assert bwd(fn, L=-1) == ssmscan.SSM_ERR_SIZE
+    assert bwd(fn, du=P) == ssmscan.SSM_ERR_ALIAS                 # du is u
+    assert bwd(fn, dB=Q + 0x40) == ssmscan.SSM_ERR_ALIAS          # dB inside du
+    assert bwd(fn, du=Q + es // 2) == ssmscan.SSM_ERR_ALIGN       # du off its element size
+    assert bwd(fn, dA=Q + 0x200000 + 2) == ssmscan.SSM_ERR_ALIGN  # fp32 dA off 4 bytes
+    assert bwd(fn, batch=0) == ssmscan.SSM_OK

@@ -8,7 +8,7 @@ import torch
 import ssm_workloads as W
 import selective_state_space_150_b300 as ssm
 from oracle.backward import selective_scan_bwd as oracle_bwd
-from tests.gpu_util import rel_err
+from tests.gpu_util import from_dev, rel_err, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -70,3 +70,62 @@ def test_backward_of_an_empty_sequence_is_zero():
     inp, dy = problem((2, 0, 32, 16), seed=4, **FLAGS[0])
     g = gpu_grads(inp, dy)
     assert all(not np.any(v) for v in g.values())
+
+
+# ---------------------------------------------------------------- bf16
+BF16_TOL = 4e-3  # bf16 gradients: one round-to-nearest-even (2^-9 relative) on the fp32 result
+
+
+def gpu_grads_bf16(inp, dy_bits):
+    d = {k: to_dev(inp[k]) for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}
+    g = ssm.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], to_dev(dy_bits),
+                               d["D"], d["z"], d["delta_bias"], inp["softplus"])
+    torch.cuda.synchronize()
+    return {k: from_dev(v) for k, v in g.items()}, {k: v.dtype for k, v in g.items()}
+
+
+@pytest.mark.parametrize("flags", FLAGS)
+@pytest.mark.parametrize("shape", [(2, 40, 72, 16), (1, 37, 33, 5), (2, 50, 32, 8),
+                                   (1, 16, 32, 16)])
+def test_bf16_backward_matches_oracle(shape, flags):
+    batch, L, dim, N = shape
+    wl = BASE.with_shape(name="g", batch=batch, L=L, dim=dim, N=N, dtype="bf16", **flags)
+    inp = W.make_inputs(wl, seed=sum(shape) + 7)
+    dy32 = np.random.default_rng(sum(shape)).standard_normal((batch, L, dim)).astype(np.float32)
+    dy_bits = W.f32_to_bf16_bits(dy32)
+    g, dtypes = gpu_grads_bf16(inp, dy_bits)
+    x = W.decoded(inp)  # the exact values the GPU reads
+    r = oracle_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
+                   x["softplus"], W.decode(dy_bits))
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "delta_bias": "ddelta_bias"}
+    for k, v in r.items():
+        n = names[k]
+        bf = k in ("u", "delta", "B", "C", "z")
+        assert dtypes[n] == (torch.bfloat16 if bf else torch.float32), (n, dtypes[n])
+        err = rel_err(g[n], v)
+        assert err <= (BF16_TOL if bf else TOL), (n, err)
+
+
+def test_bf16_backward_rounds_the_fp32_gradients():
+    """The bf16 entry widens its inputs exactly and rounds each gradient once:
+    fed the same (bf16-representable) values, it equals the fp32 entry's
+    gradients rounded to nearest even, element for element, on the
+    per-(step, channel) gradients, and matches bit for bit on the fp32 ones."""
+    shape = (2, 48, 64, 16)
+    batch, L, dim, N = shape
+    wl = BASE.with_shape(name="g", batch=batch, L=L, dim=dim, N=N, dtype="bf16", **FLAGS[0])
+    inp = W.make_inputs(wl, seed=11)
+    dy_bits = W.f32_to_bf16_bits(
+        np.random.default_rng(5).standard_normal((batch, L, dim)).astype(np.float32))
+    g16, _ = gpu_grads_bf16(inp, dy_bits)
+    x = W.decoded(inp)
+    x32 = {k: (None if v is None or k == "softplus" else np.ascontiguousarray(v, dtype=np.float32))
+           for k, v in x.items()}
+    x32["softplus"] = x["softplus"]
+    g32 = gpu_grads(x32, W.decode(dy_bits).astype(np.float32))
+    for n in ("du", "ddelta", "dz", "dB", "dC"):
+        want = W.decode(W.f32_to_bf16_bits(g32[n]))
+        assert np.array_equal(g16[n], want), n
+    for n in ("dA", "dD", "ddelta_bias"):
+        assert np.array_equal(g16[n], g32[n]), n
