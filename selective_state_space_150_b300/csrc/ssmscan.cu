@@ -175,11 +175,13 @@ template <typename T> struct Elt;
 template <> struct Elt<float> {
     __device__ static float to_f(float v) { return v; }
     __device__ static float from_f(float v) { return v; }
+    __device__ static float zero() { return 0.f; }
     static constexpr CUtensorMapDataType tmap_type = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 };
 template <> struct Elt<__nv_bfloat16> {
     __device__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
     __device__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+    __device__ static __nv_bfloat16 zero() { return __ushort_as_bfloat16((unsigned short)0); }
     static constexpr CUtensorMapDataType tmap_type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 };
 
@@ -1648,11 +1650,14 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
     // (zeros past tv or past dim; rev: also dy, z, C and the chunk's starting
     // state) one chunk ahead, so that their global loads are in flight while
     // the block works on the chunk before, and staged in shared memory once
-    // that chunk is done.  Warp sg takes rows sg, sg + WS, ...
+    // that chunk is done.  They are held as loaded and widened only when
+    // staged: a conversion right after the load would wait for it.  Warp sg
+    // takes rows sg, sg + WS, ...
     constexpr int RW = kBwdTC / WS, QB = kBwdTC * NP / NT;
     static_assert(kBwdTC % WS == 0 && (kBwdTC * NP) % NT == 0, "staging split");
     struct Fetched {
-        float raw[RW], x[RW], dy[RW], z[RW], bv[QB], cv[QB], h0[NPT];
+        T raw[RW], x[RW], dy[RW], z[RW], bv[QB], cv[QB];
+        float h0[NPT];
     };
     auto ck = [&](int64_t c, int j) {
         return ((b * q.nchunks + c) * dim + d) * N + int64_t(sg) * NPT + j;
@@ -1669,10 +1674,10 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
             const int i = sg + k * WS;
             const bool in = ok && i < tv;
             const int64_t o = (b * L + t0 + i) * dim + d;
-            f.raw[k] = in ? E::to_f(g_delta[o]) : 0.f;
-            f.x[k] = in ? E::to_f(g_u[o]) : 0.f;
-            f.dy[k] = (rev && in) ? E::to_f(g_dy[o]) : 0.f;
-            f.z[k] = (rev && in && q.z != nullptr) ? E::to_f(g_z[o]) : 0.f;
+            f.raw[k] = in ? g_delta[o] : E::zero();
+            f.x[k] = in ? g_u[o] : E::zero();
+            f.dy[k] = (rev && in) ? g_dy[o] : E::zero();
+            f.z[k] = (rev && in && q.z != nullptr) ? g_z[o] : E::zero();
         }
 #pragma unroll
         for (int k = 0; k < QB; ++k) {
@@ -1680,8 +1685,8 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
             const int i = e / NP, n = e % NP;
             const bool in = i < tv && n < N;
             const int64_t o = (b * L + t0 + i) * N + n;
-            f.bv[k] = in ? E::to_f(g_B[o]) : 0.f;
-            f.cv[k] = (rev && in) ? E::to_f(g_C[o]) : 0.f;
+            f.bv[k] = in ? g_B[o] : E::zero();
+            f.cv[k] = (rev && in) ? g_C[o] : E::zero();
         }
 #pragma unroll
         for (int j = 0; j < NPT; ++j)
@@ -1692,24 +1697,25 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
         for (int k = 0; k < RW; ++k) {
             const int i = sg + k * WS;
             const bool in = ok && i < tv;
-            const float r = f.raw[k] + (in ? bias : 0.f);
+            const float r = E::to_f(f.raw[k]) + (in ? bias : 0.f);
             s_raw[i * 32 + lane] = r;
             s_dt[i * 32 + lane] = in ? (q.softplus ? Act<float>::softplus(r) : r) : 0.f;
-            s_x[i * 32 + lane] = f.x[k];
+            s_x[i * 32 + lane] = E::to_f(f.x[k]);
             if (rev) {
-                s_dy[i * 32 + lane] = f.dy[k];
-                s_z[i * 32 + lane] = f.z[k];
+                const float dyv = E::to_f(f.dy[k]), zv = E::to_f(f.z[k]);
+                s_dy[i * 32 + lane] = dyv;
+                s_z[i * 32 + lane] = zv;
                 // the gated output gradient, once per (step, channel) rather
                 // than once per state group
-                const float g = q.z != nullptr ? f.z[k] / (1.f + expf(-f.z[k])) : 1.f;
-                s_dyc[i * 32 + lane] = f.dy[k] * g;
+                const float g = q.z != nullptr ? zv / (1.f + expf(-zv)) : 1.f;
+                s_dyc[i * 32 + lane] = dyv * g;
             }
         }
 #pragma unroll
         for (int k = 0; k < QB; ++k) {
             const int e = tid + k * NT;
-            s_B[e] = f.bv[k];
-            if (rev) s_C[e] = f.cv[k];
+            s_B[e] = E::to_f(f.bv[k]);
+            if (rev) s_C[e] = E::to_f(f.cv[k]);
         }
     };
     // one forward step of this warp's states from the staged chunk
