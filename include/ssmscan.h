@@ -279,9 +279,11 @@ SSM_API int ssm_scan_step_bf16(const uint16_t *u, const uint16_t *delta, const f
  * (doyouknow.kr Mamba guide, section 3-3): the call keeps the state at every
  * 16th step and per-block partial sums in stream-ordered scratch
  * (cudaMallocAsync / cudaFreeAsync on `stream`, about batch * L * dim * N / 4
- * plus 2 * batch * L * N * ceil(dim / 32) fp32 words).  Partials are folded in
- * a fixed order, so results are deterministic.  N <= 16 (otherwise
- * SSM_ERR_UNSUPPORTED_N).  Outputs must not overlap inputs or each other.
+ * plus 2 * batch * L * N * ceil(dim / 32) fp32 words; for N > 16, which runs
+ * as slices of 16 states, also 3 * ceil(N / 16) * batch * L * dim).  Partials
+ * are folded in a fixed order, so results are deterministic.  N <= 128
+ * (otherwise SSM_ERR_UNSUPPORTED_N).  Outputs must not overlap inputs or each
+ * other.
  */
 SSM_API int ssm_scan_bwd(const float *u, const float *delta, const float *A,
                  const float *B, const float *C, const float *D,

@@ -1528,7 +1528,8 @@ __global__ void __launch_bounds__(128) ssm_step_kernel(const StepIn<T> q) {
 // one partial per channel tile, and dA, D, delta_bias as one partial per
 // batch row; a second kernel folds the partials in a fixed order.
 constexpr int kBwdTC = 16;
-constexpr int kBwdMaxN = 16;
+constexpr int kBwdSlice = 16;  // states per block; larger N runs as slices of 16 states
+constexpr int kBwdMaxN = 128;
 
 // u, delta, B, C, z, dy and du, ddelta, dz hold the kernel's element type
 // (fp32 or bf16); everything else is fp32.
@@ -1551,9 +1552,30 @@ struct BwdParams {
     float* pA;     // [batch][dim][N]
     float* pD;     // [batch][dim]
     float* pbias;  // [batch][dim]
-    int64_t batch, L, dim, N, ntile, nchunks;
+    float* pt;     // [nslice][3][batch][L][dim] per-slice sums (N > kBwdSlice only)
+    int64_t batch, L, dim, N, ntile, nchunks, nslice;
     int softplus;
 };
+
+// The per-(step, channel) gradients from the sums over all states of the
+// readout yc (without the skip term), the dt term gdt and the u term gu.
+// Returns the gated output gradient dyc; du, ddelta, dz through references.
+__device__ __forceinline__ float grad_point(float yc, float gdt, float gu, float raw, float x,
+                                            float dyo, float zz, bool has_z, int softplus,
+                                            float Dd, float& du, float& ddelta, float& dz) {
+    float g = 1.f, gz = 0.f;
+    yc = fmaf(Dd, x, yc);
+    if (has_z) {
+        const float sgm = 1.f / (1.f + expf(-zz));
+        g = zz * sgm;
+        gz = dyo * yc * sgm * (1.f + zz * (1.f - sgm));  // d silu / dz
+    }
+    const float dyc = dyo * g;
+    du = fmaf(dyc, Dd, gu);
+    ddelta = softplus ? gdt / (1.f + expf(-raw)) : gdt;  // softplus' = sigmoid
+    dz = gz;
+    return dyc;
+}
 
 // Sum of v[j] (j < NPT) over the 32 lanes, NPT values at once: each round
 // halves the values a lane keeps and swaps the other half with the partner
@@ -1628,10 +1650,13 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
     const int64_t d = tile * 32 + lane;
     const bool ok = d < q.dim;
     const int64_t N = q.N, L = q.L, dim = q.dim;
+    // this block's states: n0 .. n0 + kBwdSlice - 1 (blockIdx.y = slice)
+    const int64_t n0 = int64_t(blockIdx.y) * kBwdSlice + int64_t(sg) * NPT;
+    const bool split = q.nslice > 1;
     float aA[NPT], a2[NPT];
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
-        const int64_t n = int64_t(sg) * NPT + j;
+        const int64_t n = n0 + j;
         aA[j] = (ok && n < N) ? q.A[d * N + n] : 0.f;
         a2[j] = aA[j] * kLog2e;
     }
@@ -1660,7 +1685,7 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
         float h0[NPT];
     };
     auto ck = [&](int64_t c, int j) {
-        return ((b * q.nchunks + c) * dim + d) * N + int64_t(sg) * NPT + j;
+        return ((b * q.nchunks + c) * dim + d) * N + n0 + j;
     };
     auto chunk_len = [&](int64_t c) {
         const int64_t t0 = c * kBwdTC;
@@ -1682,7 +1707,8 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
 #pragma unroll
         for (int k = 0; k < QB; ++k) {
             const int e = tid + k * NT;
-            const int i = e / NP, n = e % NP;
+            const int i = e / NP;
+            const int64_t n = int64_t(blockIdx.y) * kBwdSlice + e % NP;
             const bool in = i < tv && n < N;
             const int64_t o = (b * L + t0 + i) * N + n;
             f.bv[k] = in ? g_B[o] : E::zero();
@@ -1690,7 +1716,7 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
         }
 #pragma unroll
         for (int j = 0; j < NPT; ++j)
-            f.h0[j] = (rev && ok && int64_t(sg) * NPT + j < N) ? q.ckpt[ck(c, j)] : 0.f;
+            f.h0[j] = (rev && ok && n0 + j < N) ? q.ckpt[ck(c, j)] : 0.f;
     };
     auto stage = [&](const Fetched& f, int tv, bool rev) {
 #pragma unroll
@@ -1738,7 +1764,7 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
         if (ok) {
 #pragma unroll
             for (int j = 0; j < NPT; ++j)
-                if (int64_t(sg) * NPT + j < N) q.ckpt[ck(c, j)] = h[j];
+                if (n0 + j < N) q.ckpt[ck(c, j)] = h[j];
         }
         stage(f, tv, false);
         __syncthreads();
@@ -1810,11 +1836,11 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
             int nbB = 0, nbC = 0;
             reduce_rounds<NPT, NPT, 16>(vB, lane, nbB);
             reduce_rounds<NPT, NPT, 16>(vC, lane, nbC);
-            const int64_t n = int64_t(sg) * NPT + nbB;
+            const int64_t n = n0 + nbB;  // nbC == nbB: the same lane pattern
             if ((lane & (32 / NPT - 1)) == 0 && n < N) {
                 const int64_t o = ((tile * q.batch + b) * L + t0 + i) * N;
                 q.pB[o + n] = vB[0];
-                q.pC[o + int64_t(sg) * NPT + nbC] = vC[0];
+                q.pC[o + n0 + nbC] = vC[0];
             }
         };
         auto fwd_keep = [&](int i) {
@@ -1860,23 +1886,26 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
                 gdt += pp[32];
                 gu += pp[64];
             }
-            const float raw = s_raw[i * 32 + lane];
-            const float x = s_x[i * 32 + lane];
-            const float dyo = s_dy[i * 32 + lane];
-            float g = 1.f, gz = 0.f;
-            yc = fmaf(Dd, x, yc);
-            if (q.z != nullptr) {
-                const float zz = s_z[i * 32 + lane];
-                const float sgm = 1.f / (1.f + expf(-zz));
-                g = zz * sgm;
-                gz = dyo * yc * sgm * (1.f + zz * (1.f - sgm));  // d silu / dz
+            const int64_t o = (b * L + t0 + i) * dim + d;
+            if (split) {
+                // this slice's sums; a second kernel adds the slices and
+                // finishes the gradients
+                if (ok) {
+                    const int64_t plane = q.batch * L * dim;
+                    float* const pt = q.pt + int64_t(blockIdx.y) * 3 * plane + o;
+                    pt[0] = yc;
+                    pt[plane] = gdt;
+                    pt[2 * plane] = gu;
+                }
+                continue;
             }
-            const float dyc = dyo * g;
-            gu = fmaf(dyc, Dd, gu);
-            const float gdelta = q.softplus ? gdt / (1.f + expf(-raw)) : gdt;  // softplus' = sigmoid
+            const float x = s_x[i * 32 + lane];
+            float gu_, gdelta, gz;
+            const float dyc = grad_point(yc, gdt, gu, s_raw[i * 32 + lane], x, s_dy[i * 32 + lane],
+                                         s_z[i * 32 + lane], q.z != nullptr, q.softplus, Dd, gu_,
+                                         gdelta, gz);
             if (ok) {
-                const int64_t o = (b * L + t0 + i) * dim + d;
-                static_cast<T*>(q.du)[o] = E::from_f(gu);
+                static_cast<T*>(q.du)[o] = E::from_f(gu_);
                 static_cast<T*>(q.ddelta)[o] = E::from_f(gdelta);
                 if (q.dz != nullptr) static_cast<T*>(q.dz)[o] = E::from_f(gz);
             }
@@ -1888,10 +1917,11 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
     if (ok) {
 #pragma unroll
         for (int j = 0; j < NPT; ++j) {
-            const int64_t n = int64_t(sg) * NPT + j;
+            const int64_t n = n0 + j;
             if (n < N) q.pA[(b * dim + d) * N + n] = gA[j];
         }
     }
+    if (split) return;  // dD and ddelta_bias come from the slice-summing kernel
     float* const red = sm + SM::red;
     red[(sg * 2) * 32 + lane] = gD;
     red[(sg * 2 + 1) * 32 + lane] = gbias;
@@ -1919,6 +1949,53 @@ __global__ void __launch_bounds__(256)
     float acc = 0.f;
     for (int64_t k = 0; k < parts; ++k) acc += in[k * count + i];
     out[i] = Elt<O>::from_f(acc);
+}
+
+// N > kBwdSlice: adds the slices' sums per (b, t, d) in slice order and
+// finishes the per-(step, channel) gradients as the single-slice kernel does.
+// One thread per (b, run of kBwdRun steps, d) walks its steps and leaves the
+// run's dD and ddelta_bias partials at [b][run][d].
+constexpr int kBwdRun = 64;
+
+template <typename T>
+__global__ void __launch_bounds__(256) ssm_bwd_slices_kernel(const BwdParams q) {
+    using E = Elt<T>;
+    const int64_t nrun = (q.L + kBwdRun - 1) / kBwdRun;
+    const int64_t i = int64_t(blockIdx.x) * 256 + threadIdx.x;
+    if (i >= q.batch * nrun * q.dim) return;
+    const int64_t d = i % q.dim, r = i / q.dim;
+    const int64_t run = r % nrun, b = r / nrun;
+    const int64_t plane = q.batch * q.L * q.dim;
+    const float Dd = q.D != nullptr ? q.D[d] : 0.f;
+    const float bias = q.bias != nullptr ? q.bias[d] : 0.f;
+    const T* const g_u = static_cast<const T*>(q.u);
+    const T* const g_delta = static_cast<const T*>(q.delta);
+    const T* const g_z = static_cast<const T*>(q.z);
+    const T* const g_dy = static_cast<const T*>(q.dy);
+    float gD = 0.f, gbias = 0.f;
+    const int64_t t1 = (run + 1) * kBwdRun < q.L ? (run + 1) * kBwdRun : q.L;
+    for (int64_t t = run * kBwdRun; t < t1; ++t) {
+        const int64_t o = (b * q.L + t) * q.dim + d;
+        float yc = 0.f, gdt = 0.f, gu = 0.f;
+        for (int64_t sl = 0; sl < q.nslice; ++sl) {
+            const float* const pt = q.pt + sl * 3 * plane + o;
+            yc += pt[0];
+            gdt += pt[plane];
+            gu += pt[2 * plane];
+        }
+        const float x = E::to_f(g_u[o]);
+        const float zz = q.z != nullptr ? E::to_f(g_z[o]) : 0.f;
+        float du, ddelta, dz;
+        const float dyc = grad_point(yc, gdt, gu, E::to_f(g_delta[o]) + bias, x, E::to_f(g_dy[o]),
+                                     zz, q.z != nullptr, q.softplus, Dd, du, ddelta, dz);
+        static_cast<T*>(q.du)[o] = E::from_f(du);
+        static_cast<T*>(q.ddelta)[o] = E::from_f(ddelta);
+        if (q.dz != nullptr) static_cast<T*>(q.dz)[o] = E::from_f(dz);
+        gD = fmaf(dyc, x, gD);
+        gbias += ddelta;
+    }
+    q.pD[r * q.dim + d] = gD;
+    q.pbias[r * q.dim + d] = gbias;
 }
 
 // ------------------------------------------------------------------ host side
@@ -2729,9 +2806,15 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
                 return SSM_ERR_LAUNCH;
         return SSM_OK;
     }
+    const int64_t nslice = (N + kBwdSlice - 1) / kBwdSlice;
     const size_t n_ck = size_t(batch * nchunks) * size_t(n_dn);
     const size_t n_p = size_t(ntile) * size_t(n_bln);
-    const size_t n_total = n_ck + 2 * n_p + size_t(n_bdn) + 2 * size_t(batch * dim);
+    const size_t n_pt = nslice > 1 ? size_t(nslice) * 3 * size_t(n_bld) : 0;
+    // dD / ddelta_bias partials: one per batch row, or per (row, run of
+    // kBwdRun steps) when slices are summed by the second kernel
+    const int64_t nrun = nslice > 1 ? (L + kBwdRun - 1) / kBwdRun : 1;
+    const size_t n_rd = size_t(batch * nrun) * size_t(dim);
+    const size_t n_total = n_ck + 2 * n_p + size_t(n_bdn) + 2 * n_rd + n_pt;
     void* scratch = nullptr;
     if (cudaMallocAsync(&scratch, n_total * 4, stream) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -2746,15 +2829,19 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     q.pC = q.pB + n_p;
     q.pA = q.pC + n_p;
     q.pD = q.pA + n_bdn;
-    q.pbias = q.pD + batch * dim;
+    q.pbias = q.pD + n_rd;
+    q.pt = nslice > 1 ? q.pbias + n_rd : nullptr;
     q.batch = batch; q.L = L; q.dim = dim; q.N = N; q.ntile = ntile; q.nchunks = nchunks;
+    q.nslice = nslice;
     q.softplus = softplus_flag ? 1 : 0;
     // every (tile, b, t, n < N) entry of the partial dB / dC is written by
     // exactly one lane
-    const int ws = N <= 4 ? 1 : (N <= 8 ? 2 : 4);  // warps of kBwdNPT states per 32 channels
+    // warps of kBwdNPT states per 32 channels; N > kBwdSlice runs as slices
+    // of kBwdSlice states (grid.y), each with four warps
+    const int ws = N <= 4 ? 1 : (N <= 8 ? 2 : 4);
     const size_t smem = size_t(ws == 1 ? BwdSmem<1>::total
                                        : (ws == 2 ? BwdSmem<2>::total : BwdSmem<4>::total)) * 4;
-    const dim3 grid = dim3(unsigned(batch * ntile)), block = dim3(unsigned(32 * ws));
+    const dim3 grid = dim3(unsigned(batch * ntile), unsigned(nslice)), block = dim3(unsigned(32 * ws));
     auto launch = [&](auto kern) {
         // dynamic shared memory above 48 KB needs the opt-in (per device)
         static std::atomic<size_t> configured[64];
@@ -2781,6 +2868,13 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
         return SSM_ERR_LAUNCH;
     }
     int st = cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    if (st == SSM_OK && nslice > 1) {
+        const int64_t threads = batch * nrun * dim;
+        if (threads / 256 >= int64_t(0x7fffffff)) st = SSM_ERR_SIZE;
+        else ssm_bwd_slices_kernel<T><<<dim3(unsigned((threads + 255) / 256)), dim3(256), 0,
+                                        stream>>>(q);
+        if (cudaGetLastError() != cudaSuccess) st = SSM_ERR_LAUNCH;
+    }
     auto fold = [&](const float* in, auto* out, int64_t parts, int64_t count) {
         if (st != SSM_OK || out == nullptr || count == 0) return;
         ssm_fold_kernel<<<dim3(unsigned((count + 255) / 256)), dim3(256), 0, stream>>>(
@@ -2790,8 +2884,8 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     fold(q.pB, dB, ntile, n_bln);
     fold(q.pC, dC, ntile, n_bln);
     fold(q.pA, dA, batch, n_dn);
-    fold(q.pD, D ? dD : static_cast<float*>(nullptr), batch, dim);
-    fold(q.pbias, delta_bias ? ddelta_bias : static_cast<float*>(nullptr), batch, dim);
+    fold(q.pD, D ? dD : static_cast<float*>(nullptr), batch * nrun, dim);
+    fold(q.pbias, delta_bias ? ddelta_bias : static_cast<float*>(nullptr), batch * nrun, dim);
     if (cudaFreeAsync(scratch, stream) != cudaSuccess && st == SSM_OK) st = SSM_ERR_LAUNCH;
     return st;
 }

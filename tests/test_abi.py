@@ -259,7 +259,7 @@ def test_backward_checks(fn, es):
         assert bwd(fn, **{k: 0}) == ssmscan.SSM_ERR_NULL, k
     assert bwd(fn, D=P + 0x600000) == ssmscan.SSM_ERR_NULL        # D given, dD missing
     assert bwd(fn, z=P + 0x600000) == ssmscan.SSM_ERR_NULL        # z given, dz missing
-    assert bwd(fn, N=17) == ssmscan.SSM_ERR_UNSUPPORTED_N
+    assert bwd(fn, N=129) == ssmscan.SSM_ERR_UNSUPPORTED_N
     assert bwd(fn, L=-1) == ssmscan.SSM_ERR_SIZE
     assert bwd(fn, du=P) == ssmscan.SSM_ERR_ALIAS                 # du is u
     assert bwd(fn, dB=Q + 0x40) == ssmscan.SSM_ERR_ALIAS          # dB inside du

@@ -54,7 +54,10 @@ FLAGS = [
 
 @pytest.mark.parametrize("flags", FLAGS)
 @pytest.mark.parametrize("shape", [(2, 40, 72, 16), (1, 37, 33, 5), (3, 20, 40, 4),
-                                   (1, 17, 64, 1), (2, 50, 32, 8)])
+                                   (1, 17, 64, 1), (2, 50, 32, 8),
+                                   # N > 16: slices of 16 states, a ragged last slice, and
+                                   # runs of 64 steps in the summing kernel
+                                   (1, 70, 40, 17), (2, 33, 64, 40), (1, 150, 33, 64)])
 def test_backward_matches_oracle(shape, flags):
     inp, dy = problem(shape, seed=sum(shape), **flags)
     check(inp, dy)
@@ -86,7 +89,7 @@ def gpu_grads_bf16(inp, dy_bits):
 
 @pytest.mark.parametrize("flags", FLAGS)
 @pytest.mark.parametrize("shape", [(2, 40, 72, 16), (1, 37, 33, 5), (2, 50, 32, 8),
-                                   (1, 16, 32, 16)])
+                                   (1, 16, 32, 16), (1, 70, 40, 33)])
 def test_bf16_backward_matches_oracle(shape, flags):
     batch, L, dim, N = shape
     wl = BASE.with_shape(name="g", batch=batch, L=L, dim=dim, N=N, dtype="bf16", **flags)
@@ -129,3 +132,18 @@ def test_bf16_backward_rounds_the_fp32_gradients():
         assert np.array_equal(g16[n], want), n
     for n in ("dA", "dD", "ddelta_bias"):
         assert np.array_equal(g16[n], g32[n]), n
+
+
+def test_sliced_backward_is_deterministic():
+    inp, dy = problem((1, 80, 64, 48), seed=8, **FLAGS[0])
+    g1, g2 = gpu_grads(inp, dy), gpu_grads(inp, dy)
+    assert all(np.array_equal(g1[k], g2[k]) for k in g1)
+
+
+def test_backward_time_invariant_workload_sampled():
+    """The time-invariant workload's N = 64 runs as four slices: its gradients
+    on a sample of channels and a shortened sequence against the oracle."""
+    wl = W.WORKLOADS["lti_fp32"].with_shape(name="g", L=96, dim=48)
+    inp = W.make_inputs(wl, seed=12)
+    dy = np.random.default_rng(12).standard_normal((wl.batch, wl.L, wl.dim)).astype(np.float32)
+    check(inp, dy)
