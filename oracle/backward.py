@@ -14,14 +14,15 @@ from __future__ import annotations
 import numpy as np
 
 
-def _forward_torch(u, delta, A, B, C, D, z, delta_bias, softplus):
-    """The definition (Euler B, zero initial state), one step at a time, on
-    torch fp64 tensors: returns y (batch, L, dim)."""
+def _forward_torch(u, delta, A, B, C, D, z, delta_bias, softplus, h0=None, return_h=False):
+    """The definition (Euler B), one step at a time, on torch fp64 tensors,
+    from the state h0 (zero when None): returns y (batch, L, dim), and the
+    last state (batch, dim, N) too when return_h."""
     import torch
 
     batch, L, dim = u.shape
     N = A.shape[1]
-    h = torch.zeros((batch, dim, N), dtype=torch.float64)
+    h = torch.zeros((batch, dim, N), dtype=torch.float64) if h0 is None else h0
     ys = []
     for t in range(L):
         dt = delta[:, t, :]
@@ -40,7 +41,8 @@ def _forward_torch(u, delta, A, B, C, D, z, delta_bias, softplus):
             zz = z[:, t, :]
             y = y * (zz / (1.0 + torch.exp(-zz)))
         ys.append(y)
-    return torch.stack(ys, dim=1)
+    y = torch.stack(ys, dim=1) if L > 0 else torch.zeros((batch, 0, dim), dtype=torch.float64)
+    return (y, h) if return_h else y
 
 
 def selective_scan_fwd_loop(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False):
@@ -54,22 +56,32 @@ def selective_scan_fwd_loop(u, delta, A, B, C, D=None, z=None, delta_bias=None, 
 
 
 def selective_scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=False,
-                       dout=None):
-    """Vector-Jacobian product of y with the upstream gradient dout
-    (batch, L, dim).  Returns a dict of fp64 numpy gradients with the shapes
-    of the inputs: u, delta, A, B, C, and D, z, delta_bias where given."""
+                       dout=None, h0=None, dh_last=None):
+    """Vector-Jacobian product of (y, h_last) with the upstream gradients dout
+    (batch, L, dim) and dh_last (batch, dim, N; zero when None), the scan
+    starting from h0 (batch, dim, N; zero when None).  Returns a dict of fp64
+    numpy gradients with the shapes of the inputs: u, delta, A, B, C, and D,
+    z, delta_bias, h0 where given.  With h0 and dh_last a long sequence's
+    gradients follow from its pieces: a piece's h0 gradient is the dh_last of
+    the piece before it."""
     import torch
 
-    names = ("u", "delta", "A", "B", "C", "D", "z", "delta_bias")
-    vals = (u, delta, A, B, C, D, z, delta_bias)
+    names = ("u", "delta", "A", "B", "C", "D", "z", "delta_bias", "h0")
+    vals = (u, delta, A, B, C, D, z, delta_bias, h0)
     ts = {}
     for n, v in zip(names, vals):
         ts[n] = (None if v is None
                  else torch.tensor(np.asarray(v, dtype=np.float64), requires_grad=True))
-    y = _forward_torch(ts["u"], ts["delta"], ts["A"], ts["B"], ts["C"], ts["D"], ts["z"],
-                       ts["delta_bias"], softplus)
-    g = torch.as_tensor(np.asarray(dout, dtype=np.float64))
+    y, h = _forward_torch(ts["u"], ts["delta"], ts["A"], ts["B"], ts["C"], ts["D"], ts["z"],
+                          ts["delta_bias"], softplus, h0=ts["h0"], return_h=True)
+    outs, gouts = [y], [torch.as_tensor(np.asarray(dout, dtype=np.float64))]
+    if dh_last is not None:
+        outs.append(h)
+        gouts.append(torch.as_tensor(np.asarray(dh_last, dtype=np.float64)))
     leaves = [n for n in names if ts[n] is not None]
-    grads = torch.autograd.grad(y, [ts[n] for n in leaves], grad_outputs=g, allow_unused=True)
+    if not any(o.requires_grad for o in outs):  # L = 0 and no h0: nothing depends on the inputs
+        return {n: np.zeros(ts[n].shape) for n in leaves}
+    grads = torch.autograd.grad(outs, [ts[n] for n in leaves], grad_outputs=gouts,
+                                allow_unused=True)
     return {n: (np.zeros(ts[n].shape) if gr is None else gr.numpy())
             for n, gr in zip(leaves, grads)}

@@ -532,6 +532,63 @@ def pin_bwd_finite_differences(bwd, seed=16, eps=1e-6):
     return worst
 
 
+def pin_bwd_state_finite_differences(bwd, seed=17, eps=1e-6):
+    """With an initial state h0 and a gradient dh_last on the last state:
+    every gradient, h0's included, against central differences of the C
+    oracle's forward from h0 along a random direction per input:
+    <grad_X, v> = d/de (<dout, y(X + e v)> + <dh_last, h_last(X + e v)>)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for kw in (dict(), dict(softplus=False, bias=True, gate=False, skip=True, a_neg=False)):
+        p = random_problem(rng, batch=2, L=6, dim=3, N=4, **kw)
+        p["h0"] = rng.standard_normal((2, 3, 4))
+        dout = rng.standard_normal(p["u"].shape)
+        dh = rng.standard_normal((2, 3, 4))
+        grads = bwd(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"],
+                    p["delta_bias"], p["softplus"], dout, h0=p["h0"], dh_last=dh)
+        assert "h0" in grads
+        for name, g in grads.items():
+            v = rng.standard_normal(np.shape(p[name]))
+            plus = {**p, name: p[name] + eps * v}
+            minus = {**p, name: p[name] - eps * v}
+            yp, hp = _call(oracle.selective_scan_fwd, plus, h0=plus["h0"])
+            ym, hm = _call(oracle.selective_scan_fwd, minus, h0=minus["h0"])
+            fd = float((np.sum(dout * (yp - ym)) + np.sum(dh * (hp - hm))) / (2 * eps))
+            an = float(np.sum(g * v))
+            worst = max(worst, abs(fd - an) / (1.0 + abs(fd)))
+    return worst
+
+
+def pin_bwd_chaining(bwd, seed=18, cut=4):
+    """The gradients of a sequence equal those of its two pieces chained:
+    the second piece starts from the first's last state, and its h0 gradient
+    is the first piece's dh_last; per-step gradients concatenate and the
+    shared ones (A, D, delta_bias) add."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    p = random_problem(rng, batch=2, L=9, dim=3, N=4)
+    dout = rng.standard_normal(p["u"].shape)
+    whole = bwd(p["u"], p["delta"], p["A"], p["B"], p["C"], p["D"], p["z"], p["delta_bias"],
+                p["softplus"], dout)
+    cut_t = lambda a, s: None if a is None else a[:, s]  # noqa: E731
+    p1 = {k: (cut_t(v, slice(0, cut)) if k in ("u", "delta", "B", "C", "z") else v)
+          for k, v in p.items()}
+    p2 = {k: (cut_t(v, slice(cut, None)) if k in ("u", "delta", "B", "C", "z") else v)
+          for k, v in p.items()}
+    _, hmid = _call(oracle.selective_scan_fwd, p1)
+    g2 = bwd(p2["u"], p2["delta"], p2["A"], p2["B"], p2["C"], p2["D"], p2["z"],
+             p2["delta_bias"], p2["softplus"], dout[:, cut:], h0=hmid)
+    g1 = bwd(p1["u"], p1["delta"], p1["A"], p1["B"], p1["C"], p1["D"], p1["z"],
+             p1["delta_bias"], p1["softplus"], dout[:, :cut], dh_last=g2["h0"])
+    worst = 0.0
+    for k in ("u", "delta", "B", "C", "z"):
+        worst = max(worst, _rel_err(np.concatenate([g1[k], g2[k]], axis=1), whole[k]))
+    for k in ("A", "D", "delta_bias"):
+        worst = max(worst, _rel_err(g1[k] + g2[k], whole[k]))
+    return worst
+
+
 ALL_PINS = {
     "bruteforce": (pin_bruteforce, 1e-12),
     "lti_direct": (pin_lti_direct, 1e-9),

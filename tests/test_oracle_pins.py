@@ -98,3 +98,25 @@ def test_oracle_backward_catches_a_wrong_gradient():
         g["B"] = g["B"] * 1.01
         return g
     assert pin_bwd_finite_differences(broken) > 1e-5
+
+
+def test_backward_with_states_matches_finite_differences():
+    from oracle.backward import selective_scan_bwd
+    from tests.oracle_pins import pin_bwd_state_finite_differences
+    assert pin_bwd_state_finite_differences(selective_scan_bwd) <= 1e-7
+
+
+def test_backward_chains_through_the_state():
+    from oracle.backward import selective_scan_bwd
+    from tests.oracle_pins import pin_bwd_chaining
+    assert pin_bwd_chaining(selective_scan_bwd) <= 1e-12
+
+
+def test_state_finite_differences_reject_a_dropped_terminal_gradient():
+    """A backward that ignores dh_last fails the pin."""
+    from oracle.backward import selective_scan_bwd
+    from tests.oracle_pins import pin_bwd_state_finite_differences
+
+    def broken(*a, h0=None, dh_last=None):
+        return selective_scan_bwd(*a, h0=h0)
+    assert pin_bwd_state_finite_differences(broken) > 1e-3
