@@ -309,6 +309,34 @@ SSM_API int ssm_scan_bwd_bf16(const uint16_t *u, const uint16_t *delta, const fl
                  int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream);
 
 /*
+ * The backward pass of a piece of a longer sequence: the scan starts from h0
+ * (batch, dim, N; fp32, NULL = zero state, as ssm_scan_fwd*_h0) and the loss
+ * also depends on the last state through dh_last = dL/dh_last (batch, dim,
+ * N; fp32, NULL = zero).  Besides the gradients of ssm_scan_bwd /
+ * ssm_scan_bwd_bf16 (same arguments and types) it writes dh0 = dL/dh0
+ * (batch, dim, N; fp32; NULL = not written).  A sequence cut into pieces has
+ * the gradients of the whole when each piece runs from the previous piece's
+ * last state and takes as dh_last the next piece's dh0 (the adjoint
+ * recurrence of doyouknow.kr Mamba guide, section 3-3, carried across the
+ * cut).  With L = 0, dh0 = dh_last.  dh0 must not overlap any input or
+ * output; scratch, limits and errors as for ssm_scan_bwd.
+ */
+SSM_API int ssm_scan_bwd_h0(const float *u, const float *delta, const float *A,
+                 const float *B, const float *C, const float *D,
+                 const float *z, const float *delta_bias, int softplus_flag,
+                 const float *dy, float *du, float *ddelta, float *dA, float *dB,
+                 float *dC, float *dD, float *dz, float *ddelta_bias,
+                 const float *h0, const float *dh_last, float *dh0,
+                 int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream);
+SSM_API int ssm_scan_bwd_bf16_h0(const uint16_t *u, const uint16_t *delta, const float *A,
+                 const uint16_t *B, const uint16_t *C, const float *D,
+                 const uint16_t *z, const float *delta_bias, int softplus_flag,
+                 const uint16_t *dy, uint16_t *du, uint16_t *ddelta, float *dA,
+                 uint16_t *dB, uint16_t *dC, float *dD, uint16_t *dz, float *ddelta_bias,
+                 const float *h0, const float *dh_last, float *dh0,
+                 int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream);
+
+/*
  * No-allocation variant of ssm_scan_fwd_bf16 (an engineering addition: the
  * pages describe nothing like it).  Same arguments, same kernels, same
  * results bit for bit; the only difference is where the time-segment

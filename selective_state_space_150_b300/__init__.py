@@ -13,6 +13,8 @@ from .ssmscan import (  # noqa: F401
     ssm_conv_scan_fwd_bf16,
     ssm_scan_bwd,
     ssm_scan_bwd_bf16,
+    ssm_scan_bwd_bf16_h0,
+    ssm_scan_bwd_h0,
     ssm_scan_fwd,
     ssm_scan_fwd_bf16,
     ssm_scan_fwd_bf16_host,

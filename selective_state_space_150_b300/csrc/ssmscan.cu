@@ -1553,6 +1553,9 @@ struct BwdParams {
     float* pD;     // [batch][dim]
     float* pbias;  // [batch][dim]
     float* pt;     // [nslice][3][batch][L][dim] per-slice sums (N > kBwdSlice only)
+    const float* h0;       // [batch][dim][N] state before step 0, or NULL (zero)
+    const float* dh_last;  // [batch][dim][N] gradient on the last state, or NULL (zero)
+    float* dh0;            // [batch][dim][N] gradient of h0, or NULL (not written)
     int64_t batch, L, dim, N, ntile, nchunks, nslice;
     int softplus;
 };
@@ -1754,9 +1757,11 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
     };
 
     // ---- forward: the state at the start of every chunk
+    const int64_t hrow = (b * dim + d) * N;  // this channel's states in h0, dh_last, dh0
     float h[NPT];
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) h[j] = 0.f;
+    for (int j = 0; j < NPT; ++j)
+        h[j] = (q.h0 != nullptr && ok && n0 + j < N) ? q.h0[hrow + n0 + j] : 0.f;
     Fetched f;
     if (q.nchunks > 0) fetch(0, false, f);
     for (int64_t c = 0; c < q.nchunks; ++c) {
@@ -1784,9 +1789,14 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
     }
 
     // ---- reverse
-    float carry[NPT], gA[NPT];  // carry = exp(dt_{t+1} A) lam_{t+1}
+    // carry = exp(dt_{t+1} A) lam_{t+1}: the gradient on the state after step
+    // t from the steps after it; after the last step, the given dh_last
+    float carry[NPT], gA[NPT];
 #pragma unroll
-    for (int j = 0; j < NPT; ++j) carry[j] = gA[j] = 0.f;
+    for (int j = 0; j < NPT; ++j) {
+        carry[j] = (q.dh_last != nullptr && ok && n0 + j < N) ? q.dh_last[hrow + n0 + j] : 0.f;
+        gA[j] = 0.f;
+    }
     float gD = 0.f, gbias = 0.f;
     float* const myh = sm + SM::hs + sg * kBwdTC * NPT * 32;
     float* const part = sm + SM::part;
@@ -1919,6 +1929,8 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
         for (int j = 0; j < NPT; ++j) {
             const int64_t n = n0 + j;
             if (n < N) q.pA[(b * dim + d) * N + n] = gA[j];
+            // past step 0, carry is the gradient on the state before it: h0
+            if (n < N && q.dh0 != nullptr) q.dh0[hrow + n] = carry[j];
         }
     }
     if (split) return;  // dD and ddelta_bias come from the slice-summing kernel
@@ -2761,7 +2773,8 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
              const float* D, const T* z, const float* delta_bias, int softplus_flag,
              const T* dy, T* du, T* ddelta, float* dA, T* dB, T* dC,
              float* dD, T* dz, float* ddelta_bias, int64_t batch, int64_t L, int64_t dim,
-             int64_t N, cudaStream_t stream) {
+             int64_t N, cudaStream_t stream, const float* h0 = nullptr,
+             const float* dh_last = nullptr, float* dh0 = nullptr) {
     if (batch < 0 || L < 0 || dim < 0 || N < 1) return SSM_ERR_SIZE;
     if (N > kBwdMaxN) return SSM_ERR_UNSUPPORTED_N;
     int64_t n_bld, n_bln, n_dn, n_bdn, tmp;
@@ -2780,15 +2793,18 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
                             (const void*)dz})
         if (ptr && !aligned(ptr, es)) return SSM_ERR_ALIGN;
     for (const void* ptr : {(const void*)A, (const void*)D, (const void*)delta_bias,
-                            (const void*)dA, (const void*)dD, (const void*)ddelta_bias})
+                            (const void*)dA, (const void*)dD, (const void*)ddelta_bias,
+                            (const void*)h0, (const void*)dh_last, (const void*)dh0})
         if (ptr && !aligned(ptr, 4)) return SSM_ERR_ALIGN;
-    const int64_t by = n_bld * int64_t(es), bn = n_bln * int64_t(es);
+    const int64_t by = n_bld * int64_t(es), bn = n_bln * int64_t(es), bh = n_bdn * 4;
     const struct { const void* p; int64_t n; } ins[] = {
         {u, by}, {delta, by}, {z, z ? by : 0}, {dy, by}, {B, bn}, {C, bn}, {A, n_dn * 4},
-        {D, D ? dim * 4 : 0}, {delta_bias, delta_bias ? dim * 4 : 0}};
+        {D, D ? dim * 4 : 0}, {delta_bias, delta_bias ? dim * 4 : 0},
+        {h0, h0 ? bh : 0}, {dh_last, dh_last ? bh : 0}};
     const struct { const void* p; int64_t n; } outs[] = {
         {du, by}, {ddelta, by}, {dz, dz ? by : 0}, {dB, bn}, {dC, bn}, {dA, n_dn * 4},
-        {dD, dD ? dim * 4 : 0}, {ddelta_bias, ddelta_bias ? dim * 4 : 0}};
+        {dD, dD ? dim * 4 : 0}, {ddelta_bias, ddelta_bias ? dim * 4 : 0},
+        {dh0, dh0 ? bh : 0}};
     for (const auto& o : outs) {
         for (const auto& in : ins)
             if (overlaps(o.p, o.n, in.p, in.n)) return SSM_ERR_ALIAS;
@@ -2799,11 +2815,15 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     const int64_t ntile = (dim + 31) / 32;
     const int64_t nchunks = (L + kBwdTC - 1) / kBwdTC;
     if (batch * ntile > int64_t(0x7fffffff)) return SSM_ERR_SIZE;
-    if (L == 0) {  // no step: every gradient is zero
+    if (L == 0) {  // no step: every gradient is zero, but h0's, which is dh_last
         for (const auto& o : outs)
             if (o.p && o.n > 0 &&
                 cudaMemsetAsync(const_cast<void*>(o.p), 0, size_t(o.n), stream) != cudaSuccess)
                 return SSM_ERR_LAUNCH;
+        if (dh0 && dh_last && bh > 0 &&
+            cudaMemcpyAsync(dh0, dh_last, size_t(bh), cudaMemcpyDeviceToDevice, stream) !=
+                cudaSuccess)
+            return SSM_ERR_LAUNCH;
         return SSM_OK;
     }
     const int64_t nslice = (N + kBwdSlice - 1) / kBwdSlice;
@@ -2833,6 +2853,9 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     q.pt = nslice > 1 ? q.pbias + n_rd : nullptr;
     q.batch = batch; q.L = L; q.dim = dim; q.N = N; q.ntile = ntile; q.nchunks = nchunks;
     q.nslice = nslice;
+    q.h0 = h0;
+    q.dh_last = dh_last;
+    q.dh0 = dh0;
     q.softplus = softplus_flag ? 1 : 0;
     // every (tile, b, t, n < N) entry of the partial dB / dC is written by
     // exactly one lane
@@ -3018,6 +3041,35 @@ int ssm_scan_bwd(const float* u, const float* delta, const float* A, const float
                  int64_t L, int64_t dim, int64_t N, cudaStream_t stream) {
     return scan_bwd<float>(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, ddelta,
                            dA, dB, dC, dD, dz, ddelta_bias, batch, L, dim, N, stream);
+}
+
+int ssm_scan_bwd_h0(const float* u, const float* delta, const float* A, const float* B,
+                    const float* C, const float* D, const float* z, const float* delta_bias,
+                    int softplus_flag, const float* dy, float* du, float* ddelta, float* dA,
+                    float* dB, float* dC, float* dD, float* dz, float* ddelta_bias,
+                    const float* h0, const float* dh_last, float* dh0, int64_t batch,
+                    int64_t L, int64_t dim, int64_t N, cudaStream_t stream) {
+    return scan_bwd<float>(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, ddelta,
+                           dA, dB, dC, dD, dz, ddelta_bias, batch, L, dim, N, stream, h0,
+                           dh_last, dh0);
+}
+
+int ssm_scan_bwd_bf16_h0(const uint16_t* u, const uint16_t* delta, const float* A,
+                         const uint16_t* B, const uint16_t* C, const float* D,
+                         const uint16_t* z, const float* delta_bias, int softplus_flag,
+                         const uint16_t* dy, uint16_t* du, uint16_t* ddelta, float* dA,
+                         uint16_t* dB, uint16_t* dC, float* dD, uint16_t* dz,
+                         float* ddelta_bias, const float* h0, const float* dh_last, float* dh0,
+                         int64_t batch, int64_t L, int64_t dim, int64_t N,
+                         cudaStream_t stream) {
+    using bf = __nv_bfloat16;
+    return scan_bwd<bf>(reinterpret_cast<const bf*>(u), reinterpret_cast<const bf*>(delta), A,
+                        reinterpret_cast<const bf*>(B), reinterpret_cast<const bf*>(C), D,
+                        reinterpret_cast<const bf*>(z), delta_bias, softplus_flag,
+                        reinterpret_cast<const bf*>(dy), reinterpret_cast<bf*>(du),
+                        reinterpret_cast<bf*>(ddelta), dA, reinterpret_cast<bf*>(dB),
+                        reinterpret_cast<bf*>(dC), dD, reinterpret_cast<bf*>(dz), ddelta_bias,
+                        batch, L, dim, N, stream, h0, dh_last, dh0);
 }
 
 int ssm_scan_bwd_bf16(const uint16_t* u, const uint16_t* delta, const float* A,

@@ -50,6 +50,7 @@ EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc",
             "ssm_scan_step", "ssm_scan_step_bf16",
             "ssm_conv_scan_fwd", "ssm_conv_scan_fwd_bf16", "ssm_scan_host_workspace_bytes",
             "ssm_scan_fwd_host", "ssm_scan_fwd_bf16_host", "ssm_scan_bwd", "ssm_scan_bwd_bf16",
+            "ssm_scan_bwd_h0", "ssm_scan_bwd_bf16_h0",
             "ssm_scan_last_device_status", "ssm_status_string", "ssm_scan_plan", "ssm_set_knob")
 
 _vp = ctypes.c_void_p
@@ -72,6 +73,9 @@ _lib.ssm_scan_host_workspace_bytes.argtypes = [_i64, _i64, _i64, _i64, ctypes.c_
 _lib.ssm_scan_host_workspace_bytes.restype = _i64
 for _name in ("ssm_scan_bwd", "ssm_scan_bwd_bf16"):
     getattr(_lib, _name).argtypes = [_vp] * 8 + [ctypes.c_int] + [_vp] * 9 + [_i64] * 4 + [_vp]
+    getattr(_lib, _name).restype = ctypes.c_int
+for _name in ("ssm_scan_bwd_h0", "ssm_scan_bwd_bf16_h0"):
+    getattr(_lib, _name).argtypes = [_vp] * 8 + [ctypes.c_int] + [_vp] * 12 + [_i64] * 4 + [_vp]
     getattr(_lib, _name).restype = ctypes.c_int
 for _name in ("ssm_scan_step", "ssm_scan_step_bf16"):
     getattr(_lib, _name).argtypes = [_vp] * 8 + [ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _vp]
@@ -216,6 +220,27 @@ def ssm_scan_bwd_bf16(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du
                                   int(softplus_flag), p(dy), p(du), p(ddelta), p(dA), p(dB),
                                   p(dC), p(dD), p(dz), p(ddelta_bias), batch, L, dim, N,
                                   p(stream))
+
+
+def ssm_scan_bwd_h0(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, ddelta, dA, dB,
+                    dC, dD, dz, ddelta_bias, h0, dh_last, dh0, batch, L, dim, N, stream) -> int:
+    """fp32 backward from h0 with dh_last, writing dh0; pointers are ints."""
+    p = lambda v: v or None  # noqa: E731
+    return _lib.ssm_scan_bwd_h0(p(u), p(delta), p(A), p(B), p(C), p(D), p(z), p(delta_bias),
+                                int(softplus_flag), p(dy), p(du), p(ddelta), p(dA), p(dB), p(dC),
+                                p(dD), p(dz), p(ddelta_bias), p(h0), p(dh_last), p(dh0), batch,
+                                L, dim, N, p(stream))
+
+
+def ssm_scan_bwd_bf16_h0(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, ddelta, dA,
+                         dB, dC, dD, dz, ddelta_bias, h0, dh_last, dh0, batch, L, dim, N,
+                         stream) -> int:
+    """bf16 backward from h0 with dh_last, writing dh0; pointers are ints."""
+    p = lambda v: v or None  # noqa: E731
+    return _lib.ssm_scan_bwd_bf16_h0(p(u), p(delta), p(A), p(B), p(C), p(D), p(z),
+                                     p(delta_bias), int(softplus_flag), p(dy), p(du), p(ddelta),
+                                     p(dA), p(dB), p(dC), p(dD), p(dz), p(ddelta_bias), p(h0),
+                                     p(dh_last), p(dh0), batch, L, dim, N, p(stream))
 
 
 def ssm_scan_step(u, delta, A, B, C, D, z, delta_bias, softplus_flag, h, y, batch, dim, N,
@@ -372,18 +397,20 @@ def selective_scan_step(u, delta, A, B, C, h, D=None, z=None, delta_bias=None, s
 
 
 def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=False,
-                       stream=None):
+                       stream=None, h0=None, dh_last=None):
     """Gradients of selective_scan_fwd's y given dy, for contiguous CUDA
     tensors that are all fp32, or bf16 u/delta/B/C/z/dy with fp32 A/D/
     delta_bias.  Returns a dict with du, ddelta, dA, dB, dC and dD, dz,
     ddelta_bias where D, z, delta_bias are given; each gradient has the dtype
-    of its input."""
+    of its input.  With h0 (the state before step 0) or dh_last (the gradient
+    on the last state), both fp32 (batch, dim, N), the dict also holds dh0."""
     import torch
 
     bf = u.dtype == torch.bfloat16
     io = torch.bfloat16 if bf else torch.float32
     for t, want in ((u, io), (delta, io), (B, io), (C, io), (z, io), (dy, io),
-                    (A, torch.float32), (D, torch.float32), (delta_bias, torch.float32)):
+                    (A, torch.float32), (D, torch.float32), (delta_bias, torch.float32),
+                    (h0, torch.float32), (dh_last, torch.float32)):
         if t is not None and (t.dtype != want or not t.is_cuda or not t.is_contiguous()):
             raise TypeError("the backward pass takes contiguous CUDA tensors: all fp32, or bf16 "
                             "u/delta/B/C/z/dy with fp32 A/D/delta_bias")
@@ -399,12 +426,17 @@ def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, s
         g["ddelta_bias"] = torch.empty_like(delta_bias)
     if stream is None:
         stream = torch.cuda.current_stream(u.device).cuda_stream
-    fn = ssm_scan_bwd_bf16 if bf else ssm_scan_bwd
-    st = fn(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+    args = (_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
             _ptr(delta_bias), int(bool(softplus)), _ptr(dy), _ptr(g["du"]),
             _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]),
-            _ptr(g.get("dD")), _ptr(g.get("dz")), _ptr(g.get("ddelta_bias")),
-            batch, L, dim, N, int(stream))
+            _ptr(g.get("dD")), _ptr(g.get("dz")), _ptr(g.get("ddelta_bias")))
+    if h0 is not None or dh_last is not None:
+        g["dh0"] = torch.empty((batch, dim, N), dtype=torch.float32, device=u.device)
+        fn = ssm_scan_bwd_bf16_h0 if bf else ssm_scan_bwd_h0
+        st = fn(*args, _ptr(h0), _ptr(dh_last), _ptr(g["dh0"]), batch, L, dim, N, int(stream))
+    else:
+        fn = ssm_scan_bwd_bf16 if bf else ssm_scan_bwd
+        st = fn(*args, batch, L, dim, N, int(stream))
     if st != SSM_OK:
         raise SSMError(st, fn.__name__)
     return g

@@ -266,3 +266,20 @@ def test_backward_checks(fn, es):
     assert bwd(fn, du=Q + es // 2) == ssmscan.SSM_ERR_ALIGN       # du off its element size
     assert bwd(fn, dA=Q + 0x200000 + 2) == ssmscan.SSM_ERR_ALIGN  # fp32 dA off 4 bytes
     assert bwd(fn, batch=0) == ssmscan.SSM_OK
+
+
+@pytest.mark.parametrize("fn", [ssm.ssm_scan_bwd_h0, ssm.ssm_scan_bwd_bf16_h0])
+def test_backward_with_states_checks(fn):
+    def call(**kw):
+        args = dict(h0=0, dh_last=0, dh0=0)
+        args.update(kw)
+        return bwd(fn, **args)
+    H = Q + 0x800000
+    assert call(N=129) == ssmscan.SSM_ERR_UNSUPPORTED_N
+    assert call(u=0) == ssmscan.SSM_ERR_NULL
+    assert call(dh0=H + 2) == ssmscan.SSM_ERR_ALIGN
+    assert call(h0=P + 0x600002) == ssmscan.SSM_ERR_ALIGN
+    assert call(dh0=Q + 0x40) == ssmscan.SSM_ERR_ALIAS             # dh0 inside du
+    assert call(h0=H, dh0=H) == ssmscan.SSM_ERR_ALIAS              # dh0 is h0
+    assert call(dh_last=H + 0x40, dh0=H) == ssmscan.SSM_ERR_ALIAS  # dh0 overlaps dh_last
+    assert call(batch=0, h0=H, dh0=H + 0x100000) == ssmscan.SSM_OK

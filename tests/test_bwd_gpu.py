@@ -179,3 +179,81 @@ def test_backward_full_size_mamba130m_bf16_sampled():
     for name, k in (("dA", "A"), ("dD", "D"), ("ddelta_bias", "delta_bias")):
         err = rel_err(g[name][ds], r[k])
         assert err <= TOL, (name, err)
+
+
+
+# ---------------------------------------------------------------- pieces of a sequence
+def _state_problem(shape, seed, dtype="f32", **flags):
+    batch, L, dim, N = shape
+    wl = BASE.with_shape(name="g", batch=batch, L=L, dim=dim, N=N, dtype=dtype, **flags)
+    inp = W.make_inputs(wl, seed=seed)
+    rng = np.random.default_rng(seed + 1)
+    h0 = rng.standard_normal((batch, dim, N)).astype(np.float32)
+    dh = rng.standard_normal((batch, dim, N)).astype(np.float32)
+    dy = rng.standard_normal((batch, L, dim)).astype(np.float32)
+    if dtype == "bf16":
+        dy = W.f32_to_bf16_bits(dy)
+    return inp, h0, dh, dy
+
+
+def _gpu_state_grads(inp, dy, h0, dh):
+    d = {k: to_dev(inp[k]) for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}
+    g = ssm.selective_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], to_dev(dy), d["D"],
+                               d["z"], d["delta_bias"], inp["softplus"],
+                               h0=None if h0 is None else to_dev(h0),
+                               dh_last=None if dh is None else to_dev(dh))
+    torch.cuda.synchronize()
+    return {k: from_dev(v) for k, v in g.items()}
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 40, 72, 16), (1, 37, 33, 5), (1, 30, 40, 40)])
+@pytest.mark.parametrize("which", ["both", "h0", "dh_last"])
+def test_backward_with_states_matches_oracle(dtype, shape, which):
+    inp, h0, dh, dy = _state_problem(shape, sum(shape) + 3, dtype, **FLAGS[0])
+    h0 = h0 if which in ("both", "h0") else None
+    dh = dh if which in ("both", "dh_last") else None
+    g = _gpu_state_grads(inp, dy, h0, dh)
+    x = W.decoded(inp)
+    r = oracle_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
+                   x["softplus"], W.decode(dy), h0=h0, dh_last=dh)
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "delta_bias": "ddelta_bias", "h0": "dh0"}
+    if "h0" not in r:  # no h0 given: its gradient still comes back, against a zero start
+        r["h0"] = oracle_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"],
+                             x["delta_bias"], x["softplus"], W.decode(dy),
+                             h0=np.zeros_like(g["dh0"]), dh_last=dh)["h0"]
+    for k, v in r.items():
+        bf = dtype == "bf16" and k in ("u", "delta", "B", "C", "z")
+        err = rel_err(g[names[k]], v)
+        assert err <= (BF16_TOL if bf else TOL), (names[k], err)
+
+
+def test_backward_pieces_chain_to_the_whole():
+    """A sequence's gradients from two pieces: the second from the first's last
+    state, the first with the second's dh0 as dh_last."""
+    shape = (2, 80, 64, 16)
+    inp, _, _, dy = _state_problem(shape, 31, **FLAGS[0])
+    whole = _gpu_state_grads(inp, dy, None, None)
+    cut = 48
+    part = lambda s: {k: (v[:, s] if k in ("u", "delta", "B", "C", "z") and v is not None else v)
+                      for k, v in inp.items()}  # noqa: E731
+    p1, p2 = part(slice(0, cut)), part(slice(cut, None))
+    d = {k: to_dev(p1[k]) for k in ("u", "delta", "B", "C", "z", "A", "D", "delta_bias")}
+    y1, hmid = ssm.selective_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                      d["delta_bias"], p1["softplus"])
+    g2 = _gpu_state_grads(p2, dy[:, cut:], hmid.cpu().numpy(), None)
+    g1 = _gpu_state_grads(p1, dy[:, :cut], None, g2["dh0"])
+    for k in ("du", "ddelta", "dz", "dB", "dC"):
+        err = rel_err(np.concatenate([g1[k], g2[k]], axis=1), whole[k])
+        assert err <= 2e-5, (k, err)
+    for k in ("dA", "dD", "ddelta_bias"):
+        err = rel_err(g1[k] + g2[k], whole[k])
+        assert err <= 2e-5, (k, err)
+
+
+def test_backward_of_an_empty_piece_passes_dh_last_through():
+    inp, h0, dh, dy = _state_problem((2, 0, 32, 16), 5, **FLAGS[0])
+    g = _gpu_state_grads(inp, dy, h0, dh)
+    assert np.array_equal(g["dh0"], dh)
+    assert all(not np.any(v) for k, v in g.items() if k != "dh0")
