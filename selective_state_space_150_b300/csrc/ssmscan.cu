@@ -1,37 +1,38 @@
-// ssmscan.cu -- selective-scan forward (Mamba S6) for NVIDIA B300, sm_103a.
+// ssmscan.cu -- the selective scan of the Mamba S6 layer for NVIDIA B300, sm_103a.
 //
-// One fused kernel per call: discretise (dA = exp(dt*A), dBu = dt*B*u), scan
-// (h = dA*h + dBu, state in registers, never written to memory except the last
-// state), read out (y = <C, h> + D*u) and gate (y *= silu(z)).  The method is
-// the selective scan of the "State Space Models (SSM)" summary page, section
+// The forward is one fused pass: discretise (dA = exp(dt*A), dBu = dt*B*u),
+// scan (h = dA*h + dBu, state in registers, never written to memory except the
+// last state), read out (y = <C, h> + D*u) and gate (y *= silu(z)).  The method
+// is the selective scan of the "State Space Models (SSM)" summary page, section
 // 3.2; the softplus/bias, skip and gate steps follow the SelectiveSSM and
 // MambaBlock listings (same page, 5.1-5.2; youngju.dev "Mamba와 State Space
 // Model 논문 심층 분석").  Keeping the expanded state on chip is the design the
 // itwiki page ("Mamba의 선택 메커니즘") and the Obsidian "Mamba" note (5.1)
 // describe; the way it is mapped onto B300 here is our own.
 //
-// Work decomposition:
-//   * a block owns one batch row b and a tile of DT = 32 * WC consecutive
-//     channels and walks the sequence in chunks of TC = 32 timesteps;
-//   * its warps are WC channel tiles x WS state groups: lane = channel, and a
-//     warp's state group holds NPT states of each of its 32 channels in
-//     registers for the whole sequence (N <= WS * NPT);
-//   * per chunk, TMA (cp.async.bulk.tensor, 3-D maps over (dim, L, batch), with
-//     the 32/64/128-byte swizzle that matches the tile's row width) brings the
-//     u / delta / z tiles and the B / C rows into a two-stage ring tracked by
-//     mbarriers, up to three chunks ahead;
-//   * PREP: every thread handles (step, channel pair) items: B and C widened to
-//     fp32, dt = softplus(delta + bias), dt*u, the gate silu(z) and the skip
-//     D*u*silu(z), written to shared memory once per (t, d);
-//   * SCAN: every warp advances its states over the chunk; the B and C values a
-//     step needs are the same for the whole warp (uniform shared reads), dt and
-//     dt*u are one 64-bit read per lane, and each lane stores one partial
-//     readout per step;
-//   * POST: every (step, pair) item sums its WS partials, applies skip and gate,
-//     and writes y to a swizzled tile that one thread stores with a TMA bulk
-//     tensor store.
-// Shapes TMA cannot describe (rows not a multiple of 16 bytes, misaligned
-// pointers, L = 0) take the same kernel with plain loads and stores.
+// Work decomposition of the forward:
+//   * a block owns one batch row b and a tile of 32 consecutive channels (or
+//     more for small N) and walks the sequence in chunks of TC timesteps; lane
+//     = channel, and each warp's state group holds NPT states of its 32
+//     channels in registers for the whole sequence (N <= WS * NPT);
+//   * the default, warp-specialised kernel (ssm_scan_ws_kernel) is a pipeline
+//     of warp roles handing chunks over through mbarriers: one producer warp
+//     issues TMA loads (cp.async.bulk.tensor, 3-D maps over (dim, L, batch),
+//     swizzled to the tile's row width) into a ring of stages; two prepare
+//     warps compute dt = softplus(delta + bias), dt*u and widen B and C; the
+//     scan warps advance their states and leave one partial readout per
+//     (step, channel, state group); two finish warps add the partials, apply
+//     skip and gate and store y by TMA.  Three buffers between consecutive
+//     roles let each run up to three chunks ahead;
+//   * shapes TMA cannot describe (rows not a multiple of 16 bytes, misaligned
+//     pointers, L = 0) take a phase kernel (ssm_scan_fwd_kernel) that does the
+//     same arithmetic in the same order with plain loads and block barriers;
+//   * shapes with few channels cut the sequence into time segments: a summary
+//     pass records each segment's end state and sum of dt, and the main pass
+//     starts every segment from the composed state of the ones before it.
+// Also here: the prologue (causal conv1d + SiLU) and exact zero-order-hold
+// variants of the forward, a one-token recurrent step, a host-buffer call that
+// overlaps copies with compute, and the backward pass by recomputation.
 //
 // Every wait on an mbarrier is bounded by a time limit read from %globaltimer;
 // a wait that runs out sets a bit in a device status word, the block waits
@@ -1514,19 +1515,23 @@ __global__ void __launch_bounds__(128) ssm_step_kernel(const StepIn<T> q) {
 }
 
 // ============================================================ backward pass
-// Gradients of the scan (Euler B, zero initial state; fp32 or bf16 tensors,
-// fp32 arithmetic) with respect to u, delta, A, B, C, D, z and delta_bias,
-// given the gradient of y.
+// Gradients of the scan (Euler B; fp32 or bf16 tensors, fp32 arithmetic)
+// with respect to u, delta, A, B, C, D, z and delta_bias, given the gradient
+// of y, from a zero or given initial state h0 and with an optional gradient
+// on the last state (then also the gradient of h0).
 // The state is recomputed instead of stored (doyouknow.kr Mamba guide,
 // section 3-3, "recomputation"): a forward pass keeps only the state at the
 // start of every kBwdTC-step chunk; the reverse pass recomputes each chunk's
-// states into shared memory and runs the adjoint recurrence backwards,
+// states and runs the adjoint recurrence backwards,
 //   lam_t = dyc_t C_t + exp(dt_{t+1} A) lam_{t+1},   dyc_t = dy_t silu(z_t),
-// from which every input's gradient follows step by step.  One warp holds
-// 32 channels of one batch row, lane = channel, all N <= 16 states per lane.
-// Gradients of the shared B and C (sums over channels) leave each warp as
-// one partial per channel tile, and dA, D, delta_bias as one partial per
-// batch row; a second kernel folds the partials in a fixed order.
+// (lam_{L-1} also takes the last state's gradient) from which every input's
+// gradient follows step by step.  Lane = channel: a block holds 32 channels
+// of one batch row and up to kBwdSlice states, kBwdNPT per warp; larger N
+// runs as more blocks, one per slice of kBwdSlice states.  Gradients of the
+// shared B and C (sums over channels) leave each warp as one partial per
+// channel tile, and dA, D, delta_bias as partials per batch row (per run of
+// steps with slices); other kernels add the slices' per-step sums and fold
+// the partials, all in a fixed order.
 constexpr int kBwdTC = 16;
 constexpr int kBwdSlice = 16;  // states per block; larger N runs as slices of 16 states
 constexpr int kBwdMaxN = 128;
