@@ -486,6 +486,48 @@ def bwd_accounting(wl: W.Workload, es: int = 4):
     return nbytes, mufu
 
 
+def op_cpu_baseline(kind: str, wl: W.Workload, inp, rows: int = 1, n_dim: int = 16,
+                    L_s: int = 0, extra=None):
+    """The oracle, as it stands, timed single-threaded on a small sample of
+    the workload for one of the --op calls: batch rows 0 .. rows-1, n_dim
+    seeded channels, the first L_s steps (all when 0).  Returns the
+    cpu_baseline object, its value scaled to the full problem in tokens/s."""
+    import oracle
+    L_s = L_s or wl.L
+    ds = np.sort(np.random.default_rng(3).choice(wl.dim, size=min(n_dim, wl.dim), replace=False))
+    sub = W.gather(inp, np.arange(rows), ds)
+    cut = {k: (v[:, :L_s] if k in ("u", "delta", "B", "C", "z") and v is not None else v)
+           for k, v in sub.items()}
+    args = (cut["u"], cut["delta"], cut["A"], cut["B"], cut["C"], cut["D"], cut["z"],
+            cut["delta_bias"], cut["softplus"])
+    t0 = time.perf_counter()
+    if kind == "conv_scan":
+        w, cb = extra
+        oracle.conv_selective_scan_fwd(cut["u"], w[ds], cb[ds], *args[1:])
+    elif kind == "zoh_scan":
+        oracle.selective_scan_fwd(*args, zoh=True)
+    elif kind == "bwd":
+        from oracle.backward import selective_scan_bwd as oracle_bwd
+        dy = np.random.default_rng(4).standard_normal(cut["u"].shape)
+        oracle_bwd(*args, dy)
+    wall = time.perf_counter() - t0
+    tokens = rows * L_s * len(ds) / wl.dim
+    return {"value": tokens / wall, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} batch row(s) x {L_s} steps x {len(ds)} of {wl.dim} channels "
+                      f"(N={wl.N}), fp64, one host thread; tokens scaled by {len(ds)}/{wl.dim}"}
+
+
+def mufu_roofline(mufu_ops: int, ms: float, peaks) -> dict:
+    """The compute roofline of a call bound by the MUFU exponentials."""
+    roof = {"bound": "alu", "pipe": "mufu_ex2", "unit": "Gop/s", "mufu_ops_per_launch": mufu_ops,
+            "achieved": mufu_ops / (ms * 1e-3) / 1e9, "traffic": None}
+    if "ex2_per_s" in peaks:
+        roof["peak"] = peaks["ex2_per_s"] / 1e9
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["peak_source"] = "measured on this GPU by libpipepeaks, same run"
+    return roof
+
+
 def _events_mean_ms(fn, reps, stream):
     import torch
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -576,6 +618,8 @@ def run_op(args, wl):
             "ms_per_step": ms_bwd, "steps": args.steps, "warmup": args.warmup,
             "io_dtype": wl.dtype, "fp32_io_ms": ms_f32, "fp32_forward_ms": ms_fwd,
             "roofline": roof, "dtype": "f32",
+            "cpu_baseline": None if args.no_cpu_baseline else op_cpu_baseline(
+                "bwd", wl, inp, n_dim=8, L_s=256),
             "data": "synthetic (seeded; see ssm_workloads.py); fp32_io_ms: the same values "
                     "widened to fp32",
             "config": config_of(wl, "one resident copy"), "impl": "ours"}
@@ -605,6 +649,10 @@ def run_op(args, wl):
             "value": wl.tokens / (ms_zoh * 1e-3), "unit": "tokens/s", "higher_is_better": True,
             "ms_per_step": ms_zoh, "steps": args.steps, "warmup": args.warmup,
             "euler_scan_ms": ms_scan, "zoh_cost_ms": ms_zoh - ms_scan,
+            "roofline": mufu_roofline(algorithmic_ops(wl)[0], ms_zoh,
+                                      pipe_peaks(stream.cuda_stream)),
+            "cpu_baseline": None if args.no_cpu_baseline else op_cpu_baseline(
+                "zoh_scan", wl, inp, n_dim=256),
             "dtype": "f32", "data": "synthetic (seeded; see ssm_workloads.py)",
             "config": config_of(wl, "inputs rotate over 2 resident copies"), "impl": "ours"}
     if args.op == "conv_scan":
@@ -648,6 +696,11 @@ def run_op(args, wl):
             "hbm": {"achieved_gbs": bytes_launch / (ms_conv * 1e-3) / 1e9, "peak_gbs": hbm_gbs,
                     "frac": bytes_launch / (ms_conv * 1e-3) / 1e9 / hbm_gbs,
                     "peak_source": hbm_src},
+            # the prologue's SiLU adds an exponential and a reciprocal per (b, t, d)
+            "roofline": mufu_roofline(algorithmic_ops(wl)[0] + 2 * wl.batch * wl.L * wl.dim,
+                                      ms_conv, pipe_peaks(stream.cuda_stream)),
+            "cpu_baseline": None if args.no_cpu_baseline else op_cpu_baseline(
+                "conv_scan", wl, inp, n_dim=256, extra=(w.cpu().numpy(), cb.cpu().numpy())),
             "dtype": "f32", "data": "synthetic (seeded; see ssm_workloads.py)",
             "config": config_of(wl, "inputs rotate over 2 resident copies"), "impl": "ours"}
     # one-token step over the workload's (batch, dim, N) states
@@ -678,13 +731,27 @@ def run_op(args, wl):
     torch.cuda.synchronize()
     us = a.elapsed_time(b) * 1e3 / (reps * 100)
     state_bytes = wl.batch * wl.dim * wl.N * 8 + wl.dim * wl.N * 4
+    cpu = None
+    if not args.no_cpu_baseline:
+        # the oracle's step over every channel of the workload, one host thread
+        import oracle
+        x = W.decoded({k: (None if inp[k] is None else inp[k][:, :1]) if k in
+                       ("u", "delta", "B", "C", "z") else inp[k] for k in inp})
+        t0 = time.perf_counter()
+        oracle.selective_scan_step(np.zeros((wl.batch, wl.dim, wl.N)), x["u"][:, 0],
+                                   x["delta"][:, 0], x["A"], x["B"][:, 0], x["C"][:, 0], x["D"],
+                                   None if x["z"] is None else x["z"][:, 0], x["delta_bias"],
+                                   x["softplus"])
+        cpu = {"value": (time.perf_counter() - t0) * 1e6, "unit": "us", "cores": 1,
+               "kind": "oracle", "sample": f"one step of all {wl.batch} x {wl.dim} channels "
+                                           f"(N={wl.N}), fp64, one host thread"}
     return {
         "op": "step", "metric": "one-token recurrent step latency", "value": us, "unit": "us",
         "higher_is_better": False, "tokens_per_s": wl.batch / (us * 1e-6),
         "steps_timed": reps * 100,
         "hbm": {"achieved_gbs": state_bytes / (us * 1e-6) / 1e9, "peak_gbs": hbm_gbs,
                 "frac": state_bytes / (us * 1e-6) / 1e9 / hbm_gbs, "peak_source": hbm_src},
-        "timing": "CUDA graph of 100 steps, device time per step",
+        "timing": "CUDA graph of 100 steps, device time per step", "cpu_baseline": cpu,
         "dtype": "f32", "data": "synthetic (seeded; see ssm_workloads.py)",
         "config": {"workload": wl.name, "batch": wl.batch, "dim": wl.dim, "N": wl.N,
                    "io_dtype": wl.dtype}, "impl": "ours"}
