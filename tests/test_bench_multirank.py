@@ -3,7 +3,6 @@ max-over-ranks reduction of the timed region (no GPU, no data-path collective)."
 import os
 import socket
 
-import pytest
 import torch.distributed as dist
 import torch.multiprocessing as mp
 

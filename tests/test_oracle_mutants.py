@@ -1,8 +1,6 @@
 """Plant plausible mistakes in a copy of the oracle and check that the pins
 catch every one (the committed oracle is never modified)."""
 import os
-import shutil
-import subprocess
 
 import pytest
 
