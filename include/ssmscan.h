@@ -280,8 +280,10 @@ SSM_API int ssm_scan_step_bf16(const uint16_t *u, const uint16_t *delta, const f
  * 16th step and per-block partial sums in stream-ordered scratch
  * (cudaMallocAsync / cudaFreeAsync on `stream`, about batch * L * dim * N / 4
  * plus 2 * batch * L * N * ceil(dim / 32) fp32 words; for N > 16, which runs
- * as slices of 16 states, also 3 * ceil(N / 16) * batch * L * dim).  Partials
- * are folded in a fixed order, so results are deterministic.  N <= 128
+ * as slices of 16 states, also 3 * ceil(N / 16) * batch * L * dim; with time
+ * segments, which the call uses when the batch rows and channels leave most
+ * of the GPU idle, also about 2 * segments * batch * dim * N).  Partials are
+ * folded in a fixed order, so results are deterministic.  N <= 128
  * (otherwise SSM_ERR_UNSUPPORTED_N).  Outputs must not overlap inputs or each
  * other.
  */
@@ -419,6 +421,9 @@ SSM_API int ssm_scan_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, int 
  *                           capped at the number of chunks); 0 = automatic
  *   SSM_KNOB_KERNEL         1: the phase kernel; 2 (or 0, automatic): the
  *                           warp-specialised kernel where tiles move by TMA
+ *   SSM_KNOB_BWD_SEGMENTS   force the backward's number of time segments
+ *                           (1 .. 64, at most one per 16-step chunk; 0 =
+ *                           automatic)
  * A forced combination the library is not built for falls back to automatic.
  * Returns SSM_OK or SSM_ERR_ARG.
  */
@@ -430,7 +435,8 @@ enum {
     SSM_KNOB_PLAIN_LOADS = 5,
     SSM_KNOB_STAGES = 6,
     SSM_KNOB_SEGMENTS = 7,
-    SSM_KNOB_KERNEL = 8
+    SSM_KNOB_KERNEL = 8,
+    SSM_KNOB_BWD_SEGMENTS = 9
 };
 SSM_API int ssm_set_knob(int key, int64_t value);
 

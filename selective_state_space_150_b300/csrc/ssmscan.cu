@@ -1561,7 +1561,13 @@ struct BwdParams {
     const float* h0;       // [batch][dim][N] state before step 0, or NULL (zero)
     const float* dh_last;  // [batch][dim][N] gradient on the last state, or NULL (zero)
     float* dh0;            // [batch][dim][N] gradient of h0, or NULL (not written)
-    int64_t batch, L, dim, N, ntile, nchunks, nslice;
+    // time segments (blockIdx.z): segment z covers chunks z*seg_chunks ..;
+    // per segment hseg = end state from zero, lseg = adjoint carry at its
+    // start from a zero terminal gradient, sseg = sum of dt (nseg > 1 only)
+    float* hseg;   // [nseg][batch][dim][N]
+    float* lseg;   // [nseg][batch][dim][N]
+    float* sseg;   // [nseg][batch][dim]
+    int64_t batch, L, dim, N, ntile, nchunks, nslice, nseg, seg_chunks;
     int softplus;
 };
 
@@ -1761,15 +1767,33 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
         for (int j = 0; j < NPT; ++j) h[j] = fmaf(ex2_approx(dt * a2[j]), h[j], du_ * bb[j]);
     };
 
-    // ---- forward: the state at the start of every chunk
+    // ---- this block's time segment: chunks c_begin .. c_end - 1
+    const int64_t zseg = blockIdx.z;
+    const int64_t c_begin = zseg * q.seg_chunks;
+    const int64_t c_end = c_begin + q.seg_chunks < q.nchunks ? c_begin + q.seg_chunks : q.nchunks;
     const int64_t hrow = (b * dim + d) * N;  // this channel's states in h0, dh_last, dh0
+    // per-segment summaries of (b, d, state n0 + j) for segment r
+    auto srow = [&](int64_t r) { return (r * q.batch + b) * dim + d; };
+
+    // ---- forward: the state at the start of every chunk.  A later segment
+    // starts from the earlier ones' end states composed over their decay:
+    // h <- exp(A sum dt) h + h_seg (the associative composition of spans).
     float h[NPT];
 #pragma unroll
     for (int j = 0; j < NPT; ++j)
         h[j] = (q.h0 != nullptr && ok && n0 + j < N) ? q.h0[hrow + n0 + j] : 0.f;
+    if (ok) {
+        for (int64_t r = 0; r < zseg; ++r) {
+            const float sdt = q.sseg[srow(r)];
+#pragma unroll
+            for (int j = 0; j < NPT; ++j)
+                if (n0 + j < N)
+                    h[j] = fmaf(ex2_approx(a2[j] * sdt), h[j], q.hseg[srow(r) * N + n0 + j]);
+        }
+    }
     Fetched f;
-    if (q.nchunks > 0) fetch(0, false, f);
-    for (int64_t c = 0; c < q.nchunks; ++c) {
+    if (c_end > c_begin) fetch(c_begin, false, f);
+    for (int64_t c = c_begin; c < c_end; ++c) {
         const int tv = chunk_len(c);
         if (ok) {
 #pragma unroll
@@ -1780,7 +1804,7 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
         __syncthreads();
         // the next chunk, or the last one again with the reverse pass's inputs
         // (its checkpoint was just written by this thread)
-        if (c + 1 < q.nchunks) fetch(c + 1, false, f);
+        if (c + 1 < c_end) fetch(c + 1, false, f);
         else fetch(c, true, f);
         // a whole chunk unrolled: later steps' loads and exponentials issue
         // while earlier steps' state updates wait on each other
@@ -1796,16 +1820,28 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
     // ---- reverse
     // carry = exp(dt_{t+1} A) lam_{t+1}: the gradient on the state after step
     // t from the steps after it; after the last step, the given dh_last
+    // A segment before the last one starts from the later segments' carries
+    // composed backwards: carry <- lam_seg + exp(A sum dt) carry.
     float carry[NPT], gA[NPT];
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
         carry[j] = (q.dh_last != nullptr && ok && n0 + j < N) ? q.dh_last[hrow + n0 + j] : 0.f;
         gA[j] = 0.f;
     }
+    if (ok) {
+        for (int64_t r = q.nseg - 1; r > zseg; --r) {
+            const float sdt = q.sseg[srow(r)];
+#pragma unroll
+            for (int j = 0; j < NPT; ++j)
+                if (n0 + j < N)
+                    carry[j] = fmaf(ex2_approx(a2[j] * sdt), carry[j],
+                                    q.lseg[srow(r) * N + n0 + j]);
+        }
+    }
     float gD = 0.f, gbias = 0.f;
     float* const myh = sm + SM::hs + sg * kBwdTC * NPT * 32;
     float* const part = sm + SM::part;
-    for (int64_t c = q.nchunks - 1; c >= 0; --c) {
+    for (int64_t c = c_end - 1; c >= c_begin; --c) {
         const int64_t t0 = c * kBwdTC;
         const int tv = chunk_len(c);
         float hstart[NPT];
@@ -1816,7 +1852,7 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
         }
         stage(f, tv, true);
         __syncthreads();
-        if (c > 0) fetch(c - 1, true, f);
+        if (c > c_begin) fetch(c - 1, true, f);
         // One reverse step from the states after step i and before it.  Only
         // carry links consecutive steps; the shuffle reductions of dB and dC
         // hang off it, so with the chunk unrolled several steps' reductions
@@ -1933,9 +1969,9 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
 #pragma unroll
         for (int j = 0; j < NPT; ++j) {
             const int64_t n = n0 + j;
-            if (n < N) q.pA[(b * dim + d) * N + n] = gA[j];
+            if (n < N) q.pA[((zseg * q.batch + b) * dim + d) * N + n] = gA[j];
             // past step 0, carry is the gradient on the state before it: h0
-            if (n < N && q.dh0 != nullptr) q.dh0[hrow + n] = carry[j];
+            if (n < N && q.dh0 != nullptr && zseg == 0) q.dh0[hrow + n] = carry[j];
         }
     }
     if (split) return;  // dD and ddelta_bias come from the slice-summing kernel
@@ -1950,8 +1986,8 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
             sD += red[(w * 2) * 32 + lane];
             sb += red[(w * 2 + 1) * 32 + lane];
         }
-        q.pD[b * dim + d] = sD;
-        q.pbias[b * dim + d] = sb;
+        q.pD[zseg * q.batch * dim + b * dim + d] = sD;
+        q.pbias[zseg * q.batch * dim + b * dim + d] = sb;
     }
 }
 
@@ -2015,6 +2051,89 @@ __global__ void __launch_bounds__(256) ssm_bwd_slices_kernel(const BwdParams q) 
     q.pbias[r * q.dim + d] = gbias;
 }
 
+// Time segments of the backward, per (batch row, channel tile, slice,
+// segment z): the segment's end state from a zero start and its sum of dt
+// (all but the last segment), and the adjoint carry at its start from a zero
+// terminal gradient (all but the first segment), which the main kernel
+// composes into each segment's start state and terminal carry.  The same
+// expressions as the main kernel's steps; lane = channel, kBwdNPT states per
+// warp; no block barrier.
+template <typename T, int WS>
+__global__ void __launch_bounds__(WS * 32) ssm_bwd_summary_kernel(const BwdParams q) {
+    using E = Elt<T>;
+    constexpr int NPT = kBwdNPT;
+    const int lane = threadIdx.x & 31, sg = threadIdx.x >> 5;
+    const int64_t tile = blockIdx.x % q.ntile, b = blockIdx.x / q.ntile;
+    const int64_t d = tile * 32 + lane;
+    if (d >= q.dim) return;
+    const int64_t N = q.N, L = q.L, dim = q.dim, z = blockIdx.z;
+    const int64_t n0 = int64_t(blockIdx.y) * kBwdSlice + int64_t(sg) * NPT;
+    const int64_t t_b = z * q.seg_chunks * kBwdTC;
+    const int64_t t_e = t_b + q.seg_chunks * kBwdTC < L ? t_b + q.seg_chunks * kBwdTC : L;
+    const T* const g_u = static_cast<const T*>(q.u);
+    const T* const g_delta = static_cast<const T*>(q.delta);
+    const T* const g_B = static_cast<const T*>(q.B);
+    const T* const g_C = static_cast<const T*>(q.C);
+    const T* const g_z = static_cast<const T*>(q.z);
+    const T* const g_dy = static_cast<const T*>(q.dy);
+    float a2[NPT];
+#pragma unroll
+    for (int j = 0; j < NPT; ++j) a2[j] = n0 + j < N ? q.A[d * N + n0 + j] * kLog2e : 0.f;
+    const float bias = q.bias != nullptr ? q.bias[d] : 0.f;
+    const int64_t row = (z * q.batch + b) * dim + d;
+    auto dt_at = [&](int64_t o) {
+        const float r = E::to_f(g_delta[o]) + bias;
+        return q.softplus ? Act<float>::softplus(r) : r;
+    };
+    double sdt = 0.0;
+    if (z < q.nseg - 1) {
+        float h[NPT];
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) h[j] = 0.f;
+        // unrolled so that several steps' loads are in flight at once
+#pragma unroll 8
+        for (int64_t t = t_b; t < t_e; ++t) {
+            const int64_t o = (b * L + t) * dim + d;
+            const float dt = dt_at(o);
+            const float du_ = dt * E::to_f(g_u[o]);
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) {
+                const float bb = n0 + j < N ? E::to_f(g_B[(b * L + t) * N + n0 + j]) : 0.f;
+                h[j] = fmaf(ex2_approx(dt * a2[j]), h[j], du_ * bb);
+            }
+            sdt += double(dt);
+        }
+#pragma unroll
+        for (int j = 0; j < NPT; ++j)
+            if (n0 + j < N) q.hseg[row * N + n0 + j] = h[j];
+    }
+    if (z > 0) {
+        const bool count = !(z < q.nseg - 1);  // the last segment sums dt here
+        float carry[NPT];
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) carry[j] = 0.f;
+#pragma unroll 8
+        for (int64_t t = t_e - 1; t >= t_b; --t) {
+            const int64_t o = (b * L + t) * dim + d;
+            const float dt = dt_at(o);
+            const float zv = q.z != nullptr ? E::to_f(g_z[o]) : 0.f;
+            const float g = q.z != nullptr ? zv / (1.f + expf(-zv)) : 1.f;
+            const float dyc = E::to_f(g_dy[o]) * g;
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) {
+                const float cc = n0 + j < N ? E::to_f(g_C[(b * L + t) * N + n0 + j]) : 0.f;
+                const float lam = fmaf(dyc, cc, carry[j]);
+                carry[j] = ex2_approx(dt * a2[j]) * lam;
+            }
+            if (count) sdt += double(dt);
+        }
+#pragma unroll
+        for (int j = 0; j < NPT; ++j)
+            if (n0 + j < N) q.lseg[row * N + n0 + j] = carry[j];
+    }
+    if (sg == 0 && blockIdx.y == 0) q.sseg[row] = float(sdt);
+}
+
 // ------------------------------------------------------------------ host side
 std::atomic<int64_t> g_wait_ns{2000000000LL};
 std::atomic<int> g_force_timeout{0};
@@ -2023,6 +2142,7 @@ std::atomic<int> g_force_stages{0};
 std::atomic<int> g_force_chunk{0};
 std::atomic<int> g_force_segments{0};
 std::atomic<int> g_force_kernel{0};
+std::atomic<int> g_force_bwd_segments{0};
 std::atomic<int> g_plain_loads{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -2832,14 +2952,34 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
         return SSM_OK;
     }
     const int64_t nslice = (N + kBwdSlice - 1) / kBwdSlice;
+    // Time segments when the (row, tile, slice) blocks leave more than half of
+    // the SMs idle: as many as still fit one wave of three blocks per SM, each
+    // at least 4 chunks.  The summary pass walks each segment with plain
+    // loads, latency-bound, so with more blocks the split costs more than it
+    // gains (measured: 64 blocks, 1.94 -> 1.67 ms; 160 blocks, 4.4 -> 7.3 ms).
+    int64_t nseg = 1;
+    {
+        const int64_t blocks = batch * ntile * nslice, slots = 3 * 148;
+        const int64_t forced = g_force_bwd_segments.load();
+        if (forced > 0) nseg = forced;
+        else if (2 * blocks <= 148) nseg = slots / blocks;
+        nseg = std::min<int64_t>(nseg, std::min<int64_t>(kMaxSegments,
+                                                         forced > 0 ? nchunks : nchunks / 4));
+        nseg = std::max<int64_t>(nseg, 1);
+    }
+    const int64_t seg_chunks = (nchunks + nseg - 1) / nseg;
+    nseg = (nchunks + seg_chunks - 1) / seg_chunks;
     const size_t n_ck = size_t(batch * nchunks) * size_t(n_dn);
     const size_t n_p = size_t(ntile) * size_t(n_bln);
     const size_t n_pt = nslice > 1 ? size_t(nslice) * 3 * size_t(n_bld) : 0;
     // dD / ddelta_bias partials: one per batch row, or per (row, run of
     // kBwdRun steps) when slices are summed by the second kernel
+    // per batch row and segment in one pass, per (row, run) with slices
     const int64_t nrun = nslice > 1 ? (L + kBwdRun - 1) / kBwdRun : 1;
-    const size_t n_rd = size_t(batch * nrun) * size_t(dim);
-    const size_t n_total = n_ck + 2 * n_p + size_t(n_bdn) + 2 * n_rd + n_pt;
+    const int64_t nrd = nslice > 1 ? batch * nrun : nseg * batch;
+    const size_t n_rd = size_t(nrd) * size_t(dim);
+    const size_t n_seg = nseg > 1 ? size_t(nseg) * (2 * size_t(n_bdn) + size_t(batch * dim)) : 0;
+    const size_t n_total = n_ck + 2 * n_p + size_t(nseg) * size_t(n_bdn) + 2 * n_rd + n_pt + n_seg;
     void* scratch = nullptr;
     if (cudaMallocAsync(&scratch, n_total * 4, stream) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -2853,9 +2993,15 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     q.pB = f + n_ck;
     q.pC = q.pB + n_p;
     q.pA = q.pC + n_p;
-    q.pD = q.pA + n_bdn;
+    q.pD = q.pA + size_t(nseg) * size_t(n_bdn);
     q.pbias = q.pD + n_rd;
     q.pt = nslice > 1 ? q.pbias + n_rd : nullptr;
+    float* const segs = q.pbias + n_rd + n_pt;
+    q.hseg = nseg > 1 ? segs : nullptr;
+    q.lseg = nseg > 1 ? segs + size_t(nseg) * size_t(n_bdn) : nullptr;
+    q.sseg = nseg > 1 ? segs + 2 * size_t(nseg) * size_t(n_bdn) : nullptr;
+    q.nseg = nseg;
+    q.seg_chunks = seg_chunks;
     q.batch = batch; q.L = L; q.dim = dim; q.N = N; q.ntile = ntile; q.nchunks = nchunks;
     q.nslice = nslice;
     q.h0 = h0;
@@ -2869,7 +3015,19 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     const int ws = N <= 4 ? 1 : (N <= 8 ? 2 : 4);
     const size_t smem = size_t(ws == 1 ? BwdSmem<1>::total
                                        : (ws == 2 ? BwdSmem<2>::total : BwdSmem<4>::total)) * 4;
-    const dim3 grid = dim3(unsigned(batch * ntile), unsigned(nslice)), block = dim3(unsigned(32 * ws));
+    const dim3 grid = dim3(unsigned(batch * ntile), unsigned(nslice), unsigned(nseg)),
+               block = dim3(unsigned(32 * ws));
+    if (nseg > 1) {  // the segments' summaries first, on the same stream
+        switch (ws) {
+            case 1: ssm_bwd_summary_kernel<T, 1><<<grid, block, 0, stream>>>(q); break;
+            case 2: ssm_bwd_summary_kernel<T, 2><<<grid, block, 0, stream>>>(q); break;
+            default: ssm_bwd_summary_kernel<T, 4><<<grid, block, 0, stream>>>(q); break;
+        }
+        if (cudaGetLastError() != cudaSuccess) {
+            (void)cudaFreeAsync(scratch, stream);
+            return SSM_ERR_LAUNCH;
+        }
+    }
     auto launch = [&](auto kern) {
         // dynamic shared memory above 48 KB needs the opt-in (per device)
         static std::atomic<size_t> configured[64];
@@ -2911,9 +3069,9 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     };
     fold(q.pB, dB, ntile, n_bln);
     fold(q.pC, dC, ntile, n_bln);
-    fold(q.pA, dA, batch, n_dn);
-    fold(q.pD, D ? dD : static_cast<float*>(nullptr), batch * nrun, dim);
-    fold(q.pbias, delta_bias ? ddelta_bias : static_cast<float*>(nullptr), batch * nrun, dim);
+    fold(q.pA, dA, nseg * batch, n_dn);
+    fold(q.pD, D ? dD : static_cast<float*>(nullptr), nrd, dim);
+    fold(q.pbias, delta_bias ? ddelta_bias : static_cast<float*>(nullptr), nrd, dim);
     if (cudaFreeAsync(scratch, stream) != cudaSuccess && st == SSM_OK) st = SSM_ERR_LAUNCH;
     return st;
 }
@@ -3214,6 +3372,10 @@ int ssm_set_knob(int key, int64_t value) {
         case SSM_KNOB_KERNEL:
             if (value < 0 || value > 2) return SSM_ERR_ARG;
             g_force_kernel.store(int(value));
+            return SSM_OK;
+        case SSM_KNOB_BWD_SEGMENTS:
+            if (value < 0 || value > kMaxSegments) return SSM_ERR_ARG;
+            g_force_bwd_segments.store(int(value));
             return SSM_OK;
         default:
             return SSM_ERR_ARG;

@@ -44,6 +44,7 @@ SSM_KNOB_PLAIN_LOADS = 5
 SSM_KNOB_STAGES = 6
 SSM_KNOB_SEGMENTS = 7
 SSM_KNOB_KERNEL = 8
+SSM_KNOB_BWD_SEGMENTS = 9
 
 EXPORTED = ("ssm_scan_fwd", "ssm_scan_fwd_bf16", "ssm_scan_fwd_bf16_noalloc",
             "ssm_scan_fwd_h0", "ssm_scan_fwd_bf16_h0", "ssm_scan_fwd_zoh", "ssm_scan_fwd_bf16_zoh",

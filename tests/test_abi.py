@@ -98,6 +98,8 @@ def test_knobs_validate():
     assert ssm.ssm_set_knob(K.SSM_KNOB_SEGMENTS, -1) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(K.SSM_KNOB_SEGMENTS, 65) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(K.SSM_KNOB_KERNEL, 3) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(K.SSM_KNOB_BWD_SEGMENTS, 65) == K.SSM_ERR_ARG
+    assert ssm.ssm_set_knob(K.SSM_KNOB_BWD_SEGMENTS, 0) == K.SSM_OK
     assert ssm.ssm_set_knob(99, 0) == K.SSM_ERR_ARG
     assert ssm.ssm_set_knob(K.SSM_KNOB_STATE_GROUPS, 0) == K.SSM_OK
     assert ssm.ssm_set_knob(K.SSM_KNOB_WAIT_NS, 2_000_000_000) == K.SSM_OK

@@ -257,3 +257,51 @@ def test_backward_of_an_empty_piece_passes_dh_last_through():
     g = _gpu_state_grads(inp, dy, h0, dh)
     assert np.array_equal(g["dh0"], dh)
     assert all(not np.any(v) for k, v in g.items() if k != "dh0")
+
+
+
+# ---------------------------------------------------------------- time segments
+@pytest.fixture
+def bwd_segments():
+    """Force the backward's time-segment count for one test, then restore."""
+    from selective_state_space_150_b300 import ssmscan as K
+
+    def force(n):
+        assert ssm.ssm_set_knob(K.SSM_KNOB_BWD_SEGMENTS, n) == K.SSM_OK
+    yield force
+    force(0)
+
+
+@pytest.mark.parametrize("segs", [2, 3, 7])
+@pytest.mark.parametrize("shape", [(2, 200, 72, 16), (1, 203, 33, 5), (1, 150, 40, 40)])
+def test_segmented_backward_matches_oracle(bwd_segments, shape, segs):
+    bwd_segments(segs)
+    inp, dy = problem(shape, seed=sum(shape) + segs, **FLAGS[0])
+    check(inp, dy)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_segmented_backward_with_states_matches_oracle(bwd_segments, dtype):
+    bwd_segments(4)
+    inp, h0, dh, dy = _state_problem((2, 130, 40, 16), 77, dtype, **FLAGS[0])
+    g = _gpu_state_grads(inp, dy, h0, dh)
+    x = W.decoded(inp)
+    r = oracle_bwd(x["u"], x["delta"], x["A"], x["B"], x["C"], x["D"], x["z"], x["delta_bias"],
+                   x["softplus"], W.decode(dy), h0=h0, dh_last=dh)
+    names = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "z": "dz", "delta_bias": "ddelta_bias", "h0": "dh0"}
+    for k, v in r.items():
+        bf = dtype == "bf16" and k in ("u", "delta", "B", "C", "z")
+        err = rel_err(g[names[k]], v)
+        assert err <= (BF16_TOL if bf else TOL), (names[k], err)
+
+
+def test_segmented_backward_is_deterministic_and_close_to_one_segment(bwd_segments):
+    inp, dy = problem((1, 320, 64, 16), seed=9, **FLAGS[0])
+    bwd_segments(1)
+    g1 = gpu_grads(inp, dy)
+    bwd_segments(5)
+    g5, g5b = gpu_grads(inp, dy), gpu_grads(inp, dy)
+    for k in g1:
+        assert np.array_equal(g5[k], g5b[k]), k
+        assert rel_err(g5[k], g1[k]) <= 5e-5, k
