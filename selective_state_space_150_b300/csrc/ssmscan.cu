@@ -1645,7 +1645,10 @@ struct BwdSmem {
     static constexpr int total = Cs + T * NP;
 };
 
-template <typename T, int WS>
+// SUM: the time-segment summary instead of the gradients: the segment's end
+// state from a zero start and its sum of dt, and its adjoint carry at the
+// start from a zero terminal gradient, with the same staging and arithmetic.
+template <typename T, int WS, bool SUM = false>
 __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) {
     using E = Elt<T>;
     constexpr int NPT = kBwdNPT, NT = WS * 32;
@@ -1759,8 +1762,10 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
         }
     };
     // one forward step of this warp's states from the staged chunk
+    double sdt_seg = 0.0;  // SUM: the segment's sum of dt
     auto step = [&](int i, float (&h)[NPT]) {
         const float dt = s_dt[i * 32 + lane];
+        if constexpr (SUM) sdt_seg += double(dt);
         const float du_ = dt * s_x[i * 32 + lane];
         const float* const bb = s_B + i * NP + sg * NPT;
 #pragma unroll
@@ -1781,8 +1786,8 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
     float h[NPT];
 #pragma unroll
     for (int j = 0; j < NPT; ++j)
-        h[j] = (q.h0 != nullptr && ok && n0 + j < N) ? q.h0[hrow + n0 + j] : 0.f;
-    if (ok) {
+        h[j] = (!SUM && q.h0 != nullptr && ok && n0 + j < N) ? q.h0[hrow + n0 + j] : 0.f;
+    if (!SUM && ok) {
         for (int64_t r = 0; r < zseg; ++r) {
             const float sdt = q.sseg[srow(r)];
 #pragma unroll
@@ -1795,7 +1800,7 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
     if (c_end > c_begin) fetch(c_begin, false, f);
     for (int64_t c = c_begin; c < c_end; ++c) {
         const int tv = chunk_len(c);
-        if (ok) {
+        if (!SUM && ok) {
 #pragma unroll
             for (int j = 0; j < NPT; ++j)
                 if (n0 + j < N) q.ckpt[ck(c, j)] = h[j];
@@ -1815,6 +1820,45 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
             for (int i = 0; i < tv; ++i) step(i, h);
         }
         __syncthreads();
+    }
+
+    if constexpr (SUM) {
+        // the segment's end state and sum of dt; then, but for the first
+        // segment, its adjoint carry at the start from a zero terminal
+        // gradient (only the carry recursion, on the staged chunks)
+        if (ok && zseg < q.nseg - 1) {
+#pragma unroll
+            for (int j = 0; j < NPT; ++j)
+                if (n0 + j < N) q.hseg[srow(zseg) * N + n0 + j] = h[j];
+        }
+        if (ok && sg == 0 && blockIdx.y == 0) q.sseg[srow(zseg)] = float(sdt_seg);
+        if (zseg == 0) return;  // uniform over the block
+        float cs[NPT];
+#pragma unroll
+        for (int j = 0; j < NPT; ++j) cs[j] = 0.f;
+        for (int64_t c = c_end - 1; c >= c_begin; --c) {
+            const int tv = chunk_len(c);
+            stage(f, tv, true);
+            __syncthreads();
+            if (c > c_begin) fetch(c - 1, true, f);
+            for (int i = tv - 1; i >= 0; --i) {
+                const float dt = s_dt[i * 32 + lane];
+                const float dyc = s_dyc[i * 32 + lane];
+                const float* const cc = s_C + i * NP + sg * NPT;
+#pragma unroll
+                for (int j = 0; j < NPT; ++j) {
+                    const float lam = fmaf(dyc, cc[j], cs[j]);
+                    cs[j] = ex2_approx(dt * a2[j]) * lam;
+                }
+            }
+            __syncthreads();
+        }
+        if (ok) {
+#pragma unroll
+            for (int j = 0; j < NPT; ++j)
+                if (n0 + j < N) q.lseg[srow(zseg) * N + n0 + j] = cs[j];
+        }
+        return;
     }
 
     // ---- reverse
@@ -2049,89 +2093,6 @@ __global__ void __launch_bounds__(256) ssm_bwd_slices_kernel(const BwdParams q) 
     }
     q.pD[r * q.dim + d] = gD;
     q.pbias[r * q.dim + d] = gbias;
-}
-
-// Time segments of the backward, per (batch row, channel tile, slice,
-// segment z): the segment's end state from a zero start and its sum of dt
-// (all but the last segment), and the adjoint carry at its start from a zero
-// terminal gradient (all but the first segment), which the main kernel
-// composes into each segment's start state and terminal carry.  The same
-// expressions as the main kernel's steps; lane = channel, kBwdNPT states per
-// warp; no block barrier.
-template <typename T, int WS>
-__global__ void __launch_bounds__(WS * 32) ssm_bwd_summary_kernel(const BwdParams q) {
-    using E = Elt<T>;
-    constexpr int NPT = kBwdNPT;
-    const int lane = threadIdx.x & 31, sg = threadIdx.x >> 5;
-    const int64_t tile = blockIdx.x % q.ntile, b = blockIdx.x / q.ntile;
-    const int64_t d = tile * 32 + lane;
-    if (d >= q.dim) return;
-    const int64_t N = q.N, L = q.L, dim = q.dim, z = blockIdx.z;
-    const int64_t n0 = int64_t(blockIdx.y) * kBwdSlice + int64_t(sg) * NPT;
-    const int64_t t_b = z * q.seg_chunks * kBwdTC;
-    const int64_t t_e = t_b + q.seg_chunks * kBwdTC < L ? t_b + q.seg_chunks * kBwdTC : L;
-    const T* const g_u = static_cast<const T*>(q.u);
-    const T* const g_delta = static_cast<const T*>(q.delta);
-    const T* const g_B = static_cast<const T*>(q.B);
-    const T* const g_C = static_cast<const T*>(q.C);
-    const T* const g_z = static_cast<const T*>(q.z);
-    const T* const g_dy = static_cast<const T*>(q.dy);
-    float a2[NPT];
-#pragma unroll
-    for (int j = 0; j < NPT; ++j) a2[j] = n0 + j < N ? q.A[d * N + n0 + j] * kLog2e : 0.f;
-    const float bias = q.bias != nullptr ? q.bias[d] : 0.f;
-    const int64_t row = (z * q.batch + b) * dim + d;
-    auto dt_at = [&](int64_t o) {
-        const float r = E::to_f(g_delta[o]) + bias;
-        return q.softplus ? Act<float>::softplus(r) : r;
-    };
-    double sdt = 0.0;
-    if (z < q.nseg - 1) {
-        float h[NPT];
-#pragma unroll
-        for (int j = 0; j < NPT; ++j) h[j] = 0.f;
-        // unrolled so that several steps' loads are in flight at once
-#pragma unroll 8
-        for (int64_t t = t_b; t < t_e; ++t) {
-            const int64_t o = (b * L + t) * dim + d;
-            const float dt = dt_at(o);
-            const float du_ = dt * E::to_f(g_u[o]);
-#pragma unroll
-            for (int j = 0; j < NPT; ++j) {
-                const float bb = n0 + j < N ? E::to_f(g_B[(b * L + t) * N + n0 + j]) : 0.f;
-                h[j] = fmaf(ex2_approx(dt * a2[j]), h[j], du_ * bb);
-            }
-            sdt += double(dt);
-        }
-#pragma unroll
-        for (int j = 0; j < NPT; ++j)
-            if (n0 + j < N) q.hseg[row * N + n0 + j] = h[j];
-    }
-    if (z > 0) {
-        const bool count = !(z < q.nseg - 1);  // the last segment sums dt here
-        float carry[NPT];
-#pragma unroll
-        for (int j = 0; j < NPT; ++j) carry[j] = 0.f;
-#pragma unroll 8
-        for (int64_t t = t_e - 1; t >= t_b; --t) {
-            const int64_t o = (b * L + t) * dim + d;
-            const float dt = dt_at(o);
-            const float zv = q.z != nullptr ? E::to_f(g_z[o]) : 0.f;
-            const float g = q.z != nullptr ? zv / (1.f + expf(-zv)) : 1.f;
-            const float dyc = E::to_f(g_dy[o]) * g;
-#pragma unroll
-            for (int j = 0; j < NPT; ++j) {
-                const float cc = n0 + j < N ? E::to_f(g_C[(b * L + t) * N + n0 + j]) : 0.f;
-                const float lam = fmaf(dyc, cc, carry[j]);
-                carry[j] = ex2_approx(dt * a2[j]) * lam;
-            }
-            if (count) sdt += double(dt);
-        }
-#pragma unroll
-        for (int j = 0; j < NPT; ++j)
-            if (n0 + j < N) q.lseg[row * N + n0 + j] = carry[j];
-    }
-    if (sg == 0 && blockIdx.y == 0) q.sseg[row] = float(sdt);
 }
 
 // ------------------------------------------------------------------ host side
@@ -2952,17 +2913,15 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
         return SSM_OK;
     }
     const int64_t nslice = (N + kBwdSlice - 1) / kBwdSlice;
-    // Time segments when the (row, tile, slice) blocks leave more than half of
-    // the SMs idle: as many as still fit one wave of three blocks per SM, each
-    // at least 4 chunks.  The summary pass walks each segment with plain
-    // loads, latency-bound, so with more blocks the split costs more than it
-    // gains (measured: 64 blocks, 1.94 -> 1.67 ms; 160 blocks, 4.4 -> 7.3 ms).
+    // Time segments when the (row, tile, slice) blocks fill less than half of
+    // one wave of three blocks per SM: as many as still fit that wave (a
+    // second wave costs more than the split gains), each at least 4 chunks.
     int64_t nseg = 1;
     {
         const int64_t blocks = batch * ntile * nslice, slots = 3 * 148;
         const int64_t forced = g_force_bwd_segments.load();
         if (forced > 0) nseg = forced;
-        else if (2 * blocks <= 148) nseg = slots / blocks;
+        else if (2 * blocks <= slots) nseg = slots / blocks;
         nseg = std::min<int64_t>(nseg, std::min<int64_t>(kMaxSegments,
                                                          forced > 0 ? nchunks : nchunks / 4));
         nseg = std::max<int64_t>(nseg, 1);
@@ -3017,36 +2976,29 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
                                        : (ws == 2 ? BwdSmem<2>::total : BwdSmem<4>::total)) * 4;
     const dim3 grid = dim3(unsigned(batch * ntile), unsigned(nslice), unsigned(nseg)),
                block = dim3(unsigned(32 * ws));
-    if (nseg > 1) {  // the segments' summaries first, on the same stream
-        switch (ws) {
-            case 1: ssm_bwd_summary_kernel<T, 1><<<grid, block, 0, stream>>>(q); break;
-            case 2: ssm_bwd_summary_kernel<T, 2><<<grid, block, 0, stream>>>(q); break;
-            default: ssm_bwd_summary_kernel<T, 4><<<grid, block, 0, stream>>>(q); break;
-        }
-        if (cudaGetLastError() != cudaSuccess) {
-            (void)cudaFreeAsync(scratch, stream);
-            return SSM_ERR_LAUNCH;
-        }
-    }
     auto launch = [&](auto kern) {
-        // dynamic shared memory above 48 KB needs the opt-in (per device)
-        static std::atomic<size_t> configured[64];
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return false;
-        if (configured[dev & 63].load() < smem) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     int(smem)) != cudaSuccess)
-                return false;
-            configured[dev & 63].store(smem);
-        }
+        // dynamic shared memory above 48 KB needs the opt-in, per kernel
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+                cudaSuccess)
+            return false;
         kern<<<grid, block, smem, stream>>>(q);
         return true;
     };
-    bool launched;
-    switch (ws) {
-        case 1: launched = launch(ssm_bwd_kernel<T, 1>); break;
-        case 2: launched = launch(ssm_bwd_kernel<T, 2>); break;
-        default: launched = launch(ssm_bwd_kernel<T, 4>); break;
+    bool launched = true;
+    if (nseg > 1) {  // the segments' summaries first, on the same stream
+        switch (ws) {
+            case 1: launched = launch(ssm_bwd_kernel<T, 1, true>); break;
+            case 2: launched = launch(ssm_bwd_kernel<T, 2, true>); break;
+            default: launched = launch(ssm_bwd_kernel<T, 4, true>); break;
+        }
+    }
+    if (launched) {
+        switch (ws) {
+            case 1: launched = launch(ssm_bwd_kernel<T, 1>); break;
+            case 2: launched = launch(ssm_bwd_kernel<T, 2>); break;
+            default: launched = launch(ssm_bwd_kernel<T, 4>); break;
+        }
     }
     if (!launched) {
         (void)cudaGetLastError();
