@@ -244,6 +244,13 @@ def oracle_rate(wl: W.Workload, inp, budget_s: float, threads: int, seed: int = 
     return tokens_equiv / wall, desc, wall
 
 
+def l2_note_for(wl: W.Workload) -> str:
+    """How the timed steps keep their working set out of the L2 cache: the GPU
+    arm alternates two resident copies of the inputs and outputs."""
+    return (f"inputs and outputs rotate over 2 resident copies "
+            f"({2 * algorithmic_bytes(wl) / 1e6:.0f} MB > 126 MB L2); no flush")
+
+
 def config_of(wl: W.Workload, l2_note: str):
     return {"workload": wl.name, "batch": wl.batch, "L": wl.L, "dim": wl.dim, "N": wl.N,
             "io_dtype": wl.dtype, "state_dtype": "f32", "softplus": wl.softplus,
@@ -271,7 +278,8 @@ def run_reference(args, wl):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * wl.tokens / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(wl, "n/a (host)"),
+        # the same workload keys as the GPU arm's line
+        "config": config_of(wl, l2_note_for(wl)),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": desc + "; each step a fresh channel sample"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -325,9 +333,7 @@ def run_ours(args, wl, world, rank, local):
     plan = ssm.ssm_scan_plan(wl.batch, wl.L, wl.dim, wl.N, 1 if bf else 0)
     # a call runs one kernel, or two (segment summaries, then the main pass)
     launches_per_call = 2 if plan["segments"] > 1 else 1
-    working_set = 2 * (algorithmic_bytes(wl))
-    l2_note = (f"inputs and outputs rotate over 2 resident copies "
-               f"({working_set / 1e6:.0f} MB > 126 MB L2); no flush")
+    l2_note = l2_note_for(wl)
 
     for i in range(args.warmup):
         launch(i)
@@ -429,6 +435,17 @@ def run_ours(args, wl, world, rank, local):
     st = ssm.ssm_scan_last_device_status(sptr)
     if st != 0:
         raise RuntimeError("device status: " + ssm.ssm_status_string(st))
+    del ws
+    link = link_peaks(dev, stream)
+    t_h2d = h2d / (link["h2d_gbs"] * 1e9)
+    t_d2h = d2h / (link["d2h_gbs"] * 1e9)
+    step_ms = e2e_ms / Ke
+    link.update({
+        # the host-buffer call overlaps uploads, downloads and compute, so the
+        # link bound of a step is the slower direction (a full-duplex link);
+        # the serial bound adds both directions
+        "bound_ms": max(t_h2d, t_d2h) * 1e3, "serial_bound_ms": (t_h2d + t_d2h) * 1e3,
+        "e2e_ms_per_step": step_ms, "frac": max(t_h2d, t_d2h) * 1e3 / step_ms})
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -441,7 +458,7 @@ def run_ours(args, wl, world, rank, local):
         "roofline": roof,
         "pipe_peaks": peaks,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": Ke,
+                "d2h_bytes_per_step": d2h, "steps": Ke, "link": link,
                 "path": f"{fn_host.__name__} (C ABI on pinned host buffers: uploads, scan "
                         "and downloads overlapped across parts of the batch)"},
         "gpu_launches": K * launches_per_call,
@@ -455,6 +472,28 @@ def run_ours(args, wl, world, rank, local):
         line["cpu_baseline"] = {"value": r, "unit": "tokens/s", "cores": threads,
                                 "kind": "oracle", "sample": desc}
     return line
+
+
+def link_peaks(dev, stream, nbytes: int = 256 << 20, reps: int = 5):
+    """The host link's copy rate in each direction, measured alone: one large
+    cudaMemcpyAsync between pinned host memory and the device, timed with
+    CUDA events after one untimed copy."""
+    import torch
+    hbuf = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {"bytes_per_copy": nbytes, "copies": reps,
+           "how": "pinned host <-> device, one cudaMemcpyAsync per copy, CUDA events"}
+    for name, dst, src in (("h2d_gbs", dbuf, hbuf), ("d2h_gbs", hbuf, dbuf)):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        out[name] = nbytes * reps / (a.elapsed_time(b) * 1e-3) / 1e9
+    return out
 
 
 def pipe_peaks(stream_ptr):

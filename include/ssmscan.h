@@ -34,8 +34,10 @@
  *   h_last         : (batch, dim, N)  fp32
  * "dim" is the channel count the pages call D (renamed so it does not clash
  * with the skip vector D).  Every pointer is a DEVICE pointer owned by the
- * caller; the library never allocates, frees or keeps a pointer past the
- * call.  Work is enqueued on `stream` and the call returns without
+ * caller; the library never allocates, frees or keeps a caller's pointer
+ * past the call (the only device address it keeps is that of its own static
+ * buffer, see ssm_scan_fwd_bf16_noalloc).  Work is enqueued on `stream` and
+ * the call returns without
  * synchronising.  The one exception to "never allocates": when the batch
  * rows and channels alone leave most of the GPU idle (few channels, a long
  * sequence), the sequence is cut into time segments (see below) and the call
@@ -102,8 +104,9 @@ typedef enum {
     SSM_ERR_ALIAS = 7,           /* y overlaps an input                        */
     SSM_ERR_ARG = 8,             /* an invalid debug key or value              */
     SSM_ERR_NOMEM = 9,           /* stream-ordered scratch allocation failed   */
-    SSM_ERR_SCRATCH = 10         /* the no-alloc entry point's static buffer   */
-                                 /* is too small for this problem              */
+    SSM_ERR_SCRATCH = 10         /* reserved: the no-alloc entry point's       */
+                                 /* static buffer too small (no longer         */
+                                 /* returned; it plans fewer segments)         */
 } ssm_status;
 
 /* Largest state size N the kernels are built for. */
@@ -352,18 +355,22 @@ SSM_API int ssm_scan_bwd_bf16_h0(const uint16_t *u, const uint16_t *delta, const
  * must not enter an allocator (growing a pool maps new pages); and devices
  * where the stream-ordered allocator is unavailable.
  *
- * Limit: a problem the plan runs in one pass (ssm_scan_plan: segments = 1)
- * needs no scratch and is accepted at any size.  A segmented problem needs
- * (segments - 1) * batch * dim * (N + 1) words; above
- * SSM_NOALLOC_SCRATCH_FLOATS the call returns SSM_ERR_SCRATCH and launches
- * nothing.  The summary pass writes every word the main pass reads, so
- * nothing in the buffer has to start at zero and the call clears nothing.
+ * Limit: a segmented plan needs (segments - 1) * batch * dim * (N + 1) words
+ * of summaries.  This entry point takes at most 1 + SSM_NOALLOC_SCRATCH_FLOATS
+ * / (batch * dim * (N + 1)) segments, so the summaries always fit: where the
+ * allocating entry point would cut the sequence into more segments, this one
+ * uses fewer (a plain one-pass call at the extreme), which changes only the
+ * speed and the fp32 rounding order, not the definition.  It never returns
+ * SSM_ERR_SCRATCH.  The summary pass writes every word the main pass reads,
+ * so nothing in the buffer has to start at zero and the call clears nothing.
  *
  * The buffer is shared by every call on a device: two calls in flight at the
  * same time (other streams, other host threads) race on it and give wrong
  * results.  Calls in one stream are ordered and safe.  The first call on a
- * device looks up the buffer's address (cudaGetSymbolAddress, with that device
- * current) and keeps it; make that first call before any stream capture.
+ * device (and the first in a new context after a device reset) looks up the
+ * buffer's address (cudaGetSymbolAddress, with that device current) and keeps
+ * it with the context it belongs to; make that first call before any stream
+ * capture.
  */
 #define SSM_NOALLOC_SCRATCH_FLOATS 2097152
 SSM_API int ssm_scan_fwd_bf16_noalloc(const uint16_t *u, const uint16_t *delta,

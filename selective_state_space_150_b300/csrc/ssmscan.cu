@@ -1574,6 +1574,8 @@ struct BwdParams {
 // The per-(step, channel) gradients from the sums over all states of the
 // readout yc (without the skip term), the dt term gdt and the u term gu.
 // Returns the gated output gradient dyc; du, ddelta, dz through references.
+// The activations are the accurate fp32 forms for either input type, so the
+// bf16 entry's gradients are the fp32 entry's, rounded.
 __device__ __forceinline__ float grad_point(float yc, float gdt, float gu, float raw, float x,
                                             float dyo, float zz, bool has_z, int softplus,
                                             float Dd, float& du, float& ddelta, float& dz) {
@@ -1631,7 +1633,7 @@ template <int WS>
 struct BwdSmem {
     static constexpr int NP = WS * kBwdNPT, T = kBwdTC;
     // floats, in this order
-    static constexpr int hs = 0;                          // [WS][T][4][32] states after each step
+    static constexpr int hs = 0;                          // [WS][T][32][4] states after each step
     static constexpr int part = hs + WS * T * 4 * 32;     // [WS][T][3][32] per-warp shares
     static constexpr int red = part + WS * T * 3 * 32;    // [WS][2][32]
     static constexpr int raw = red + WS * 2 * 32;         // [T][32] delta + bias
@@ -1763,13 +1765,22 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
     };
     // one forward step of this warp's states from the staged chunk
     double sdt_seg = 0.0;  // SUM: the segment's sum of dt
+    static_assert(NPT % 2 == 0, "state pairs");
     auto step = [&](int i, float (&h)[NPT]) {
         const float dt = s_dt[i * 32 + lane];
         if constexpr (SUM) sdt_seg += double(dt);
         const float du_ = dt * s_x[i * 32 + lane];
         const float* const bb = s_B + i * NP + sg * NPT;
+        const float2 dt2 = make_float2(dt, dt), du2 = make_float2(du_, du_);
 #pragma unroll
-        for (int j = 0; j < NPT; ++j) h[j] = fmaf(ex2_approx(dt * a2[j]), h[j], du_ * bb[j]);
+        for (int j = 0; j < NPT; j += 2) {
+            const float2 xx = __fmul2_rn(dt2, make_float2(a2[j], a2[j + 1]));
+            const float2 e = make_float2(ex2_approx(xx.x), ex2_approx(xx.y));
+            const float2 w = __fmul2_rn(du2, make_float2(bb[j], bb[j + 1]));
+            const float2 hh = __ffma2_rn(e, make_float2(h[j], h[j + 1]), w);
+            h[j] = hh.x;
+            h[j + 1] = hh.y;
+        }
     };
 
     // ---- this block's time segment: chunks c_begin .. c_end - 1
@@ -1845,10 +1856,15 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
                 const float dt = s_dt[i * 32 + lane];
                 const float dyc = s_dyc[i * 32 + lane];
                 const float* const cc = s_C + i * NP + sg * NPT;
+                const float2 dt2 = make_float2(dt, dt), dyc2 = make_float2(dyc, dyc);
 #pragma unroll
-                for (int j = 0; j < NPT; ++j) {
-                    const float lam = fmaf(dyc, cc[j], cs[j]);
-                    cs[j] = ex2_approx(dt * a2[j]) * lam;
+                for (int j = 0; j < NPT; j += 2) {
+                    const float2 lam =
+                        __ffma2_rn(dyc2, make_float2(cc[j], cc[j + 1]), make_float2(cs[j], cs[j + 1]));
+                    const float2 xx = __fmul2_rn(dt2, make_float2(a2[j], a2[j + 1]));
+                    const float2 c2 = __fmul2_rn(make_float2(ex2_approx(xx.x), ex2_approx(xx.y)), lam);
+                    cs[j] = c2.x;
+                    cs[j + 1] = c2.y;
                 }
             }
             __syncthreads();
@@ -1901,54 +1917,81 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
         // carry links consecutive steps; the shuffle reductions of dB and dC
         // hang off it, so with the chunk unrolled several steps' reductions
         // are in flight at once.
+        // Per state, with lam = dyc C + carry and eh = e h_prev (e the step's
+        // decay): dA += dt lam eh; the dt term sums A lam eh + x lam B and the u
+        // term dt lam B, so both take sum_j lam B once; dB gets dt x lam and dC
+        // dyc h_cur (summed over the channels), and the carry to the step
+        // before is e lam.  State pairs use packed f32x2 arithmetic.
         auto rev_step = [&](int i, const float (&hc)[NPT], const float (&hp)[NPT]) {
             const float dt = s_dt[i * 32 + lane];
             const float x = s_x[i * 32 + lane];
             const float dyc = s_dyc[i * 32 + lane];
             const float* const bb = s_B + i * NP + sg * NPT;
             const float* const cc = s_C + i * NP + sg * NPT;
-            float vB[NPT], vC[NPT];
-            float yc = 0.f, gdt = 0.f, gu = 0.f;
+            const float2 dt2 = make_float2(dt, dt), dyc2 = make_float2(dyc, dyc);
+            const float2 dtx2 = make_float2(dt * x, dt * x);
+            float v[2 * NPT];  // dB shares (states 0..NPT-1), then dC shares
+            float2 yc2 = make_float2(0.f, 0.f), ga2 = make_float2(0.f, 0.f),
+                   lb2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < NPT; ++j) {
-                const float hcur = hc[j];
-                const float hprev = hp[j];
-                yc = fmaf(cc[j], hcur, yc);
-                const float lam = fmaf(dyc, cc[j], carry[j]);
-                const float e = ex2_approx(dt * a2[j]);
-                const float eh = e * hprev;
-                gdt = fmaf(lam, fmaf(aA[j], eh, bb[j] * x), gdt);
-                gA[j] = fmaf(lam * dt, eh, gA[j]);
-                gu = fmaf(lam * dt, bb[j], gu);
-                vB[j] = lam * dt * x;
-                vC[j] = dyc * hcur;
-                carry[j] = e * lam;
+            for (int j = 0; j < NPT; j += 2) {
+                const float2 c2 = make_float2(cc[j], cc[j + 1]);
+                const float2 b2 = make_float2(bb[j], bb[j + 1]);
+                const float2 hcur = make_float2(hc[j], hc[j + 1]);
+                const float2 hprev = make_float2(hp[j], hp[j + 1]);
+                yc2 = __ffma2_rn(c2, hcur, yc2);
+                const float2 lam = __ffma2_rn(dyc2, c2, make_float2(carry[j], carry[j + 1]));
+                const float2 xx = __fmul2_rn(dt2, make_float2(a2[j], a2[j + 1]));
+                const float2 e = make_float2(ex2_approx(xx.x), ex2_approx(xx.y));
+                const float2 pe = __fmul2_rn(lam, __fmul2_rn(e, hprev));  // lam e h_prev
+                const float2 gA2 = __ffma2_rn(dt2, pe, make_float2(gA[j], gA[j + 1]));
+                gA[j] = gA2.x;
+                gA[j + 1] = gA2.y;
+                ga2 = __ffma2_rn(make_float2(aA[j], aA[j + 1]), pe, ga2);
+                lb2 = __ffma2_rn(lam, b2, lb2);
+                const float2 vb = __fmul2_rn(lam, dtx2);
+                const float2 vc = __fmul2_rn(dyc2, hcur);
+                v[j] = vb.x;
+                v[j + 1] = vb.y;
+                v[NPT + j] = vc.x;
+                v[NPT + j + 1] = vc.y;
+                const float2 cr = __fmul2_rn(e, lam);
+                carry[j] = cr.x;
+                carry[j + 1] = cr.y;
             }
+            const float lamB = lb2.x + lb2.y;
             float* const pp = part + ((sg * kBwdTC + i) * 3) * 32 + lane;
-            pp[0] = yc;
-            pp[32] = gdt;
-            pp[64] = gu;
-            int nbB = 0, nbC = 0;
-            reduce_rounds<NPT, NPT, 16>(vB, lane, nbB);
-            reduce_rounds<NPT, NPT, 16>(vC, lane, nbC);
-            const int64_t n = n0 + nbB;  // nbC == nbB: the same lane pattern
-            if ((lane & (32 / NPT - 1)) == 0 && n < N) {
-                const int64_t o = ((tile * q.batch + b) * L + t0 + i) * N;
-                q.pB[o + n] = vB[0];
-                q.pC[o + n0 + nbC] = vC[0];
+            pp[0] = yc2.x + yc2.y;
+            pp[32] = fmaf(x, lamB, ga2.x + ga2.y);
+            pp[64] = dt * lamB;
+            // dB and dC together: afterwards lane l holds the channel sum of
+            // share nb, and lanes differing only in their low two bits agree
+            int nb = 0;
+            reduce_rounds<2 * NPT, 2 * NPT, 16>(v, lane, nb);
+            if ((lane & (32 / (2 * NPT) - 1)) == 0) {
+                const int64_t n = n0 + (nb % NPT);
+                if (n < N) {
+                    const int64_t o = ((tile * q.batch + b) * L + t0 + i) * N + n;
+                    (nb < NPT ? q.pB : q.pC)[o] = v[0];
+                }
             }
         };
+        static_assert(NPT == 4, "one 16-byte row of states per (step, lane)");
         auto fwd_keep = [&](int i) {
             step(i, h);
-#pragma unroll
-            for (int j = 0; j < NPT; ++j) myh[(i * NPT + j) * 32 + lane] = h[j];
+            *reinterpret_cast<float4*>(myh + (i * 32 + lane) * NPT) = make_float4(h[0], h[1], h[2], h[3]);
         };
         // the state after step i comes from the step before in registers;
         // only the state before it is read back
         auto rev_from = [&](int i, float (&hc)[NPT]) {
             float hp[NPT];
+            if (i > 0) {
+                const float4 v4 = *reinterpret_cast<const float4*>(myh + ((i - 1) * 32 + lane) * NPT);
+                hp[0] = v4.x; hp[1] = v4.y; hp[2] = v4.z; hp[3] = v4.w;
+            } else {
 #pragma unroll
-            for (int j = 0; j < NPT; ++j) hp[j] = i > 0 ? myh[((i - 1) * NPT + j) * 32 + lane] : hstart[j];
+                for (int j = 0; j < NPT; ++j) hp[j] = hstart[j];
+            }
             rev_step(i, hc, hp);
 #pragma unroll
             for (int j = 0; j < NPT; ++j) hc[j] = hp[j];
@@ -2106,6 +2149,20 @@ std::atomic<int> g_force_kernel{0};
 std::atomic<int> g_force_bwd_segments{0};
 std::atomic<int> g_plain_loads{0};
 
+PFN_cuCtxGetCurrent_v4000 get_ctx_current() {
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
+    });
+    return fn;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -2220,7 +2277,8 @@ constexpr size_t kWsSmemTarget = 72 * 1024;
 template <typename T>
 Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, const void* dt,
                const void* z, const void* y, const void* Bp, const void* Cp,
-               bool allow_tma = true, bool conv = false, bool need_ws = false) {
+               bool allow_tma = true, bool conv = false, bool need_ws = false,
+               int64_t max_seg = kMaxSegments) {
     const size_t es = sizeof(T);
     Plan pl;
     const int64_t channels = batch * dim;
@@ -2315,6 +2373,7 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
         ns = std::min<int64_t>(ns, nchunks / kMinSegChunks);
         const int fseg = g_force_segments.load();
         if (fseg > 0) ns = std::min<int64_t>(fseg, nchunks);
+        ns = std::min<int64_t>(ns, max_seg);
         if (ns < 2) ns = 1;
         pl.seg_chunks = ns > 1 ? (nchunks + ns - 1) / ns : nchunks;
         pl.n_seg = ns > 1 ? int((nchunks + pl.seg_chunks - 1) / pl.seg_chunks) : 1;
@@ -2444,29 +2503,43 @@ bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
     return a0 < b0 + uintptr_t(nb) && b0 < a0 + uintptr_t(na);
 }
 
-// Device address of g_static_scratch on the current device, looked up once
-// per device (with that device current) and kept.
+// Device address of g_static_scratch on the current device.  It is looked up
+// (with that device current) on the device's first call and kept together
+// with the context it was looked up in; a call from another context (after a
+// device reset the module is loaded again, possibly elsewhere) looks it up
+// again.
 int static_scratch(float** out) {
     static std::mutex mu;
     static float* addr[64] = {};
+    static CUcontext ctx_of[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SSM_ERR_LAUNCH;
+    // make the device's primary context current (a no-op once it is)
+    if (cudaFree(nullptr) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SSM_ERR_LAUNCH;
+    }
+    CUcontext ctx = nullptr;
+    auto cur = get_ctx_current();
+    if (cur == nullptr || cur(&ctx) != CUDA_SUCCESS || ctx == nullptr) return SSM_ERR_LAUNCH;
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+    if (addr[dev] == nullptr || ctx_of[dev] != ctx) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
             (void)cudaGetLastError();
             return SSM_ERR_LAUNCH;
         }
         addr[dev] = static_cast<float*>(ptr);
+        ctx_of[dev] = ctx;
     }
     *out = addr[dev];
     return SSM_OK;
 }
 
 // fixed_scratch: false = segment scratch from cudaMallocAsync on the stream;
-// true = from g_static_scratch (nothing allocated; a problem whose segment
-// summaries do not fit is refused with SSM_ERR_SCRATCH before any launch).
+// true = from g_static_scratch (nothing allocated; the plan takes no more time
+// segments than the buffer holds summaries for -- segments only speed the
+// call up, any count gives the same result up to rounding order).
 template <typename T>
 int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C, const float* D,
              const T* z, const float* delta_bias, int softplus_flag, T* y, float* h_last,
@@ -2512,7 +2585,12 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
 
     const bool conv = conv_k > 0;
     // The prologue and the ZOH variant run in the warp-specialised kernel only.
-    Plan pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C, true, conv, zoh);
+    // With the static buffer, at most 1 + (buffer words / words per segment)
+    // segments: segment summaries take batch * dim * (N + 1) words each.
+    const int64_t seg_cap =
+        fixed_scratch ? 1 + kStaticScratchFloats / std::max<int64_t>(1, n_bdn + batch * dim)
+                      : int64_t(kMaxSegments);
+    Plan pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C, true, conv, zoh, seg_cap);
     if (pl.grid * pl.n_seg > int64_t(0x7fffffff)) return SSM_ERR_SIZE;
     // That kernel needs rows TMA can describe; with L = 0 there is no step.
     if ((conv || zoh) && L > 0 && !pl.ws) return SSM_ERR_ALIGN;
@@ -2542,7 +2620,8 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
         if (!tma_udz) {
             if (conv || zoh) return SSM_ERR_ALIGN;
             // The tensor maps could not be encoded: plan again for plain loads.
-            pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C, /*allow_tma=*/false);
+            pl = make_plan<T>(batch, L, dim, N, u, delta, z, y, B, C, /*allow_tma=*/false, false,
+                              false, seg_cap);
             tma_bc = false;
         }
     }
@@ -2588,7 +2667,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     const int64_t nsum = int64_t(pl.n_seg - 1) * batch * dim;
     void* scratch = nullptr;
     if (fixed_scratch) {
-        if (nsum * (N + 1) > kStaticScratchFloats) return SSM_ERR_SCRATCH;
+        if (nsum * (N + 1) > kStaticScratchFloats) return SSM_ERR_SCRATCH;  // excluded by seg_cap
         float* fs = nullptr;
         const int st = static_scratch(&fs);
         if (st != SSM_OK) return st;
@@ -3263,7 +3342,8 @@ const char* ssm_status_string(int status) {
         case SSM_ERR_ARG: return "invalid knob key or value";
         case SSM_ERR_NOMEM: return "stream-ordered scratch allocation failed";
         case SSM_ERR_SCRATCH:
-            return "segment summaries exceed the 8 MiB static buffer of the no-alloc entry point";
+            return "segment summaries exceed the 8 MiB static buffer of the no-alloc entry point "
+                   "(not returned: that entry point plans no more segments than fit)";
         default: return "unknown status";
     }
 }

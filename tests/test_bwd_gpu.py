@@ -76,7 +76,7 @@ def test_backward_of_an_empty_sequence_is_zero():
 
 
 # ---------------------------------------------------------------- bf16
-BF16_TOL = 4e-3  # bf16 gradients: one round-to-nearest-even (2^-9 relative) on the fp32 result
+BF16_TOL = 4e-3  # bf16 gradients: one round-to-nearest-even on the fp32 result (unit roundoff 2^-8)
 
 
 def gpu_grads_bf16(inp, dy_bits):

@@ -102,14 +102,67 @@ def test_noalloc_takes_nothing_from_the_stream_ordered_pool():
     assert ssm.ssm_scan_last_device_status(stream) == ssmscan.SSM_OK
 
 
-def test_noalloc_refuses_problems_whose_summaries_do_not_fit():
-    """One row of 5120 channels, N = 96, 131072 steps: 8 segments whose
-    summaries need 13.9 MB, more than the 8 MiB buffer.  Refused on the host
-    (fake addresses: nothing is dereferenced or launched)."""
-    batch, L, dim, N = 1, 131072, 5120, 96
-    pl = ssm.ssm_scan_plan(batch, L, dim, N, 1)
-    assert pl["segments"] > 1 and pl["scratch_bytes"] > 4 * ssmscan.SSM_NOALLOC_SCRATCH_FLOATS
-    P, Y, H = 0x10000000, 1 << 40, 2 << 40
-    st = ssm.ssm_scan_fwd_bf16_noalloc(P, P, P, P, P, 0, 0, 0, 1, Y, H, batch, L, dim, N, 0)
-    assert st == ssmscan.SSM_ERR_SCRATCH
-    assert "static buffer" in ssm.ssm_status_string(st)
+def _segmented_pair(d, forced, stream):
+    """The no-alloc entry point and, with the same forced segment count, the
+    allocating one (which always honours the count)."""
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, forced)
+    try:
+        y, h = _call(ssm.ssm_scan_fwd_bf16_noalloc, d, BASE.softplus, stream)
+        r, g = _call(ssm.ssm_scan_fwd_bf16, d, BASE.softplus, stream)
+    finally:
+        ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, 0)
+    return y, h, r, g
+
+
+# batch 1, dim 4096, N 15: one segment's summaries take 4096 * 16 = 2^16 words,
+# so 33 segments fill the 2^21-word buffer exactly.  577 chunks of 16 steps
+# split into exactly 33 segments (of 18 chunks) when 33 are asked for, and into
+# exactly 34 (of 17) when 34 are.
+EDGE = (1, 577 * 16, 4096, 15)
+
+
+def _oracle_sampled(inp, y, h):
+    wl = BASE.with_shape(name="noalloc", batch=EDGE[0], L=EDGE[1], dim=EDGE[2], N=EDGE[3])
+    bs, ds = W.channel_sample(wl, n_dim=16, n_batch=1)
+    yr, hr = oracle_ref(W.gather(inp, bs, ds))
+    ys, hs = from_dev(y)[bs][:, :, ds], from_dev(h)[bs][:, ds, :]
+    assert rel_err(ys, yr) <= TOL["bf16"] and rel_err(hs, hr) <= TOL["bf16"]
+
+
+@pytest.mark.gpu
+def test_noalloc_at_the_exact_capacity_of_its_buffer():
+    """(segments - 1) * batch * dim * (N + 1) = 2^21 words: the no-alloc entry
+    point runs those 33 segments, bit for bit like the allocating one."""
+    batch, L, dim, N = EDGE
+    assert 32 * batch * dim * (N + 1) == ssmscan.SSM_NOALLOC_SCRATCH_FLOATS
+    stream = torch.cuda.current_stream().cuda_stream
+    inp, d = _inputs(EDGE, 34)
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, 33)
+    try:
+        assert ssm.ssm_scan_plan(*EDGE, 1)["segments"] == 33
+    finally:
+        ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, 0)
+    y, h, r, g = _segmented_pair(d, 33, stream)
+    assert ssm.ssm_scan_last_device_status(stream) == ssmscan.SSM_OK
+    assert np.array_equal(_bits(y), _bits(r)) and np.array_equal(_bits(h), _bits(g))
+    _oracle_sampled(inp, y, h)
+
+
+@pytest.mark.gpu
+def test_noalloc_one_segment_past_its_buffer_plans_fewer_segments():
+    """34 segments would need 2^21 + 2^16 words: the no-alloc entry point runs
+    the 33 that fit instead (it never refuses), so it equals the allocating
+    entry point forced to 33 segments, not the one forced to 34."""
+    stream = torch.cuda.current_stream().cuda_stream
+    inp, d = _inputs(EDGE, 35)
+    ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, 34)
+    try:
+        assert ssm.ssm_scan_plan(*EDGE, 1)["segments"] == 34
+    finally:
+        ssm.ssm_set_knob(ssmscan.SSM_KNOB_SEGMENTS, 0)
+    y, h, r34, g34 = _segmented_pair(d, 34, stream)
+    _, _, r33, g33 = _segmented_pair(d, 33, stream)
+    assert ssm.ssm_scan_last_device_status(stream) == ssmscan.SSM_OK
+    assert np.array_equal(_bits(y), _bits(r33)) and np.array_equal(_bits(h), _bits(g33))
+    assert not (np.array_equal(_bits(y), _bits(r34)) and np.array_equal(_bits(h), _bits(g34)))
+    _oracle_sampled(inp, y, h)
