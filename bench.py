@@ -556,6 +556,37 @@ def op_cpu_baseline(kind: str, wl: W.Workload, inp, rows: int = 1, n_dim: int = 
                       f"(N={wl.N}), fp64, one host thread; tokens scaled by {len(ds)}/{wl.dim}"}
 
 
+def compute_roofline(mufu_ops: int, fp32_ops: int, ms: float, peaks) -> dict:
+    """The compute roofline of a call: its MUFU and FP32 lane ops against the
+    pipe rates measured in the same run; the slower pipe binds, and the line
+    reports its fraction (the other pipe's beside it)."""
+    roof = {"bound": "alu", "unit": "Gop/s", "mufu_ops_per_launch": mufu_ops,
+            "fp32_ops_per_launch": fp32_ops}
+    if "ex2_per_s" not in peaks:
+        return roof
+    t_mufu = mufu_ops / peaks["ex2_per_s"]
+    t_fp32 = fp32_ops / peaks["fma_lane_ops_per_s"]
+    pipe = "mufu_ex2" if t_mufu >= t_fp32 else "fp32_fma"
+    ops, peak = ((mufu_ops, peaks["ex2_per_s"]) if pipe == "mufu_ex2"
+                 else (fp32_ops, peaks["fma_lane_ops_per_s"]))
+    roof.update({"pipe": pipe, "achieved": ops / (ms * 1e-3) / 1e9, "peak": peak / 1e9,
+                 "frac": ops / (ms * 1e-3) / peak,
+                 "mufu_frac": mufu_ops / (ms * 1e-3) / peaks["ex2_per_s"],
+                 "fp32_frac": fp32_ops / (ms * 1e-3) / peaks["fma_lane_ops_per_s"],
+                 "floor_ms": max(t_mufu, t_fp32) * 1e3,
+                 "peak_source": "measured on this GPU by libpipepeaks, same run"})
+    return roof
+
+
+def zoh_ops(wl: W.Workload):
+    """(MUFU ops, FP32 lane ops) of the exact zero-order-hold scan: the Euler
+    scan's, plus per (b, t, d, n) the factor (e - 1) / A applied to B u: a
+    subtraction and two multiplications (no further exponential: e is the
+    decay's)."""
+    mufu, fp32 = algorithmic_ops(wl)
+    return mufu, fp32 + 3 * wl.batch * wl.L * wl.dim * wl.N
+
+
 def mufu_roofline(mufu_ops: int, ms: float, peaks) -> dict:
     """The compute roofline of a call bound by the MUFU exponentials."""
     roof = {"bound": "alu", "pipe": "mufu_ex2", "unit": "Gop/s", "mufu_ops_per_launch": mufu_ops,
@@ -688,8 +719,8 @@ def run_op(args, wl):
             "value": wl.tokens / (ms_zoh * 1e-3), "unit": "tokens/s", "higher_is_better": True,
             "ms_per_step": ms_zoh, "steps": args.steps, "warmup": args.warmup,
             "euler_scan_ms": ms_scan, "zoh_cost_ms": ms_zoh - ms_scan,
-            "roofline": mufu_roofline(algorithmic_ops(wl)[0], ms_zoh,
-                                      pipe_peaks(stream.cuda_stream)),
+            "zoh_over_euler": ms_zoh / ms_scan,
+            "roofline": compute_roofline(*zoh_ops(wl), ms_zoh, pipe_peaks(stream.cuda_stream)),
             "cpu_baseline": None if args.no_cpu_baseline else op_cpu_baseline(
                 "zoh_scan", wl, inp, n_dim=256),
             "dtype": "f32", "data": "synthetic (seeded; see ssm_workloads.py)",

@@ -429,19 +429,23 @@ __device__ __forceinline__ float scan_step(float2 v, const float (&bb)[NPT], con
 // The same step with the exact zero-order-hold B (itwiki "상태 공간 모델",
 // section "이산화": Bbar = (dt A)^-1 (exp(dt A) - 1) dt B, per state
 // (e - 1) / A B with e = exp(dt A)).  v = (dt, u); ia = 1 / A (0 where A = 0).
-// For |dt A| < 1/16 the factor is dt (1 + x/2 + x^2/6 + x^3/24 + x^4/120),
-// x = dt A (the dropped terms are below 2e-9 relative), which also gives the
-// limit dt at A = 0; elsewhere (e - 1) / A loses at most ~3e-6 relative.
+// The factor (e - 1) / A = dt phi(x), phi(x) = (e^x - 1) / x, x = dt A.  For
+// |x| < 1/16 it is dt (1 + x/2 + x^2/6 + x^3/24): the series of phi to third
+// order (the first dropped term, x^4/120, is below 1.3e-7 relative), evaluated
+// in the base-2 exponent x2 = x log2(e) the decay already needs
+// (coefficients ln2/2, ln2^2/6, ln2^3/24); it also gives the limit dt at A = 0.
+// Elsewhere (e - 1) / A loses at most ~3e-6 relative (e's ex2 error over |x|).
+constexpr float kZ1 = 0.34657359027997264f;   // ln2 / 2
+constexpr float kZ2 = 0.08007550231970023f;   // ln2^2 / 6
+constexpr float kZ3 = 0.013876027166205394f;  // ln2^3 / 24
+constexpr float kZCut = 0.09016844005556021f; // 1 / (16 ln2): |x| < 1/16
 __device__ __forceinline__ float2 zoh_factor2(float2 vx, float2 x2, float2 e, float2 ia) {
-    const float2 xa = __fmul2_rn(x2, make_float2(kLn2, kLn2));  // dt A
-    float2 s = __ffma2_rn(xa, make_float2(1.f / 120.f, 1.f / 120.f),
-                          make_float2(1.f / 24.f, 1.f / 24.f));
-    s = __ffma2_rn(s, xa, make_float2(1.f / 6.f, 1.f / 6.f));
-    s = __ffma2_rn(s, xa, make_float2(0.5f, 0.5f));
-    s = __ffma2_rn(s, xa, make_float2(1.f, 1.f));
+    float2 s = __ffma2_rn(x2, make_float2(kZ3, kZ3), make_float2(kZ2, kZ2));
+    s = __ffma2_rn(s, x2, make_float2(kZ1, kZ1));
+    s = __ffma2_rn(s, x2, make_float2(1.f, 1.f));
     const float2 fs = __fmul2_rn(vx, s);
     const float2 fl = __fmul2_rn(__fadd2_rn(e, make_float2(-1.f, -1.f)), ia);
-    return make_float2(fabsf(xa.x) < 0.0625f ? fs.x : fl.x, fabsf(xa.y) < 0.0625f ? fs.y : fl.y);
+    return make_float2(fabsf(x2.x) < kZCut ? fs.x : fl.x, fabsf(x2.y) < kZCut ? fs.y : fl.y);
 }
 
 template <int NPT, bool WITH_C>
@@ -1166,6 +1170,14 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
         // channel pair pp, steps tq0 .. tq0 + ITEMS - 1 (consecutive, so the
         // prologue's convolution window slides by one row per step)
         const int pp = pt % NPAIR, tq0 = (pt / NPAIR) * ITEMS;
+        // byte offsets of this thread's items in a [TC][WB] tile, and (with the
+        // prologue) of its x rows, the same for every chunk
+        uint32_t off[ITEMS], offx[ITEMS + kConvHalo];
+#pragma unroll
+        for (int it = 0; it < ITEMS; ++it) off[it] = TT::off(tq0 + it, 2 * pp * ES, TC);
+#pragma unroll
+        for (int r = 0; r < ITEMS + kConvHalo; ++r)
+            offx[r] = conv ? TT::off_cbs(tq0 + r, 2 * pp * ES, cbsx) : 0u;
         float bias2[2];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -1190,6 +1202,7 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
         const T* gB = static_cast<const T*>(p.B);
         const T* gC = static_cast<const T*>(p.C);
         const bool bc_vec = p.tma_bc && N == NP && (N % 4) == 0;
+        const bool softplus = p.softplus != 0;
         int s = 0;
         uint32_t ph = 0;
         int bf = 0;        // buffer of chunk k: k % kBufs
@@ -1245,42 +1258,51 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
 #pragma unroll
                 for (int j = 0; j < kMaxConvK - 1; ++j) {
                     float xv[2];
-                    ld_k<T, 2>(ru + TT::off_cbs(tq0 + j, 2 * pp * ES, cbsx), xv);
+                    ld_k<T, 2>(ru + offx[j], xv);
                     xw[j + 1] = make_float2(xv[0], xv[1]);
                 }
             }
+            // The chunk's items; only the last chunk of the sequence (tail) has
+            // padded steps, whose dt = dt*u = 0 keep the state unchanged.
+            auto items = [&](auto tail) {
 #pragma unroll
-            for (int it = 0; it < ITEMS; ++it) {
-                const int t = tq0 + it;
-                const uint32_t o = TT::off(t, 2 * pp * ES, TC);
-                float xr[2], uu[2];
-                ld_k<T, 2>(rdt + o, xr);
-                if constexpr (conv) {
-                    // u = silu(causal conv) over the window ending at step t
-                    float xv[2];
-                    ld_k<T, 2>(ru + TT::off_cbs(t + kConvHalo, 2 * pp * ES, cbsx), xv);
+                for (int it = 0; it < ITEMS; ++it) {
+                    const int t = tq0 + it;
+                    const uint32_t o = off[it];
+                    float xr[2], uu[2];
+                    ld_k<T, 2>(rdt + o, xr);
+                    if constexpr (conv) {
+                        // u = silu(causal conv) over the window ending at step t
+                        float xv[2];
+                        ld_k<T, 2>(ru + offx[it + kConvHalo], xv);
 #pragma unroll
-                    for (int j = 0; j < kMaxConvK - 1; ++j) xw[j] = xw[j + 1];
-                    xw[kMaxConvK - 1] = make_float2(xv[0], xv[1]);
-                    float2 acc = make_float2(cbias[0], cbias[1]);
+                        for (int j = 0; j < kMaxConvK - 1; ++j) xw[j] = xw[j + 1];
+                        xw[kMaxConvK - 1] = make_float2(xv[0], xv[1]);
+                        float2 acc = make_float2(cbias[0], cbias[1]);
 #pragma unroll
-                    for (int j = 0; j < kMaxConvK; ++j)
-                        acc = __ffma2_rn(make_float2(cw[0][j], cw[1][j]), xw[j], acc);
-                    const float2 uv = Act<T>::silu2(acc);
-                    uu[0] = uv.x;
-                    uu[1] = uv.y;
-                    if constexpr (!summary) su2[t * (DT / 2) + pp] = uv;
-                } else {
-                    ld_k<T, 2>(ru + o, uu);
+                        for (int j = 0; j < kMaxConvK; ++j)
+                            acc = __ffma2_rn(make_float2(cw[0][j], cw[1][j]), xw[j], acc);
+                        const float2 uv = Act<T>::silu2(acc);
+                        uu[0] = uv.x;
+                        uu[1] = uv.y;
+                        if constexpr (!summary) su2[t * (DT / 2) + pp] = uv;
+                    } else {
+                        ld_k<T, 2>(ru + o, uu);
+                    }
+                    float2 x = __fadd2_rn(make_float2(xr[0], xr[1]), b2);
+                    if (softplus) x = Act<T>::softplus2(x);
+                    if constexpr (decltype(tail)::value) {
+                        if (t >= tv) x = make_float2(0.f, 0.f);
+                    }
+                    // (dt, dt u); with the ZOH B the scan scales u itself: (dt, u)
+                    const float2 xu = ZOH ? make_float2(uu[0], uu[1])
+                                          : __fmul2_rn(x, make_float2(uu[0], uu[1]));
+                    *reinterpret_cast<float4*>(sdd + t * DT + 2 * pp) =
+                        make_float4(x.x, xu.x, x.y, xu.y);
                 }
-                float2 x = __fadd2_rn(make_float2(xr[0], xr[1]), b2);
-                if (p.softplus) x = Act<T>::softplus2(x);
-                // (dt, dt u); with the ZOH B the scan scales u itself: (dt, u)
-                const float2 xu = ZOH ? make_float2(uu[0], uu[1])
-                                      : __fmul2_rn(x, make_float2(uu[0], uu[1]));
-                *reinterpret_cast<float4*>(sdd + t * DT + 2 * pp) =
-                    t < tv ? make_float4(x.x, xu.x, x.y, xu.y) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            };
+            if (tv == TC) items(std::false_type{});
+            else items(std::true_type{});
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(bar_full(bf));
