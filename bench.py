@@ -800,6 +800,20 @@ def run_op(args, wl):
     b.record()
     torch.cuda.synchronize()
     us = a.elapsed_time(b) * 1e3 / (reps * 100)
+    # the same graph shape around a kernel that does nothing (torch's spin
+    # kernel for 0 cycles): the launch and scheduling floor of a graph node
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ge):
+        for _ in range(100):
+            torch.cuda._sleep(0)
+    ge.replay()
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        ge.replay()
+    b.record()
+    torch.cuda.synchronize()
+    empty_us = a.elapsed_time(b) * 1e3 / (reps * 100)
     state_bytes = wl.batch * wl.dim * wl.N * 8 + wl.dim * wl.N * 4
     cpu = None
     if not args.no_cpu_baseline:
@@ -821,7 +835,10 @@ def run_op(args, wl):
         "steps_timed": reps * 100,
         "hbm": {"achieved_gbs": state_bytes / (us * 1e-6) / 1e9, "peak_gbs": hbm_gbs,
                 "frac": state_bytes / (us * 1e-6) / 1e9 / hbm_gbs, "peak_source": hbm_src},
-        "timing": "CUDA graph of 100 steps, device time per step", "cpu_baseline": cpu,
+        "timing": "CUDA graph of 100 steps, device time per step",
+        "empty_kernel_graph_us": empty_us,
+        "above_empty_kernel_us": us - empty_us,
+        "cpu_baseline": cpu,
         "dtype": "f32", "data": "synthetic (seeded; see ssm_workloads.py)",
         "config": {"workload": wl.name, "batch": wl.batch, "dim": wl.dim, "N": wl.N,
                    "io_dtype": wl.dtype}, "impl": "ours"}

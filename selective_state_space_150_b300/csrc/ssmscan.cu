@@ -429,35 +429,54 @@ __device__ __forceinline__ float scan_step(float2 v, const float (&bb)[NPT], con
 // The same step with the exact zero-order-hold B (itwiki "상태 공간 모델",
 // section "이산화": Bbar = (dt A)^-1 (exp(dt A) - 1) dt B, per state
 // (e - 1) / A B with e = exp(dt A)).  v = (dt, u); ia = 1 / A (0 where A = 0).
-// The factor (e - 1) / A = dt phi(x), phi(x) = (e^x - 1) / x, x = dt A.  For
-// |x| < 1/16 it is dt (1 + x/2 + x^2/6 + x^3/24): the series of phi to third
-// order (the first dropped term, x^4/120, is below 1.3e-7 relative), evaluated
-// in the base-2 exponent x2 = x log2(e) the decay already needs
-// (coefficients ln2/2, ln2^2/6, ln2^3/24); it also gives the limit dt at A = 0.
-// Elsewhere (e - 1) / A loses at most ~3e-6 relative (e's ex2 error over |x|).
-constexpr float kZ1 = 0.34657359027997264f;   // ln2 / 2
-constexpr float kZ2 = 0.08007550231970023f;   // ln2^2 / 6
-constexpr float kZ3 = 0.013876027166205394f;  // ln2^3 / 24
-constexpr float kZCut = 0.09016844005556021f; // 1 / (16 ln2): |x| < 1/16
-__device__ __forceinline__ float2 zoh_factor2(float2 vx, float2 x2, float2 e, float2 ia) {
-    float2 s = __ffma2_rn(x2, make_float2(kZ3, kZ3), make_float2(kZ2, kZ2));
-    s = __ffma2_rn(s, x2, make_float2(kZ1, kZ1));
-    s = __ffma2_rn(s, x2, make_float2(1.f, 1.f));
-    const float2 fs = __fmul2_rn(vx, s);
-    const float2 fl = __fmul2_rn(__fadd2_rn(e, make_float2(-1.f, -1.f)), ia);
-    return make_float2(fabsf(x2.x) < kZCut ? fs.x : fl.x, fabsf(x2.y) < kZCut ? fs.y : fl.y);
+// The factor (e - 1) / A = dt phi(x), phi(x) = (e^x - 1) / x, x = dt A.  Near
+// x = 0 it is dt times a truncated series of phi, evaluated in the base-2
+// exponent x2 = x log2(e) the decay already needs; that also gives the limit
+// dt at A = 0.  Elsewhere it is e / A - 1 / A in one fused multiply-add, which
+// loses |error of e| / |x| relative to cancellation (e from ex2.approx).
+//   fp32 tensors: |x| < 1/16, series to third order (coefficients ln2/2,
+//     ln2^2/6, ln2^3/24; the first dropped term, x^4/120, is below 1.3e-7
+//     relative); the other side loses at most ~3e-6.
+//   bf16 tensors: |x| < 1/64, series to first order (dropped x^2/6 below
+//     4.1e-5 relative); the other side loses at most ~2e-5.  Both are far
+//     below the 2^-9 relative rounding of a bf16 output.
+// A lane computes both sides for its states and keeps one: lanes are channels
+// with their own dt, so a branch would diverge.
+constexpr float kZ1 = 0.34657359027997264f;     // ln2 / 2
+constexpr float kZ2 = 0.08007550231970023f;     // ln2^2 / 6
+constexpr float kZ3 = 0.013876027166205394f;    // ln2^3 / 24
+constexpr float kZCut = 0.09016844005556021f;   // 1 / (16 ln2): |x| < 1/16
+constexpr float kZCutLo = 0.022542110013890053f; // 1 / (64 ln2): |x| < 1/64
+// vxk = dt ln2 / 2 (used by the first-order form only)
+template <bool LOWP>
+__device__ __forceinline__ float2 zoh_factor2(float2 vx, float2 vxk, float2 x2, float2 e,
+                                              float2 ia) {
+    float2 fs;
+    if constexpr (LOWP) {
+        fs = __ffma2_rn(vxk, x2, vx);  // dt (1 + x/2)
+    } else {
+        float2 s = __ffma2_rn(x2, make_float2(kZ3, kZ3), make_float2(kZ2, kZ2));
+        s = __ffma2_rn(s, x2, make_float2(kZ1, kZ1));
+        s = __ffma2_rn(s, x2, make_float2(1.f, 1.f));
+        fs = __fmul2_rn(vx, s);
+    }
+    const float2 fl = __ffma2_rn(e, ia, make_float2(-ia.x, -ia.y));
+    constexpr float cut = LOWP ? kZCutLo : kZCut;
+    return make_float2(fabsf(x2.x) < cut ? fs.x : fl.x, fabsf(x2.y) < cut ? fs.y : fl.y);
 }
 
-template <int NPT, bool WITH_C>
+template <int NPT, bool WITH_C, bool LOWP>
 __device__ __forceinline__ float scan_step_zoh(float2 v, const float (&bb)[NPT],
                                                const float (&cc)[NPT], const float (&a2)[NPT],
                                                const float (&ia)[NPT], float (&h)[NPT]) {
     const float2 vx = make_float2(v.x, v.x), vy = make_float2(v.y, v.y);
+    const float k = v.x * kZ1;
+    const float2 vxk = make_float2(k, k);
     if constexpr (NPT == 1) {
         const float x2 = v.x * a2[0];
         const float e = ex2_approx(x2);
-        const float2 f = zoh_factor2(vx, make_float2(x2, x2), make_float2(e, e),
-                                     make_float2(ia[0], ia[0]));
+        const float2 f = zoh_factor2<LOWP>(vx, vxk, make_float2(x2, x2), make_float2(e, e),
+                                           make_float2(ia[0], ia[0]));
         h[0] = fmaf(e, h[0], (v.y * bb[0]) * f.x);
         return WITH_C ? cc[0] * h[0] : 0.f;
     } else {
@@ -466,7 +485,7 @@ __device__ __forceinline__ float scan_step_zoh(float2 v, const float (&bb)[NPT],
         for (int j = 0; j < NPT; j += 2) {
             const float2 x = __fmul2_rn(vx, make_float2(a2[j], a2[j + 1]));
             const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            const float2 f = zoh_factor2(vx, x, e, make_float2(ia[j], ia[j + 1]));
+            const float2 f = zoh_factor2<LOWP>(vx, vxk, x, e, make_float2(ia[j], ia[j + 1]));
             const float2 w = __fmul2_rn(__fmul2_rn(vy, make_float2(bb[j], bb[j + 1])), f);
             const float2 hh = __ffma2_rn(e, make_float2(h[j], h[j + 1]), w);
             h[j] = hh.x;
@@ -477,17 +496,18 @@ __device__ __forceinline__ float scan_step_zoh(float2 v, const float (&bb)[NPT],
     }
 }
 
-template <int NPT, bool WITH_C, bool ZOH>
+// ZK: 0 Euler B; 1 exact ZOH B for fp32 tensors; 2 for bf16 tensors
+template <int NPT, bool WITH_C, int ZK>
 __device__ __forceinline__ float scan_step_any(float2 v, const float (&bb)[NPT],
                                                const float (&cc)[NPT], const float (&a2)[NPT],
                                                const float (&ia)[NPT], float (&h)[NPT]) {
-    if constexpr (ZOH) return scan_step_zoh<NPT, WITH_C>(v, bb, cc, a2, ia, h);
+    if constexpr (ZK != 0) return scan_step_zoh<NPT, WITH_C, ZK == 2>(v, bb, cc, a2, ia, h);
     else return scan_step<NPT, WITH_C>(v, bb, cc, a2, h);
 }
 
 // Summary variant: the same state update without the readout; returns the
 // chunk's sum of dt for this channel (padded steps hold dt = 0).
-template <int NPT, int NP, int DT, int TC, bool ZOH = false>
+template <int NPT, int NP, int DT, int TC, int ZK = 0>
 __device__ __forceinline__ float scan_chunk_summary(const float2* __restrict__ dd,
                                                    const float* __restrict__ Bs,
                                                    const float (&a2)[NPT],
@@ -503,7 +523,7 @@ __device__ __forceinline__ float scan_chunk_summary(const float2* __restrict__ d
             float bb[NPT];
             ld_states<NPT>(Bs + t * NP, bb);
             sdt += v.x;
-            scan_step_any<NPT, false, ZOH>(v, bb, bb, a2, ia, h);
+            scan_step_any<NPT, false, ZK>(v, bb, bb, a2, ia, h);
         }
     }
     return sdt;
@@ -514,7 +534,7 @@ __device__ __forceinline__ float scan_chunk_summary(const float2* __restrict__ d
 // stay in registers until its steps are done: a shared store between steps
 // would keep the compiler from issuing later steps' loads ahead of it and
 // serialise the steps.
-template <int NPT, int NP, int DT, int TC, bool ZOH = false>
+template <int NPT, int NP, int DT, int TC, int ZK = 0>
 __device__ __forceinline__ void scan_chunk(const float2* __restrict__ dd,
                                            const float* __restrict__ Bs,
                                            const float* __restrict__ Cs,
@@ -531,7 +551,7 @@ __device__ __forceinline__ void scan_chunk(const float2* __restrict__ dd,
             float bb[NPT], cc[NPT];
             ld_states<NPT>(Bs + t * NP, bb);
             ld_states<NPT>(Cs + t * NP, cc);
-            pv[i] = scan_step_any<NPT, true, ZOH>(dd[t * DT], bb, cc, a2, ia, h);
+            pv[i] = scan_step_any<NPT, true, ZK>(dd[t * DT], bb, cc, a2, ia, h);
         }
 #pragma unroll
         for (int i = 0; i < SB; ++i) part[(t0 + i) * DT] = pv[i];
@@ -983,6 +1003,7 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
     volatile int* const abort_flag = &s_abort;
     unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     constexpr bool conv = CONV;  // the convolution prologue (p.conv_k > 0)
+    constexpr int ZK = ZOH ? (sizeof(T) == 2 ? 2 : 1) : 0;  // the B of the scan step
     const LayoutW<T, NPT, WS, TC, SUMMARY> lay(p.N, p.stages, conv);
     const int nst = p.stages;
 
@@ -1088,12 +1109,12 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
                 return;
             }
             if constexpr (summary) {
-                sdt_seg += double(scan_chunk_summary<NPT, NP, DT, TC, ZOH>(
+                sdt_seg += double(scan_chunk_summary<NPT, NP, DT, TC, ZK>(
                     s_dd(bf) + c, s_B(bf) + sg * NPT, a2, ia, h));
             } else {
-                scan_chunk<NPT, NP, DT, TC, ZOH>(s_dd(bf) + c, s_B(bf) + sg * NPT,
-                                                 s_C(bf) + sg * NPT,
-                                                 s_part(bf) + sg * TC * DT + c, a2, ia, h);
+                scan_chunk<NPT, NP, DT, TC, ZK>(s_dd(bf) + c, s_B(bf) + sg * NPT,
+                                                s_C(bf) + sg * NPT,
+                                                s_part(bf) + sg * TC * DT + c, a2, ia, h);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_done(bf));
