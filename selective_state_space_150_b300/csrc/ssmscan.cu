@@ -341,6 +341,12 @@ struct KParams {
     const float* conv_b;  // [dim] or null
     int conv_k;           // 0 (no prologue) or 1 .. kMaxConvK
     int zoh;              // 1: exact zero-order-hold B (warp-specialised kernel only)
+    // Checkpoints for the backward (warp-specialised summary instantiation,
+    // one segment): the state before every 16-step chunk c goes to
+    // ckpt[((b * nchunks + c) * dim + d) * N + n], the walk starts from h0, dt
+    // takes the backward's softplus (the MUFU form) for either input type, and
+    // nothing else is written.  NULL otherwise.
+    float* ckpt;
 };
 
 // Compile-time geometry of one block.
@@ -1084,7 +1090,7 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
             const float a = (scan_ok && n < N) ? p.A[d_scan * N + n] : 0.f;
             a2[j] = a * kLog2e;
             ia[j] = (ZOH && a != 0.f) ? 1.f / a : 0.f;  // the ZOH factor's 1 / A
-            h[j] = (p.h0 != nullptr && !summary && scan_ok && n < N)
+            h[j] = (p.h0 != nullptr && (!summary || p.ckpt != nullptr) && scan_ok && n < N)
                        ? p.h0[(b * dim + d_scan) * N + n]
                        : 0.f;
         }
@@ -1109,6 +1115,18 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
                 return;
             }
             if constexpr (summary) {
+                if (p.ckpt != nullptr && scan_ok) {  // the state before chunk c_begin + k
+                    float* const ck = p.ckpt + ((b * nchunks + c_begin + k) * dim + d_scan) * N +
+                                      int64_t(sg) * NPT;
+                    if (NPT == 4 && (N & 3) == 0) {
+                        *reinterpret_cast<float4*>(ck) = make_float4(h[0], h[1 % NPT],
+                                                                     h[2 % NPT], h[3 % NPT]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < NPT; ++j)
+                            if (int64_t(sg) * NPT + j < N) ck[j] = h[j];
+                    }
+                }
                 sdt_seg += double(scan_chunk_summary<NPT, NP, DT, TC, ZK>(
                     s_dd(bf) + c, s_B(bf) + sg * NPT, a2, ia, h));
             } else {
@@ -1121,7 +1139,7 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
             if (++bf == kBufs) { bf = 0; par ^= 1u; }
         }
         if constexpr (summary) {
-            if (scan_ok) {
+            if (scan_ok && p.hseg != nullptr) {
                 const int64_t r = (seg * p.batch + b) * dim + d_scan;
 #pragma unroll
                 for (int j = 0; j < NPT; ++j) {
@@ -1224,6 +1242,7 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
         const T* gC = static_cast<const T*>(p.C);
         const bool bc_vec = p.tma_bc && N == NP && (N % 4) == 0;
         const bool softplus = p.softplus != 0;
+        const bool mufu_sp = p.ckpt != nullptr;  // checkpoints: the backward's dt
         int s = 0;
         uint32_t ph = 0;
         int bf = 0;        // buffer of chunk k: k % kBufs
@@ -1311,7 +1330,8 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
                         ld_k<T, 2>(ru + o, uu);
                     }
                     float2 x = __fadd2_rn(make_float2(xr[0], xr[1]), b2);
-                    if (softplus) x = Act<T>::softplus2(x);
+                    if (softplus) x = (summary && mufu_sp) ? Act<__nv_bfloat16>::softplus2(x)
+                                                           : Act<T>::softplus2(x);
                     if constexpr (decltype(tail)::value) {
                         if (t >= tv) x = make_float2(0.f, 0.f);
                     }
@@ -1612,26 +1632,37 @@ struct BwdParams {
     float* sseg;   // [nseg][batch][dim]
     int64_t batch, L, dim, N, ntile, nchunks, nslice, nseg, seg_chunks;
     int softplus;
+    // 1: ckpt already holds every chunk's starting state (written by the
+    // forward's warp-specialised pipeline; one segment only), so the kernel
+    // starts with the reverse pass
+    int ckpt_ready;
 };
+
+// The backward's activations, for either input type: the MUFU forms of the
+// bf16 forward (softplus, and sigmoid = 1 / (1 + 2^(-x log2 e)), ~1e-7
+// error), the same arithmetic whatever the tensors' type, so that the bf16
+// entry's gradients are the fp32 entry's, rounded.  Their error is three
+// orders below the gradients' tolerance.
+__device__ __forceinline__ float sigmoid_mufu(float x) {
+    return rcp_approx(1.f + ex2_approx(-x * kLog2e));
+}
 
 // The per-(step, channel) gradients from the sums over all states of the
 // readout yc (without the skip term), the dt term gdt and the u term gu.
 // Returns the gated output gradient dyc; du, ddelta, dz through references.
-// The activations are the accurate fp32 forms for either input type, so the
-// bf16 entry's gradients are the fp32 entry's, rounded.
 __device__ __forceinline__ float grad_point(float yc, float gdt, float gu, float raw, float x,
                                             float dyo, float zz, bool has_z, int softplus,
                                             float Dd, float& du, float& ddelta, float& dz) {
     float g = 1.f, gz = 0.f;
     yc = fmaf(Dd, x, yc);
     if (has_z) {
-        const float sgm = 1.f / (1.f + expf(-zz));
+        const float sgm = sigmoid_mufu(zz);
         g = zz * sgm;
         gz = dyo * yc * sgm * (1.f + zz * (1.f - sgm));  // d silu / dz
     }
     const float dyc = dyo * g;
     du = fmaf(dyc, Dd, gu);
-    ddelta = softplus ? gdt / (1.f + expf(-raw)) : gdt;  // softplus' = sigmoid
+    ddelta = softplus ? gdt * sigmoid_mufu(raw) : gdt;  // softplus' = sigmoid
     dz = gz;
     return dyc;
 }
@@ -1787,7 +1818,7 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
             const bool in = ok && i < tv;
             const float r = E::to_f(f.raw[k]) + (in ? bias : 0.f);
             s_raw[i * 32 + lane] = r;
-            s_dt[i * 32 + lane] = in ? (q.softplus ? Act<float>::softplus(r) : r) : 0.f;
+            s_dt[i * 32 + lane] = in ? (q.softplus ? Act<__nv_bfloat16>::softplus(r) : r) : 0.f;
             s_x[i * 32 + lane] = E::to_f(f.x[k]);
             if (rev) {
                 const float dyv = E::to_f(f.dy[k]), zv = E::to_f(f.z[k]);
@@ -1795,7 +1826,7 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
                 s_z[i * 32 + lane] = zv;
                 // the gated output gradient, once per (step, channel) rather
                 // than once per state group
-                const float g = q.z != nullptr ? zv / (1.f + expf(-zv)) : 1.f;
+                const float g = q.z != nullptr ? zv * sigmoid_mufu(zv) : 1.f;
                 s_dyc[i * 32 + lane] = dyv * g;
             }
         }
@@ -1851,8 +1882,13 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
         }
     }
     Fetched f;
-    if (c_end > c_begin) fetch(c_begin, false, f);
-    for (int64_t c = c_begin; c < c_end; ++c) {
+    if (!SUM && q.ckpt_ready) {
+        // the checkpoints are there: the reverse pass's first chunk
+        if (c_end > c_begin) fetch(c_end - 1, true, f);
+    } else if (c_end > c_begin) {
+        fetch(c_begin, false, f);
+    }
+    for (int64_t c = c_begin; c < ((!SUM && q.ckpt_ready) ? c_begin : c_end); ++c) {
         const int tv = chunk_len(c);
         if (!SUM && ok) {
 #pragma unroll
@@ -2696,6 +2732,7 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     kp.seg_chunks = pl.seg_chunks;
     kp.hseg = nullptr;
     kp.sseg = nullptr;
+    kp.ckpt = nullptr;
     kp.h0 = h0;
     kp.conv_w = conv_w;
     kp.conv_b = conv_b;
@@ -2731,6 +2768,58 @@ int scan_fwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     if (!fixed_scratch && cudaFreeAsync(scratch, stream) != cudaSuccess && st == SSM_OK)
         st = SSM_ERR_LAUNCH;
     return st;
+}
+
+// The backward's checkpoints by the warp-specialised summary kernel over the
+// whole sequence: the state before every 16-step chunk, from h0 (zero when
+// NULL), with the backward's own dt (the MUFU softplus), so that they equal
+// the states the backward kernel's own forward walk would keep.  Returns
+// false, launching nothing, where the kernel's tiles cannot move by TMA;
+// otherwise *st is the launch status.
+template <typename T>
+bool ckpt_fwd_ws(const T* u, const T* delta, const float* A, const T* B,
+                 const float* delta_bias, int softplus_flag, const float* h0, float* ckpt,
+                 int64_t batch, int64_t L, int64_t dim, int64_t N, cudaStream_t stream, int* st) {
+    if (L <= 0 || batch <= 0 || dim <= 0) return false;
+    const Plan pl = make_plan<T>(batch, L, dim, N, u, delta, nullptr, u, B, B, true, false,
+                                 /*need_ws=*/true);
+    if (!pl.ws || pl.TC != kBwdTC || !pl.tma_udz) return false;
+    const size_t es = sizeof(T);
+    CUtensorMap tms[6];
+    std::memset(tms, 0, sizeof(tms));
+    const auto ty = Elt<T>::tmap_type;
+    const int box = pl.row_span / int(es);
+    const auto swz = swizzle_for(pl.row_span);
+    if (!encode3d(&tms[0], ty, es, u, dim, L, batch, box, pl.TC, swz) ||
+        !encode3d(&tms[1], ty, es, delta, dim, L, batch, box, pl.TC, swz))
+        return false;
+    const bool tma_bc = pl.tma_bc && encode3d(&tms[3], ty, es, B, N, L, batch, int(N), pl.TC,
+                                              CU_TENSOR_MAP_SWIZZLE_NONE);
+    KParams kp;
+    std::memset(&kp, 0, sizeof(kp));
+    kp.u = u;
+    kp.delta = delta;
+    kp.B = B;
+    kp.C = B;  // not read by the summary instantiation
+    kp.A = A;
+    kp.bias = delta_bias;
+    kp.batch = batch;
+    kp.L = L;
+    kp.dim = dim;
+    kp.N = N;
+    kp.nblk_d = (dim + pl.DT - 1) / pl.DT;
+    kp.wait_ns = uint64_t(g_wait_ns.load());
+    kp.softplus = softplus_flag ? 1 : 0;
+    kp.tma_udz = 1;
+    kp.tma_bc = tma_bc ? 1 : 0;
+    kp.stages = pl.stages;
+    kp.summary = 1;
+    kp.n_seg = 1;
+    kp.seg_chunks = (L + pl.TC - 1) / pl.TC;
+    kp.h0 = h0;
+    kp.ckpt = ckpt;
+    *st = dispatch<T>(pl, pl.grid, tms, kp, stream);
+    return true;
 }
 
 // One recurrent step: checks, then one thread per channel.
@@ -3089,6 +3178,20 @@ int scan_bwd(const T* u, const T* delta, const float* A, const T* B, const T* C,
     q.dh_last = dh_last;
     q.dh0 = dh0;
     q.softplus = softplus_flag ? 1 : 0;
+    q.ckpt_ready = 0;
+    if (nseg == 1) {
+        // the checkpoints by the forward's TMA pipeline, where it applies
+        int cst = SSM_OK;
+        if (ckpt_fwd_ws<T>(u, delta, A, B, delta_bias, softplus_flag, h0, q.ckpt, batch, L, dim,
+                           N, stream, &cst)) {
+            if (cst != SSM_OK) {
+                (void)cudaGetLastError();
+                (void)cudaFreeAsync(scratch, stream);
+                return cst;
+            }
+            q.ckpt_ready = 1;
+        }
+    }
     // every (tile, b, t, n < N) entry of the partial dB / dC is written by
     // exactly one lane
     // warps of kBwdNPT states per 32 channels; N > kBwdSlice runs as slices
