@@ -1667,32 +1667,6 @@ __device__ __forceinline__ float grad_point(float yc, float gdt, float gu, float
     return dyc;
 }
 
-// Sum of v[j] (j < NPT) over the 32 lanes, NPT values at once: each round
-// halves the values a lane keeps and swaps the other half with the partner
-// lane (NPT - 1 + log2(32 / NPT) shuffles instead of 5 NPT).  Afterwards the
-// lane holds the total for index nb, and lanes that differ only in their
-// low log2(32 / NPT) bits hold the same total.
-template <int NPT, int M, int O>
-__device__ __forceinline__ void reduce_rounds(float (&v)[NPT], int lane, int& nb) {
-    if constexpr (O >= 1) {
-        if constexpr (M > 1) {
-            constexpr int HM = M / 2;
-            const bool up = (lane & O) != 0;
-#pragma unroll
-            for (int j = 0; j < HM; ++j) {
-                const float send = up ? v[j] : v[j + HM];
-                const float keep = up ? v[j + HM] : v[j];
-                v[j] = keep + __shfl_xor_sync(0xffffffffu, send, O);
-            }
-            if (up) nb += HM;
-            reduce_rounds<NPT, HM, O / 2>(v, lane, nb);
-        } else {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], O);
-            reduce_rounds<NPT, 1, O / 2>(v, lane, nb);
-        }
-    }
-}
-
 // Block = WS warps over the same 32 channels (lane = channel); warp sg holds
 // states sg*4 .. sg*4 + 3.  Each chunk's inputs are loaded into registers one
 // chunk ahead and staged in shared memory by the whole block; the per-step
@@ -2043,17 +2017,21 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
             pp[0] = yc2.x + yc2.y;
             pp[32] = fmaf(x, lamB, ga2.x + ga2.y);
             pp[64] = dt * lamB;
-            // dB and dC together: afterwards lane l holds the channel sum of
-            // share nb, and lanes differing only in their low two bits agree
-            int nb = 0;
-            reduce_rounds<2 * NPT, 2 * NPT, 16>(v, lane, nb);
-            if ((lane & (32 / (2 * NPT) - 1)) == 0) {
-                const int64_t n = n0 + (nb % NPT);
-                if (n < N) {
-                    const int64_t o = ((tile * q.batch + b) * L + t0 + i) * N + n;
-                    (nb < NPT ? q.pB : q.pC)[o] = v[0];
-                }
+            // dB and dC shares: one shuffle round leaves lanes 0-15 with the B
+            // shares and lanes 16-31 with the C shares, each summed over two
+            // lanes; they go to the step's row of myh (free again: the step
+            // after it has read it), each lane's 16 bytes at position lane ^ i
+            // so that the sums after the chunk read it without bank conflicts
+            const bool up = (lane & 16) != 0;
+            float r[NPT];
+#pragma unroll
+            for (int j = 0; j < NPT; ++j) {
+                const float send = up ? v[j] : v[NPT + j];
+                const float keep = up ? v[NPT + j] : v[j];
+                r[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
             }
+            *reinterpret_cast<float4*>(myh + (i * 32 + (lane ^ i)) * NPT) =
+                make_float4(r[0], r[1], r[2], r[3]);
         };
         static_assert(NPT == 4, "one 16-byte row of states per (step, lane)");
         auto fwd_keep = [&](int i) {
@@ -2091,6 +2069,31 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
 #pragma unroll
             for (int j = 0; j < NPT; ++j) hc[j] = h[j];
             for (int i = tv - 1; i >= 0; --i) rev_from(i, hc);
+        }
+        __syncwarp();
+        {
+            // the chunk's dB (lanes 0-15) and dC (16-31) channel sums of this
+            // warp's states: lane l sums step l % 16 over the 16 two-lane sums
+            // in order, and leaves one partial per (tile, row, step, state)
+            const int i = lane & 15, gC = lane >> 4;
+            if (i < tv) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const float4 x4 = *reinterpret_cast<const float4*>(
+                        myh + (i * 32 + ((16 * gC + m) ^ i)) * NPT);
+                    acc.x += x4.x; acc.y += x4.y; acc.z += x4.z; acc.w += x4.w;
+                }
+                float* const dst = (gC ? q.pC : q.pB) + ((tile * q.batch + b) * L + t0 + i) * N + n0;
+                const float av[NPT] = {acc.x, acc.y, acc.z, acc.w};
+                if (n0 + NPT <= N && (N & 3) == 0) {
+                    *reinterpret_cast<float4*>(dst) = acc;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < NPT; ++j)
+                        if (n0 + j < N) dst[j] = av[j];
+                }
+            }
         }
         __syncthreads();
         // the chunk's per-(step, channel) gradients: warp sg takes steps sg, sg + WS, ...
