@@ -512,17 +512,24 @@ def pipe_peaks(stream_ptr):
 
 
 def bwd_accounting(wl: W.Workload, es: int = 4):
-    """(bytes, MUFU ops) of one backward call whose tensors are es bytes per
-    element.  Bytes: u, delta, z, dy, B, C read once, du, ddelta, dz, dB, dC
-    written once, plus A, D, bias and their fp32 gradients.  MUFU ops: the recomputation evaluates exp(dt A) three
-    times per (b, t, d, n) -- the checkpoint pass, the chunk's recomputed
-    states and the adjoint step -- and per (b, t, d) a softplus (ex2, lg2) in
-    each pass and the gate's exponential in the reverse pass."""
+    """(bytes, MUFU ops, FP32 lane ops) of one backward call whose tensors are
+    es bytes per element.  Bytes: u, delta, z, dy, B, C read once, du, ddelta,
+    dz, dB, dC written once, plus A, D, bias and their fp32 gradients.  MUFU
+    ops: the recomputation evaluates exp(dt A) three times per (b, t, d, n) --
+    the checkpoint pass, the chunk's recomputed states and the adjoint step --
+    and per (b, t, d) a softplus (ex2, lg2) in each pass and the gate's
+    exponential in the reverse pass.  FP32 lane ops per (b, t, d, n): 3 for
+    each of the two forward walks (dt A, (dt u) B, the state FMA), 11 for the
+    adjoint step (readout, lambda, dt A, e h_prev, lambda e h_prev, dA, the dt
+    term, lambda B, the dB and dC shares, the carry) and 2 for the channel sums
+    of the dB and dC shares; per (b, t, d) 8 (bias, dt u twice, skip, du,
+    ddelta, dD and dbias sums) and 6 more with the gate."""
     bld, bln = wl.batch * wl.L * wl.dim, wl.batch * wl.L * wl.N
     gate = 1 if wl.gate else 0
     nbytes = es * bld * (2 * (2 + gate) + 1) + es * bln * 4 + 8 * wl.dim * (wl.N + 2)
     mufu = 3 * bld * wl.N + bld * ((4 if wl.softplus else 0) + gate)
-    return nbytes, mufu
+    fp32 = 19 * bld * wl.N + bld * (8 + 6 * gate)
+    return nbytes, mufu, fp32
 
 
 def op_cpu_baseline(kind: str, wl: W.Workload, inp, rows: int = 1, n_dim: int = 16,
@@ -673,15 +680,10 @@ def run_op(args, wl):
         ms_fwd = _events_mean_ms(fwd_call, args.steps, stream)
         ms_bwd = ms_io
         peaks = pipe_peaks(stream.cuda_stream)
-        nbytes, mufu = bwd_accounting(wl, es)
-        roof = {"bound": "alu", "pipe": "mufu_ex2", "unit": "Gop/s",
-                "achieved": mufu / (ms_bwd * 1e-3) / 1e9, "mufu_ops_per_launch": mufu,
-                "algorithmic_bytes_per_launch": nbytes, "traffic": None,
-                "hbm_frac": nbytes / (ms_bwd * 1e-3) / 1e9 / hbm_gbs}
-        if "ex2_per_s" in peaks:
-            roof["peak"] = peaks["ex2_per_s"] / 1e9
-            roof["frac"] = roof["achieved"] / roof["peak"]
-            roof["peak_source"] = "measured on this GPU by libpipepeaks, same run"
+        nbytes, mufu, fp32 = bwd_accounting(wl, es)
+        roof = compute_roofline(mufu, fp32, ms_bwd, peaks)
+        roof.update({"algorithmic_bytes_per_launch": nbytes, "traffic": None,
+                     "hbm_frac": nbytes / (ms_bwd * 1e-3) / 1e9 / hbm_gbs})
         return {
             "op": "bwd", "metric": "selective-scan backward (recomputation) tokens/s",
             "value": wl.tokens / (ms_bwd * 1e-3), "unit": "tokens/s", "higher_is_better": True,

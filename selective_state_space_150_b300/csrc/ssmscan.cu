@@ -341,8 +341,8 @@ struct KParams {
     const float* conv_b;  // [dim] or null
     int conv_k;           // 0 (no prologue) or 1 .. kMaxConvK
     int zoh;              // 1: exact zero-order-hold B (warp-specialised kernel only)
-    // Checkpoints for the backward (warp-specialised summary instantiation,
-    // one segment): the state before every 16-step chunk c goes to
+    // Checkpoints for the backward (the warp-specialised kernel's checkpoint
+    // instantiation, one segment): the state before every 16-step chunk c goes to
     // ckpt[((b * nchunks + c) * dim + d) * N + n], the walk starts from h0, dt
     // takes the backward's softplus (the MUFU form) for either input type, and
     // nothing else is written.  NULL otherwise.
@@ -992,7 +992,8 @@ struct LayoutW {
 
 // The block's work; the tensor maps are the kernel's own __grid_constant__
 // parameters, passed by reference so that TMA sees their parameter addresses.
-template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH>
+template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH,
+          bool CKPT = false>
 __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensorMap& tm_dt,
                                          const CUtensorMap& tm_z, const CUtensorMap& tm_B,
                                          const CUtensorMap& tm_C, const CUtensorMap& tm_y,
@@ -1010,6 +1011,7 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
     unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     constexpr bool conv = CONV;  // the convolution prologue (p.conv_k > 0)
     constexpr int ZK = ZOH ? (sizeof(T) == 2 ? 2 : 1) : 0;  // the B of the scan step
+    constexpr bool ckpt = SUMMARY && CKPT;  // the backward's checkpoints (KParams::ckpt)
     const LayoutW<T, NPT, WS, TC, SUMMARY> lay(p.N, p.stages, conv);
     const int nst = p.stages;
 
@@ -1090,7 +1092,7 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
             const float a = (scan_ok && n < N) ? p.A[d_scan * N + n] : 0.f;
             a2[j] = a * kLog2e;
             ia[j] = (ZOH && a != 0.f) ? 1.f / a : 0.f;  // the ZOH factor's 1 / A
-            h[j] = (p.h0 != nullptr && (!summary || p.ckpt != nullptr) && scan_ok && n < N)
+            h[j] = (p.h0 != nullptr && (!summary || ckpt) && scan_ok && n < N)
                        ? p.h0[(b * dim + d_scan) * N + n]
                        : 0.f;
         }
@@ -1115,7 +1117,7 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
                 return;
             }
             if constexpr (summary) {
-                if (p.ckpt != nullptr && scan_ok) {  // the state before chunk c_begin + k
+                if (ckpt && scan_ok) {  // the state before chunk c_begin + k
                     float* const ck = p.ckpt + ((b * nchunks + c_begin + k) * dim + d_scan) * N +
                                       int64_t(sg) * NPT;
                     if (NPT == 4 && (N & 3) == 0) {
@@ -1139,7 +1141,7 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
             if (++bf == kBufs) { bf = 0; par ^= 1u; }
         }
         if constexpr (summary) {
-            if (scan_ok && p.hseg != nullptr) {
+            if (scan_ok && !ckpt) {
                 const int64_t r = (seg * p.batch + b) * dim + d_scan;
 #pragma unroll
                 for (int j = 0; j < NPT; ++j) {
@@ -1242,7 +1244,6 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
         const T* gC = static_cast<const T*>(p.C);
         const bool bc_vec = p.tma_bc && N == NP && (N % 4) == 0;
         const bool softplus = p.softplus != 0;
-        const bool mufu_sp = p.ckpt != nullptr;  // checkpoints: the backward's dt
         int s = 0;
         uint32_t ph = 0;
         int bf = 0;        // buffer of chunk k: k % kBufs
@@ -1330,8 +1331,8 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
                         ld_k<T, 2>(ru + o, uu);
                     }
                     float2 x = __fadd2_rn(make_float2(xr[0], xr[1]), b2);
-                    if (softplus) x = (summary && mufu_sp) ? Act<__nv_bfloat16>::softplus2(x)
-                                                           : Act<T>::softplus2(x);
+                    // (the checkpoints take the backward's dt: the MUFU form)
+                    if (softplus) x = ckpt ? Act<__nv_bfloat16>::softplus2(x) : Act<T>::softplus2(x);
                     if constexpr (decltype(tail)::value) {
                         if (t >= tv) x = make_float2(0.f, 0.f);
                     }
@@ -1464,15 +1465,15 @@ __device__ __forceinline__ void ws_block(const CUtensorMap& tm_u, const CUtensor
         const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_B, \
         const __grid_constant__ CUtensorMap tm_C, const __grid_constant__ CUtensorMap tm_y, \
         const KParams p
-template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH>
+template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH, bool CKPT>
 __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT, GeoW<T, NPT, WS, TC>::MINB)
     ssm_scan_ws_kernel(SSM_WS_PARAMS) {
-    ws_block<T, NPT, WS, TC, SUMMARY, CONV, ZOH>(tm_u, tm_dt, tm_z, tm_B, tm_C, tm_y, p);
+    ws_block<T, NPT, WS, TC, SUMMARY, CONV, ZOH, CKPT>(tm_u, tm_dt, tm_z, tm_B, tm_C, tm_y, p);
 }
-template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH>
+template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH, bool CKPT>
 __global__ void __launch_bounds__(GeoW<T, NPT, WS, TC>::NT)
     ssm_scan_ws_kernel_free(SSM_WS_PARAMS) {
-    ws_block<T, NPT, WS, TC, SUMMARY, CONV, ZOH>(tm_u, tm_dt, tm_z, tm_B, tm_C, tm_y, p);
+    ws_block<T, NPT, WS, TC, SUMMARY, CONV, ZOH, CKPT>(tm_u, tm_dt, tm_z, tm_B, tm_C, tm_y, p);
 }
 #undef SSM_WS_PARAMS
 
@@ -2490,13 +2491,14 @@ int launch_one(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStre
     return cudaGetLastError() == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
-template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH = false>
+template <typename T, int NPT, int WS, int TC, bool SUMMARY, bool CONV, bool ZOH = false,
+          bool CKPT = false>
 int launch_one_w(int64_t grid, const CUtensorMap* tms, const KParams& kp, cudaStream_t stream) {
     using G = GeoW<T, NPT, WS, TC>;
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                  KParams);
-    if constexpr (G::MINB > 0) kern = ssm_scan_ws_kernel<T, NPT, WS, TC, SUMMARY, CONV, ZOH>;
-    else kern = ssm_scan_ws_kernel_free<T, NPT, WS, TC, SUMMARY, CONV, ZOH>;
+    if constexpr (G::MINB > 0) kern = ssm_scan_ws_kernel<T, NPT, WS, TC, SUMMARY, CONV, ZOH, CKPT>;
+    else kern = ssm_scan_ws_kernel_free<T, NPT, WS, TC, SUMMARY, CONV, ZOH, CKPT>;
     const size_t smem = smem_bytes_w<T, NPT, WS, SUMMARY>(kp.N, kp.stages, TC, CONV);
     static std::atomic<size_t> configured[64];
     int dev = 0;
@@ -2540,6 +2542,15 @@ int dispatch(const Plan& pl, int64_t grid, const CUtensorMap* tms, const KParams
                           : launch_one_w<T, NPT_, WS_, 16, false, true>(grid, tms, kp, stream);
         SSM_FOR_EACH_VARIANT(SSM_CASE_WC)
 #undef SSM_CASE_WC
+        return SSM_ERR_UNSUPPORTED_N;
+    }
+    if (pl.ws && kp.ckpt != nullptr) {  // the backward's checkpoints: 16-step chunks
+        if (pl.TC != 16 || kp.conv_k > 0 || !kp.summary) return SSM_ERR_ARG;
+#define SSM_CASE_WK(NPT_, WS_) \
+    if (pl.NPT == NPT_ && pl.WS == WS_) \
+        return launch_one_w<T, NPT_, WS_, 16, true, false, false, true>(grid, tms, kp, stream);
+        SSM_FOR_EACH_VARIANT(SSM_CASE_WK)
+#undef SSM_CASE_WK
         return SSM_ERR_UNSUPPORTED_N;
     }
     if (pl.ws) {

@@ -26,11 +26,14 @@ def test_forward_mufu_and_fp32_ops():
 
 def test_backward_accounting():
     bld, bln = 8 * 2048 * 1536, 8 * 2048 * 16
-    nbytes, mufu = bench.bwd_accounting(WL, es=2)
+    nbytes, mufu, fp32 = bench.bwd_accounting(WL, es=2)
     # reads u, delta, z, dy and writes du, ddelta, dz (2 bytes), B, C read and
     # dB, dC written, plus A, D, bias and their fp32 gradients
     assert nbytes == 2 * bld * 7 + 2 * bln * 4 + 8 * 1536 * 18
     assert mufu == 3 * bld * 16 + bld * 5
+    # per (b, t, d, n): two forward walks of 3, the adjoint step's 11, the
+    # dB / dC channel sums' 2; per (b, t, d): 8, and 6 for the gate
+    assert fp32 == (3 + 3 + 11 + 2) * bld * 16 + (8 + 6) * bld
     assert bench.bwd_accounting(WL, es=4)[0] == 4 * bld * 7 + 4 * bln * 4 + 8 * 1536 * 18
 
 
