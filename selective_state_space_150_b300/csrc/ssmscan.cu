@@ -290,6 +290,9 @@ struct Tile {
     static constexpr int RS = WB < 128 ? WB : 128;
     static constexpr int NB = WB / RS;
     static constexpr uint32_t SWZ_MASK = uint32_t(RS / 16 - 1);
+    // Period of the swizzle pattern: a column block must start on a multiple
+    // of it (address bits [7, 7 + log2(RS/16)) select the XOR).
+    static constexpr size_t SPAN = size_t(RS) * 8 < 128 ? 128 : size_t(RS) * 8;
     // Byte offset of byte b of row t in a tile of TC rows.
     __device__ static __forceinline__ uint32_t off(int t, int b, int TC) {
         return off_cbs(t, b, uint32_t(TC * RS));
@@ -955,7 +958,7 @@ struct GeoW {
 //   raw ring  stages x { u, delta, z : tile ; B, C : [TC][N] T }   (summary: u, delta, B)
 //             with the convolution prologue the u tile is the x tile, TC +
 //             kConvHalo rows from step t0 - kConvHalo, each column block
-//             padded to a multiple of 1024 bytes
+//             padded to a multiple of the swizzle period (Tile::SPAN)
 //   s_B, s_C  kBufs x [TC][NP] fp32        (summary: no s_C)
 //   s_dd      kBufs x [TC][DT] float2      (dt, dt*u)
 //   s_u       kBufs x [TC][DT] fp32        (prologue only: u for the skip term)
@@ -971,7 +974,8 @@ struct LayoutW {
     __host__ __device__ LayoutW(int64_t N, int stages, bool conv = false) {
         using TT = typename G::TileT;
         tile_bc = round1k(size_t(TC) * size_t(N) * G::ES);
-        cbs_x = conv ? round1k(size_t(TC + kConvHalo) * TT::RS) : size_t(TC) * TT::RS;
+        cbs_x = conv ? (size_t(TC + kConvHalo) * TT::RS + TT::SPAN - 1) / TT::SPAN * TT::SPAN
+                     : size_t(TC) * TT::RS;
         tile_x = conv ? TT::NB * cbs_x : G::TILE;
         stage = tile_x + (SUM ? 1 : 2) * G::TILE + (SUM ? 1 : 2) * tile_bc;
         bc = round1k(size_t(TC) * G::NP * 4);
@@ -2354,8 +2358,9 @@ size_t variant_smem_w(int npt, int ws, int64_t N, int stages, int TC, bool conv 
     return 0;
 }
 
-// Shared memory per warp-specialised block that still lets three blocks share an SM.
-constexpr size_t kWsSmemTarget = 72 * 1024;
+// Shared memory per warp-specialised block that still lets three blocks share
+// an SM: 3 x (75 KB + the 1 KB the hardware reserves per block) = 228 KB.
+constexpr size_t kWsSmemTarget = 75 * 1024;
 
 template <typename T>
 Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, const void* dt,
