@@ -286,9 +286,13 @@ SSM_API int ssm_scan_step_bf16(const uint16_t *u, const uint16_t *delta, const f
  * as slices of 16 states, also 3 * ceil(N / 16) * batch * L * dim; with time
  * segments, which the call uses when the batch rows and channels leave most
  * of the GPU idle, also about 2 * segments * batch * dim * N).  Partials are
- * folded in a fixed order, so results are deterministic.  N <= 128
- * (otherwise SSM_ERR_UNSUPPORTED_N).  Outputs must not overlap inputs or each
- * other.
+ * folded in a fixed order, so results are deterministic.  The softplus,
+ * SiLU and sigmoid inside the backward are the MUFU forms of the bf16
+ * forward (about 1e-7 absolute error) for both entry points, so the bf16
+ * entry's gradients are this entry's rounded; the fp32 forward's own
+ * softplus is the accurate library form, which differs by at most that
+ * much.  N <= 128 (otherwise SSM_ERR_UNSUPPORTED_N).  Outputs must not
+ * overlap inputs or each other.
  */
 SSM_API int ssm_scan_bwd(const float *u, const float *delta, const float *A,
                  const float *B, const float *C, const float *D,
