@@ -448,7 +448,7 @@ __device__ __forceinline__ float scan_step(float2 v, const float (&bb)[NPT], con
 //     relative); the other side loses at most ~3e-6.
 //   bf16 tensors: |x| < 1/64, series to first order (dropped x^2/6 below
 //     4.1e-5 relative); the other side loses at most ~2e-5.  Both are far
-//     below the 2^-9 relative rounding of a bf16 output.
+//     below the 2^-8 relative rounding of a bf16 output.
 // A lane computes both sides for its states and keeps one: lanes are channels
 // with their own dt, so a branch would diverge.
 constexpr float kZ1 = 0.34657359027997264f;     // ln2 / 2
