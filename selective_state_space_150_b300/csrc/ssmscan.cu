@@ -2467,6 +2467,17 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
         pl.n_seg = ns > 1 ? int((nchunks + pl.seg_chunks - 1) / pl.seg_chunks) : 1;
         if (pl.seg_chunks < 1) pl.seg_chunks = 1;
     }
+    // A warp-specialised grid of at most one block per SM has no residency to
+    // keep: it takes the deepest ring one block can hold (more chunks in
+    // flight; the results do not depend on the depth).
+    if (pl.ws && fs == 0 && pl.grid * pl.n_seg <= 148) {
+        for (int st : {6, 5, 4, 3})
+            if (st > pl.stages && variant_smem_w<T>(pl.NPT, pl.WS, N, st, pl.TC, conv) <= kMaxSmem) {
+                pl.stages = st;
+                pl.smem = variant_smem_w<T>(pl.NPT, pl.WS, N, st, pl.TC, conv);
+                break;
+            }
+    }
     return pl;
 }
 

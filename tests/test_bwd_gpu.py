@@ -229,6 +229,30 @@ def test_backward_with_states_matches_oracle(dtype, shape, which):
         assert err <= (BF16_TOL if bf else TOL), (names[k], err)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(8, 64, 256, 16), (4, 50, 96, 40), (6, 33, 96, 5)])
+def test_checkpoints_by_the_forward_pipeline_equal_the_kernels_own_walk(dtype, shape):
+    """Where the tiles can move by TMA the backward takes its checkpoints from
+    the forward's warp-specialised kernel (checkpoint instantiation); with
+    plain loads forced, the backward kernel walks forward itself.  The two
+    compute every state with the same arithmetic in the same order, so all
+    gradients, dh0 included, agree bit for bit."""
+    from selective_state_space_150_b300 import ssmscan as K
+    batch, L, dim, N = shape
+    plan = ssm.ssm_scan_plan(batch, L, dim, N, 1 if dtype == "bf16" else 0)
+    assert plan["tma"] == 1 and plan["kernel"] == 2  # the pipeline applies to this shape
+    inp, h0, dh, dy = _state_problem(shape, sum(shape) + 11, dtype, **FLAGS[0])
+    a = _gpu_state_grads(inp, dy, h0, dh)
+    assert ssm.ssm_set_knob(K.SSM_KNOB_PLAIN_LOADS, 1) == K.SSM_OK
+    try:
+        b = _gpu_state_grads(inp, dy, h0, dh)
+    finally:
+        ssm.ssm_set_knob(K.SSM_KNOB_PLAIN_LOADS, 0)
+    assert a.keys() == b.keys()
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
 def test_backward_pieces_chain_to_the_whole():
     """A sequence's gradients from two pieces: the second from the first's last
     state, the first with the second's dh0 as dh_last."""
