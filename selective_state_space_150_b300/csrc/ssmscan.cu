@@ -59,6 +59,11 @@ constexpr int kMaxStages = 8;  // deepest TMA ring
 constexpr int kMaxSegments = 64;   // time segments of one call
 constexpr int kMinSegChunks = 8;   // shortest automatic segment, in chunks
 constexpr int kMinSegments = 8;    // fewest automatic segments once a split pays
+// Shortest sequences (steps) worth an automatic split: with more than half of
+// the SMs idle, and with up to about one block per SM (where the split's extra
+// occupancy only just pays for its summary pass and second launch).
+constexpr int64_t kMinSplitSteps = 1024;
+constexpr int64_t kMinSplitStepsDense = 4096;
 constexpr int kMaxConvK = 4;       // longest causal convolution of the prologue
 constexpr int kConvHalo = kMaxConvK - 1;  // rows before a chunk that it reads
 constexpr size_t kMaxSmem = 227 * 1024;  // opt-in shared memory per block on sm_103
@@ -2450,13 +2455,19 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
     // wave, cut the sequence into segments: as many as fill one wave, and at
     // least kMinSegments (the summary pass then has enough blocks too and the
     // main pass's last wave is small), each segment at least kMinSegChunks
-    // chunks long.
+    // chunks long.  The split costs a summary pass over all but the last
+    // segment (about 0.6 of a main pass per step) and a second launch, so it
+    // needs a sequence of at least kMinSplitSteps when more than half of the
+    // SMs would be idle, and kMinSplitStepsDense when the blocks already come
+    // near one per SM (measured crossovers on the Mamba layer shapes).
     const int64_t nchunks = (L + pl.TC - 1) / pl.TC;
     {
         const int64_t by_smem = int64_t((228 * 1024) / (pl.smem + 1024));
         const int64_t cap = std::min<int64_t>(by_smem, 2048 / pl.NT) * 148;
         int64_t ns = 1;
-        if (pl.grid > 0 && 2 * pl.grid <= cap) ns = std::max<int64_t>(kMinSegments, cap / pl.grid);
+        const int64_t min_steps = 2 * pl.grid <= 148 ? kMinSplitSteps : kMinSplitStepsDense;
+        if (pl.grid > 0 && 2 * pl.grid <= cap && L >= min_steps)
+            ns = std::max<int64_t>(kMinSegments, cap / pl.grid);
         ns = std::min<int64_t>(ns, kMaxSegments);
         ns = std::min<int64_t>(ns, nchunks / kMinSegChunks);
         const int fseg = g_force_segments.load();
