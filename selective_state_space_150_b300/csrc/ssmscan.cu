@@ -559,13 +559,55 @@ __device__ __forceinline__ void scan_chunk(const float2* __restrict__ dd,
 #pragma unroll 1
     for (int t0 = 0; t0 < TC; t0 += SB) {
         float pv[SB];
+        if constexpr (ZK == 0 && NPT == 4 && NP == 16 && DT == 32 && SB % 4 == 0) {
+            // Four state groups of four states over one 32-channel tile: groups
+            // of four steps, the group's loads, decays and inputs first, then
+            // its four state updates and readouts in order (the same
+            // arithmetic as scan_step; 158.0 vs 160.2 us on the Mamba-130M
+            // layer shape, same bits; blocks of several channel tiles keep the
+            // per-step form, which needs fewer registers).
 #pragma unroll
-        for (int i = 0; i < SB; ++i) {
-            const int t = t0 + i;
-            float bb[NPT], cc[NPT];
-            ld_states<NPT>(Bs + t * NP, bb);
-            ld_states<NPT>(Cs + t * NP, cc);
-            pv[i] = scan_step_any<NPT, true, ZK>(dd[t * DT], bb, cc, a2, ia, h);
+            for (int g0 = 0; g0 < SB; g0 += 4) {
+                float2 e[4][2], w[4][2];
+                float cc[4][NPT];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = t0 + g0 + i;
+                    const float2 v = dd[t * DT];
+                    float bb[NPT];
+                    ld_states<NPT>(Bs + t * NP, bb);
+                    ld_states<NPT>(Cs + t * NP, cc[i]);
+                    const float2 vx = make_float2(v.x, v.x), vy = make_float2(v.y, v.y);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float2 x = __fmul2_rn(vx, make_float2(a2[2 * j], a2[2 * j + 1]));
+                        e[i][j] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                        w[i][j] = __fmul2_rn(vy, make_float2(bb[2 * j], bb[2 * j + 1]));
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float2 hh =
+                            __ffma2_rn(e[i][j], make_float2(h[2 * j], h[2 * j + 1]), w[i][j]);
+                        h[2 * j] = hh.x;
+                        h[2 * j + 1] = hh.y;
+                        acc = __ffma2_rn(make_float2(cc[i][2 * j], cc[i][2 * j + 1]), hh, acc);
+                    }
+                    pv[g0 + i] = acc.x + acc.y;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < SB; ++i) {
+                const int t = t0 + i;
+                float bb[NPT], cc[NPT];
+                ld_states<NPT>(Bs + t * NP, bb);
+                ld_states<NPT>(Cs + t * NP, cc);
+                pv[i] = scan_step_any<NPT, true, ZK>(dd[t * DT], bb, cc, a2, ia, h);
+            }
         }
 #pragma unroll
         for (int i = 0; i < SB; ++i) part[(t0 + i) * DT] = pv[i];
