@@ -2106,8 +2106,39 @@ __global__ void __launch_bounds__(WS * 32, 3) ssm_bwd_kernel(const BwdParams q) 
             for (int j = 0; j < NPT; ++j) hc[j] = hp[j];
         };
         if (tv == kBwdTC) {
+            // groups of four steps: their decays and inputs first, then the
+            // four state updates in order (the arithmetic of step(); 990 ->
+            // 980 us on the Mamba-130M layer, same bits)
 #pragma unroll
-            for (int i = 0; i < kBwdTC; ++i) fwd_keep(i);
+            for (int g0 = 0; g0 < kBwdTC; g0 += 4) {
+                float2 e[4][NPT / 2], w[4][NPT / 2];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int i = g0 + k;
+                    const float dt = s_dt[i * 32 + lane];
+                    const float du_ = dt * s_x[i * 32 + lane];
+                    const float* const bb = s_B + i * NP + sg * NPT;
+                    const float2 dt2 = make_float2(dt, dt), du2 = make_float2(du_, du_);
+#pragma unroll
+                    for (int j = 0; j < NPT; j += 2) {
+                        const float2 xx = __fmul2_rn(dt2, make_float2(a2[j], a2[j + 1]));
+                        e[k][j / 2] = make_float2(ex2_approx(xx.x), ex2_approx(xx.y));
+                        w[k][j / 2] = __fmul2_rn(du2, make_float2(bb[j], bb[j + 1]));
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                    for (int j = 0; j < NPT; j += 2) {
+                        const float2 hh =
+                            __ffma2_rn(e[k][j / 2], make_float2(h[j], h[j + 1]), w[k][j / 2]);
+                        h[j] = hh.x;
+                        h[j + 1] = hh.y;
+                    }
+                    *reinterpret_cast<float4*>(myh + ((g0 + k) * 32 + lane) * NPT) =
+                        make_float4(h[0], h[1], h[2], h[3]);
+                }
+            }
             __syncwarp();
             float hc[NPT];
 #pragma unroll
