@@ -59,6 +59,8 @@ constexpr int kMaxStages = 8;  // deepest TMA ring
 constexpr int kMaxSegments = 64;   // time segments of one call
 constexpr int kMinSegChunks = 8;   // shortest automatic segment, in chunks
 constexpr int kMinSegments = 8;    // fewest automatic segments once a split pays
+constexpr int kMinSegmentsDense = 12;  // the same near one block per SM (measured best of
+                                       // 6 .. 32 on 160 blocks)
 // Shortest sequences (steps) worth an automatic split: with more than half of
 // the SMs idle, and with up to about one block per SM (where the split's extra
 // occupancy only just pays for its summary pass and second launch).
@@ -2540,7 +2542,8 @@ Plan make_plan(int64_t batch, int64_t L, int64_t dim, int64_t N, const void* u, 
         int64_t ns = 1;
         const int64_t min_steps = 2 * pl.grid <= 148 ? kMinSplitSteps : kMinSplitStepsDense;
         if (pl.grid > 0 && 2 * pl.grid <= cap && L >= min_steps)
-            ns = std::max<int64_t>(kMinSegments, cap / pl.grid);
+            ns = std::max<int64_t>(2 * pl.grid <= 148 ? kMinSegments : kMinSegmentsDense,
+                                   cap / pl.grid);
         ns = std::min<int64_t>(ns, kMaxSegments);
         ns = std::min<int64_t>(ns, nchunks / kMinSegChunks);
         const int fseg = g_force_segments.load();
