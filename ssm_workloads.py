@@ -78,6 +78,10 @@ WORKLOADS: Dict[str, Workload] = {
     "mamba2p8b_bf16": Workload("mamba2p8b_bf16", 4, 8192, 5120, 16, "bf16",
                                softplus=True, delta_bias=True, gate=True, skip=True,
                                delta_kind="normal_raw"),
+    # the Mamba-130M layer shape with the SiLU(z) gate off (no z tensor)
+    "mamba130m_bf16_nogate": Workload("mamba130m_bf16_nogate", 8, 2048, 1536, 16, "bf16",
+                                      softplus=True, delta_bias=True, gate=False, skip=True,
+                                      delta_kind="normal_raw"),
 }
 LONGCTX_LS = (2048, 8192, 32768, 131072)
 for _L in LONGCTX_LS:

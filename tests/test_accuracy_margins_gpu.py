@@ -48,7 +48,7 @@ def test_small_workloads_every_element(name):
     record(name, wl.dtype, TOL["f32"], y=rel_err(y, yr), h_last=rel_err(h, hr))
 
 
-@pytest.mark.parametrize("name", ["mamba130m_bf16", "mamba2p8b_bf16"] +
+@pytest.mark.parametrize("name", ["mamba130m_bf16", "mamba130m_bf16_nogate", "mamba2p8b_bf16"] +
                          [f"longctx_L{L}" for L in W.LONGCTX_LS])
 def test_large_workloads_sampled(name):
     wl = W.WORKLOADS[name]
