@@ -134,6 +134,16 @@ def test_time_split_only_where_channels_leave_the_gpu_idle():
     assert ssm.ssm_scan_plan(1, 131072, 5120, 16, 1)["segments"] > 1
 
 
+def test_time_split_needs_a_sequence_that_repays_the_summary_pass():
+    seg = lambda *shape: ssm.ssm_scan_plan(*shape, 1)["segments"]
+    # two blocks, most SMs idle: split from 1024 steps on
+    assert seg(1, 256, 64, 16) == 1 and seg(1, 512, 64, 16) == 1
+    assert seg(1, 1024, 64, 16) > 1
+    # 160 blocks, about one per SM: one pass below 4096 steps, then at least 12 segments
+    assert seg(1, 2048, 5120, 16) == 1 and seg(1, 4095, 5120, 16) == 1
+    assert seg(1, 4096, 5120, 16) >= 12 and seg(1, 131072, 5120, 16) >= 12
+
+
 @pytest.mark.parametrize("forced,L,expect", [(5, 1000, 5), (64, 100, 4), (3, 32, 1), (1, 5000, 1)])
 def test_forced_segments_are_capped_by_chunks(forced, L, expect):
     K = ssmscan
